@@ -1,0 +1,161 @@
+"""CPU oracle for the FP8 (e4m3) block-scaled linear layer.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product package (``fp8_block_scaled_18_b300``) never imports it, and the two
+share no code: the oracle is the plain C in ``oracle.c`` (see its header for
+the passages each function follows), wrapped here with numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import numpy as np
+
+from . import build as _build
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_lock = threading.Lock()
+_libs: dict[int, ctypes.CDLL] = {}
+
+
+def load(mutant: int = 0) -> ctypes.CDLL:
+    """Build (if needed) and load the oracle library; mutant>0 loads a copy
+    with a deliberately planted mistake (used only by the mutant tests)."""
+    with _lock:
+        if mutant in _libs:
+            return _libs[mutant]
+        lib = ctypes.CDLL(_build.build(mutant))
+        lib.orc_e4m3_decode.restype = ctypes.c_double
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_e4m3_encode_search.restype = ctypes.c_uint8
+        lib.orc_e4m3_encode_search.argtypes = [ctypes.c_float]
+        lib.orc_f32_to_bf16_rne.restype = ctypes.c_uint16
+        lib.orc_f32_to_bf16_rne.argtypes = [ctypes.c_float]
+        for name, args in {
+            "orc_e4m3_encode_array": [_P, _I64, _P],
+            "orc_e4m3_encode_search_array": [_P, _I64, _P],
+            "orc_act_quant": [_P, _I64, _I64, _I64, _P, _I64, _P, _I64],
+            "orc_weight_quant": [_P, _I64, _I64, _P, _P],
+            "orc_weight_dequant": [_P, _P, _I64, _I64, _P],
+            "orc_gemm_rows": [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P],
+            "orc_grouped_gemm_rows": [_P, _I64, _P, _I64, _P, _P, _P, ctypes.c_int32,
+                                      _I64, _I64, _P, _I64, _P, _P],
+        }.items():
+            fn = getattr(lib, name)
+            fn.restype = None
+            fn.argtypes = args
+        lib.orc_mutant_id.restype = ctypes.c_int
+        _libs[mutant] = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+class Oracle:
+    """numpy front end of one oracle build (mutant=0 is the real one)."""
+
+    def __init__(self, mutant: int = 0):
+        self.lib = load(mutant)
+        self.mutant = mutant
+
+    # -- codec -----------------------------------------------------------
+    def e4m3_decode(self, codes) -> np.ndarray:
+        codes = np.asarray(codes, dtype=np.uint8)
+        return np.array([self.lib.orc_e4m3_decode(int(c)) for c in codes.ravel()],
+                        dtype=np.float64).reshape(codes.shape)
+
+    def e4m3_encode(self, v) -> np.ndarray:
+        v = np.ascontiguousarray(v, dtype=np.float32)
+        out = np.empty(v.shape, dtype=np.uint8)
+        self.lib.orc_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+        return out
+
+    def e4m3_encode_search(self, v) -> np.ndarray:
+        v = np.ascontiguousarray(v, dtype=np.float32)
+        out = np.empty(v.shape, dtype=np.uint8)
+        self.lib.orc_e4m3_encode_search_array(_ptr(v), v.size, _ptr(out))
+        return out
+
+    def bf16_rne(self, v) -> np.ndarray:
+        v = np.asarray(v, dtype=np.float32)
+        return np.array([self.lib.orc_f32_to_bf16_rne(float(x)) for x in v.ravel()],
+                        dtype=np.uint16).reshape(v.shape)
+
+    # -- quantisers --------------------------------------------------------
+    def act_quant(self, x_bits: np.ndarray, lds: int | None = None):
+        """x_bits: uint16 bf16 bit patterns [M, K].  Returns (xq [M,K] u8,
+        sx [M, lds] f32); padding columns of sx (>= K/128) are left 0."""
+        x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        M, K = x_bits.shape
+        kb = K // 128
+        lds = kb if lds is None else lds
+        xq = np.zeros((M, K), dtype=np.uint8)
+        sx = np.zeros((M, lds), dtype=np.float32)
+        self.lib.orc_act_quant(_ptr(x_bits), M, K, K, _ptr(xq), K, _ptr(sx), lds)
+        return xq, sx
+
+    def weight_quant(self, w_bits: np.ndarray):
+        w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+        N, K = w_bits.shape
+        wq = np.zeros((N, K), dtype=np.uint8)
+        sw = np.zeros(((N + 127) // 128, K // 128), dtype=np.float32)
+        self.lib.orc_weight_quant(_ptr(w_bits), N, K, _ptr(wq), _ptr(sw))
+        return wq, sw
+
+    def weight_dequant(self, wq: np.ndarray, sw: np.ndarray) -> np.ndarray:
+        wq = np.ascontiguousarray(wq, dtype=np.uint8)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        N, K = wq.shape
+        assert sw.shape == ((N + 127) // 128, K // 128)
+        w = np.zeros((N, K), dtype=np.uint16)
+        self.lib.orc_weight_dequant(_ptr(wq), _ptr(sw), N, K, _ptr(w))
+        return w
+
+    # -- gemm --------------------------------------------------------------
+    def gemm(self, xq, sx, wq, sw, rows=None):
+        """Returns (y_ref fp64 [len(rows), N], L fp64 [len(rows), N])."""
+        xq = np.ascontiguousarray(xq, dtype=np.uint8)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        wq = np.ascontiguousarray(wq, dtype=np.uint8)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        M, K = xq.shape
+        N = wq.shape[0]
+        assert wq.shape[1] == K and sw.shape == ((N + 127) // 128, K // 128)
+        assert sx.shape[0] == M and sx.shape[1] >= K // 128
+        rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        y = np.zeros((rows.size, N), dtype=np.float64)
+        L = np.zeros((rows.size, N), dtype=np.float64)
+        self.lib.orc_gemm_rows(_ptr(xq), K, _ptr(sx), sx.shape[1], _ptr(wq), _ptr(sw),
+                               N, K, _ptr(rows), rows.size, _ptr(y), _ptr(L))
+        return y, L
+
+    def grouped_gemm(self, xq, sx, wq, sw, offsets, rows=None):
+        """wq: [G, N, K] u8, sw: [G, ceil(N/128), K/128], offsets int32 [G+1]."""
+        xq = np.ascontiguousarray(xq, dtype=np.uint8)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        wq = np.ascontiguousarray(wq, dtype=np.uint8)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+        T, K = xq.shape
+        G, N, _ = wq.shape
+        assert sw.shape == (G, (N + 127) // 128, K // 128) and offsets.size == G + 1
+        rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        y = np.zeros((rows.size, N), dtype=np.float64)
+        L = np.zeros((rows.size, N), dtype=np.float64)
+        self.lib.orc_grouped_gemm_rows(_ptr(xq), K, _ptr(sx), sx.shape[1], _ptr(wq), _ptr(sw),
+                                       _ptr(offsets), G, N, K, _ptr(rows), rows.size,
+                                       _ptr(y), _ptr(L))
+        return y, L
+
+
+def gemm_tolerance(y_ref: np.ndarray, L: np.ndarray) -> np.ndarray:
+    """Per-element GEMM acceptance bound: 2^-8 |y_ref| + 1e-4 L."""
+    return np.ldexp(np.abs(y_ref), -8) + 1e-4 * L

@@ -1,0 +1,331 @@
+/*
+ * oracle.c -- plain, slow CPU statement of the FP8 (e4m3) block-scaled linear
+ * layer.  TEST INFRASTRUCTURE ONLY: tests/, __graft_entry__.smoke() and the
+ * bench's CPU-baseline / reference legs may load it; the product library never
+ * does, and this file shares no code, header or table with the CUDA path.
+ *
+ * Sources (pages on DeepSeek-V3):
+ *   [hub/FP8]   "DeepSeek-V3" repository overview (pomoai hub), section
+ *               "FP8 混合精度训练：首次在 671B 模型上验证": 128x128 weight blocks
+ *               with one fp32 scale each (weight_scale_inv), activations
+ *               quantized per token per 128 channels, float8 e4m3, and the
+ *               linear() excerpt: act_quant -> fp8_gemm -> (+bias), with
+ *               weight_dequant as the bf16 branch.
+ *   [blog/FP8]  88811315.cn post on DeepSeek v3, Float8 paragraph: E4M3 only,
+ *               fp32 accumulation at a fixed interval of FP8 multiply-adds.
+ *   [qd/FP8]    qdgithub overview, section "FP8 量化：存储与计算的平衡":
+ *               blockwise FP8 compute, dequantisation on CUDA cores.
+ *   E4M3 itself is the OCP 8-bit floating point format "E4M3" (bias 7, no
+ *   infinities, S.1111.111 = NaN, largest finite 448); the pages only say
+ *   "float8 e4m3".
+ *
+ * Readings where the pages are silent (each also listed in the design doc):
+ *   R1 e4m3 = OCP E4M3 ("fn"): saturating encode, max 448.
+ *   R2 scale s = amax / 448 in fp32 with IEEE round-to-nearest division, and
+ *      the stored scale is the dequantisation multiplier (w ~= dec(q) * s).
+ *   R3 the value encoded is the fp32 quotient RN32(x / s) (not x * (1/s)).
+ *   R4 an all-zero group/block has s = 0 and codes +-0 (sign of the input).
+ *   R5 encode = round to nearest, ties to even mantissa, any |v| > 448
+ *      (including +-Inf) saturates to +-448, NaN -> 0x7F, sign kept on zero.
+ *   R6 the ragged last weight row-block takes its amax over valid rows only.
+ *   R7 gemm: per 128-wide K chunk kb the exact partial sum
+ *      B_kb = sum_k dec(xq) dec(wq) is scaled by sx[m,kb] * sw[n/128,kb]
+ *      and promoted into the running sum; output rounded to bf16 only for
+ *      reporting (the GPU result is compared against the fp64 value).
+ *
+ * Compiled with: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off
+ *                -fno-fast-math  (see oracle/build.py)
+ * so that every float operation below is one IEEE binary32 operation.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_BLOCK 128          /* [hub/FP8]: 128x128 weight blocks, 1x128 activation groups */
+#define ORC_E4M3_MAX 448.0f    /* OCP E4M3 largest finite magnitude (S.1111.110) */
+
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0           /* >0 plants a deliberate mistake (tests/test_oracle_mutants.py) */
+#endif
+
+/* ------------------------------------------------------------------ */
+/* bf16 <-> fp32                                                       */
+/* ------------------------------------------------------------------ */
+
+/* bf16 is the top half of an fp32 bit pattern, so widening is exact. */
+float orc_bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* fp32 -> bf16, round to nearest, ties to even (on the dropped 16 bits). */
+uint16_t orc_f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) /* NaN: keep sign, quiet */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lower = u & 0xFFFFu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u; /* carries into the exponent correctly, Inf on overflow */
+    return (uint16_t)upper;
+}
+
+/* ------------------------------------------------------------------ */
+/* E4M3 codec                                                          */
+/* ------------------------------------------------------------------ */
+
+/* Decode one code: sign bit 7, exponent bits 6..3 (bias 7), mantissa 2..0.
+ * e = 0 is subnormal: m/8 * 2^-6.  S.1111.111 is NaN; there is no Inf. */
+double orc_e4m3_decode(uint8_t c) {
+    int s = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* Encode fp32 -> E4M3 by integer arithmetic on the fp32 bit pattern (R5).
+ * The step (quantum) of E4M3 at |v| is 2^(E-3) for a normal E4M3 result with
+ * unbiased exponent E >= -6, and 2^-9 below 2^-6 (subnormals). */
+uint8_t orc_e4m3_encode(float v) {
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u)
+        return 0x7F;                 /* NaN */
+    if (a >= 0x7F800000u)
+        return sign | 0x7E;          /* +-Inf saturates */
+    if (a < 0x00800000u)
+        return sign;                 /* fp32 zero / subnormal: far below 2^-10 */
+
+    int E = (int)(a >> 23) - 127;                /* |v| = sig * 2^(E-23) */
+    uint32_t sig = (a & 0x7FFFFFu) | 0x800000u;  /* 24-bit significand */
+    int qexp = (E < -6 ? -6 : E) - 3;            /* exponent of the E4M3 step */
+    int shift = qexp - (E - 23);                 /* >= 20 */
+    uint32_t n;
+    if (shift >= 32) {
+        n = 0;                                   /* |v| < 2^-33: rounds to 0 */
+    } else {
+        n = sig >> shift;
+        uint32_t rem = sig & ((1u << shift) - 1u);
+        uint32_t half = 1u << (shift - 1);
+#if ORC_MUTANT == 3
+        if (rem >= half) /* mutant: ties away from zero */
+            n += 1;
+#else
+        if (rem > half || (rem == half && (n & 1u)))
+            n += 1;                              /* ties to even */
+#endif
+    }
+    if (n == 0)
+        return sign;
+    if (n == 16) {                               /* rounded up into the next binade */
+        n = 8;
+        qexp += 1;
+    }
+    if (qexp == -9 && n < 8)                     /* subnormal: m/8 * 2^-6 */
+        return sign | (uint8_t)n;
+    int ebits = qexp + 10;                       /* value = (n/8) * 2^(qexp+3), n in [8,16) */
+    int mbits = (int)n - 8;
+    if (ebits > 15 || (ebits == 15 && mbits == 7))
+        return sign | 0x7E;                      /* beyond 448: saturate */
+    return sign | (uint8_t)((ebits << 3) | mbits);
+}
+
+/* Second, independent encoder: exhaustive nearest search over the 127
+ * non-negative finite codes, ties to the even code.  Used only to cross-check
+ * orc_e4m3_encode in the tests. */
+uint8_t orc_e4m3_encode_search(float v) {
+    if (isnan(v))
+        return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int best = 0;
+    double bestd = a; /* distance to code 0 */
+    for (int c = 1; c <= 0x7E; c++) {
+        double d = fabs(orc_e4m3_decode((uint8_t)c) - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+void orc_e4m3_encode_array(const float* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; i++)
+        out[i] = orc_e4m3_encode(v[i]);
+}
+
+void orc_e4m3_encode_search_array(const float* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; i++)
+        out[i] = orc_e4m3_encode_search(v[i]);
+}
+
+/* ------------------------------------------------------------------ */
+/* Quantisers                                                          */
+/* ------------------------------------------------------------------ */
+
+/* The scale of a group / block from its amax (R2). */
+static float orc_scale_from_amax(float amax) {
+#if ORC_MUTANT == 1
+    return amax / 447.0f; /* mutant: wrong e4m3 maximum */
+#else
+    return amax / ORC_E4M3_MAX;
+#endif
+}
+
+/* One element: R3 + R4. */
+static uint8_t orc_quantize_one(float x, float amax, float s) {
+    if (amax == 0.0f)
+        return signbit(x) ? 0x80 : 0x00;
+#if ORC_MUTANT == 2
+    return orc_e4m3_encode(x * (ORC_E4M3_MAX / amax)); /* mutant: reciprocal multiply */
+#else
+    return orc_e4m3_encode(x / s);
+#endif
+}
+
+/* act_quant [hub/FP8]: per row m and per group g of 128 channels,
+ * amax = max |x|, s = amax/448, q = e4m3(x/s).
+ * x: bf16 bits [M, K] with row stride ldx; xq: [M, K] with row stride ldq;
+ * sx: fp32 [M, lds] (group g of row m at sx[m*lds + g]).  K % 128 == 0. */
+void orc_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                   uint8_t* xq, int64_t ldq, float* sx, int64_t lds) {
+    int64_t G = K / ORC_BLOCK;
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t g = 0; g < G; g++) {
+            const uint16_t* xg = x + m * ldx + g * ORC_BLOCK;
+            float amax = 0.0f;
+            for (int k = 0; k < ORC_BLOCK; k++)
+                amax = fmaxf(amax, fabsf(orc_bf16_to_f32(xg[k])));
+            float s = orc_scale_from_amax(amax);
+            for (int k = 0; k < ORC_BLOCK; k++)
+                xq[m * ldq + g * ORC_BLOCK + k] = orc_quantize_one(orc_bf16_to_f32(xg[k]), amax, s);
+            sx[m * lds + g] = s;
+        }
+    }
+}
+
+/* weight_quant [hub/FP8]: per 128x128 block (nb, kb) of w [N, K] (row-major,
+ * row stride K), amax over the block's valid rows (R6), s = amax/448,
+ * q = e4m3(w/s).  sw: fp32 [ceil(N/128), K/128] row-major. */
+void orc_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw) {
+    int64_t NB = (N + ORC_BLOCK - 1) / ORC_BLOCK, KB = K / ORC_BLOCK;
+    for (int64_t nb = 0; nb < NB; nb++) {
+        int64_t n_end = (nb + 1) * ORC_BLOCK < N ? (nb + 1) * ORC_BLOCK : N;
+        for (int64_t kb = 0; kb < KB; kb++) {
+            float amax = 0.0f;
+            for (int64_t n = nb * ORC_BLOCK; n < n_end; n++)
+                for (int64_t k = kb * ORC_BLOCK; k < (kb + 1) * ORC_BLOCK; k++)
+                    amax = fmaxf(amax, fabsf(orc_bf16_to_f32(w[n * K + k])));
+            float s = orc_scale_from_amax(amax);
+            for (int64_t n = nb * ORC_BLOCK; n < n_end; n++)
+                for (int64_t k = kb * ORC_BLOCK; k < (kb + 1) * ORC_BLOCK; k++)
+                    wq[n * K + k] = orc_quantize_one(orc_bf16_to_f32(w[n * K + k]), amax, s);
+            sw[nb * KB + kb] = s;
+        }
+    }
+}
+
+/* weight_dequant [hub/FP8] (the bf16 branch of linear(), and the FP8->BF16
+ * checkpoint cast): w = bf16_rne(fp32(dec(q)) * s_block), one fp32 multiply. */
+void orc_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w) {
+    int64_t KB = K / ORC_BLOCK;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++) {
+            float q = (float)orc_e4m3_decode(wq[n * K + k]); /* exact in fp32 */
+            float s = sw[(n / ORC_BLOCK) * KB + k / ORC_BLOCK];
+            w[n * K + k] = orc_f32_to_bf16_rne(q * s);
+        }
+}
+
+/* ------------------------------------------------------------------ */
+/* GEMM                                                                */
+/* ------------------------------------------------------------------ */
+
+/* fp8_gemm [hub/FP8] with per-chunk promotion [blog/FP8], R7:
+ *   y[m,n] = sum_kb (sx[m,kb] * sw[n/128,kb]) * B_kb[m,n]
+ *   B_kb[m,n] = sum_{k in chunk kb} dec(xq[m,k]) * dec(wq[n,k])
+ * All in fp64.  Each product of two e4m3 values has <= 8 significant bits and
+ * lies in [2^-18, 2^18); 128 of them sum exactly in fp64, and the scale
+ * product of two fp32 numbers is exact in fp64.  Also returns
+ *   L[m,n] = sum_k |dec(xq[m,k]) sx[m,k/128]| * |dec(wq[n,k]) sw[n/128,k/128]|
+ * used by the error bound.  Only the rows listed in `rows` (nrows of them)
+ * are computed; y and L are [nrows, N] row-major. */
+void orc_gemm_rows(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds,
+                   const uint8_t* wq, const float* sw,
+                   int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
+                   double* y, double* L) {
+    int64_t KB = K / ORC_BLOCK;
+    double* xd = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int64_t r = 0; r < nrows; r++) {
+        int64_t m = rows[r];
+        for (int64_t k = 0; k < K; k++)
+            xd[k] = orc_e4m3_decode(xq[m * ldq + k]);
+        for (int64_t n = 0; n < N; n++) {
+            const uint8_t* wrow = wq + n * K;
+            double acc = 0.0, lsum = 0.0;
+#if ORC_MUTANT == 5
+            int64_t kb_end = KB - 1; /* mutant: last K chunk dropped */
+#else
+            int64_t kb_end = KB;
+#endif
+            for (int64_t kb = 0; kb < kb_end; kb++) {
+                double b = 0.0, babs = 0.0;
+                for (int64_t k = kb * ORC_BLOCK; k < (kb + 1) * ORC_BLOCK; k++) {
+                    double p = xd[k] * orc_e4m3_decode(wrow[k]);
+                    b += p;
+                    babs += fabs(p);
+                }
+#if ORC_MUTANT == 4
+                double scale = (double)sx[m * lds + kb] * (double)sw[kb * ((N + 127) / 128) + n / ORC_BLOCK]; /* mutant: scale grid transposed */
+#else
+                double scale = (double)sx[m * lds + kb] * (double)sw[(n / ORC_BLOCK) * KB + kb];
+#endif
+                acc += scale * b;
+                lsum += fabs(scale) * babs;
+            }
+            y[r * N + n] = acc;
+            L[r * N + n] = lsum;
+        }
+    }
+    free(xd);
+}
+
+/* grouped_gemm: the same product per expert g over token rows
+ * offsets[g] .. offsets[g+1]-1 of xq/sx, with expert weights
+ * wq + g*N*K (row-major [N, K]) and scales sw + g*ceil(N/128)*(K/128).
+ * Computes the listed global rows (each must lie in some expert's range);
+ * rows outside every range are left untouched. */
+void orc_grouped_gemm_rows(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds,
+                           const uint8_t* wq, const float* sw, const int32_t* offsets, int32_t G,
+                           int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
+                           double* y, double* L) {
+    int64_t NB = (N + ORC_BLOCK - 1) / ORC_BLOCK, KB = K / ORC_BLOCK;
+    for (int64_t r = 0; r < nrows; r++) {
+        int64_t m = rows[r];
+        for (int32_t g = 0; g < G; g++) {
+            if (m >= offsets[g] && m < offsets[g + 1]) {
+                orc_gemm_rows(xq, ldq, sx, lds, wq + (int64_t)g * N * K, sw + (int64_t)g * NB * KB,
+                              N, K, &m, 1, y + r * N, L + r * N);
+                break;
+            }
+        }
+    }
+}
+
+int orc_mutant_id(void) { return ORC_MUTANT; }

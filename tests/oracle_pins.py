@@ -1,0 +1,416 @@
+"""Pins that tie the CPU oracle to facts fixed outside itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError on a
+mismatch.  tests/test_oracle_pins.py runs them on the real oracle;
+tests/test_oracle_mutants.py runs them on copies of the oracle with a planted
+mistake and requires every mistake to be caught by at least one pin.
+
+The expected values come from: exact rational arithmetic (fractions), closed
+forms that hold by construction (power-of-two scales, e4m3-representable
+operands), integer arithmetic, and independent libraries (ml_dtypes, numpy).
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import ml_dtypes
+import numpy as np
+
+from fp8_block_scaled_18_b300 import synth
+
+E4M3_MAX = 448
+
+# ---------------------------------------------------------------------------
+# exact helpers (independent of the oracle's C code)
+# ---------------------------------------------------------------------------
+
+
+def f32_round(fr: Fraction) -> float:
+    """Round an exact rational to the nearest binary32 value, ties to even."""
+    if fr == 0:
+        return 0.0
+    neg = fr < 0
+    a = -fr if neg else fr
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    assert Fraction(2) ** e <= a < Fraction(2) ** (e + 1)
+    e = max(e, -126)
+    scaled = a / Fraction(2) ** (e - 23)
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = Fraction(n) * Fraction(2) ** (e - 23)
+    if val >= Fraction(2) ** 128:
+        out = float("inf")
+    else:
+        out = float(val)  # exact: n has <= 24 bits
+    return -out if neg else out
+
+
+def e4m3_values() -> np.ndarray:
+    """All 254 finite e4m3 values indexed by code (NaN codes -> nan), from ml_dtypes."""
+    return np.arange(256, dtype=np.uint8).view(ml_dtypes.float8_e4m3fn).astype(np.float64)
+
+
+def e4m3_code_lib(v: np.ndarray) -> np.ndarray:
+    """Library encode with saturation: clip to +-448 then ml_dtypes RNE cast."""
+    v = np.clip(np.asarray(v, dtype=np.float32), -E4M3_MAX, E4M3_MAX)
+    return v.astype(ml_dtypes.float8_e4m3fn).view(np.uint8)
+
+
+def bf16_bits(v) -> np.ndarray:
+    return synth.to_bf16_bits(np.asarray(v, dtype=np.float32))
+
+
+def f32_of_bf16(bits) -> np.ndarray:
+    return synth.bf16_bits_to_f32(bits)
+
+
+def _pos_codes_with_max(rng, n, allow_sub=True):
+    """n positive-or-negative e4m3 codes with |max| == 448 (code 0x7E present)."""
+    lo = 0 if allow_sub else 0x08
+    mags = rng.integers(lo, 0x7E, size=n)            # 0 .. 447-ish, excludes NaN
+    signs = rng.integers(0, 2, size=n) * 0x80
+    codes = (mags | signs).astype(np.uint8)
+    codes[rng.integers(0, n)] = 0x7E | (0x80 if rng.integers(0, 2) else 0)
+    return codes
+
+
+# ---------------------------------------------------------------------------
+# codec
+# ---------------------------------------------------------------------------
+
+
+def pin_codec_midpoints(o):
+    pos = [c for c in range(0x7F)]
+    vals = e4m3_values()[pos]
+    mids, want = [], []
+    for i in range(len(pos) - 1):
+        mid = (vals[i] + vals[i + 1]) / 2
+        mids.append(mid)
+        want.append(pos[i] if pos[i] % 2 == 0 else pos[i + 1])
+    got = o.e4m3_encode(np.array(mids, dtype=np.float32))
+    assert np.array_equal(got, np.array(want, dtype=np.uint8)), "midpoint ties must go to the even code"
+
+
+# ---------------------------------------------------------------------------
+# act_quant
+# ---------------------------------------------------------------------------
+
+
+def pin_act_quant_rank1(o):
+    """x[m,k] = 2^a_m * c_k with each 128-group of c holding a +-448: then
+    s = 2^a_m exactly and the codes are c's codes exactly."""
+    rng = np.random.default_rng(11)
+    M, K = 24, 512
+    codes = np.concatenate([_pos_codes_with_max(rng, 128) for _ in range(K // 128)])
+    c = e4m3_values()[codes]
+    a = rng.integers(-20, 20, size=M)
+    x = np.ldexp(c[None, :], a[:, None])
+    xb = bf16_bits(x)
+    assert np.array_equal(f32_of_bf16(xb).astype(np.float64), x)  # exactly representable
+    xq, sx = o.act_quant(xb)
+    assert np.array_equal(sx, np.ldexp(np.ones((M, K // 128), np.float32), a[:, None]).astype(np.float32))
+    assert np.array_equal(xq, np.broadcast_to(codes, (M, K)))
+
+
+def _division_sensitive_groups(rng, n_groups):
+    """Groups [amax, x, x, ...] whose quotient x/s lies within a few fp32 ulps
+    of an e4m3 rounding boundary, where dividing and multiplying by a rounded
+    reciprocal can disagree.  Found by a numpy search (inputs only)."""
+    xs = f32_of_bf16(np.arange(0x3C00, 0x4400, dtype=np.uint16))  # bf16 in [2^-7, 2^8)
+    groups = []
+    tries = 0
+    while len(groups) < n_groups and tries < 4000:
+        tries += 1
+        amax = np.float32(f32_of_bf16(np.array([rng.integers(0x4000, 0x4300)], np.uint16))[0])
+        s = np.float32(amax / np.float32(448))
+        cand = xs[xs < amax]
+        q_div = cand / s
+        q_mul = cand * np.float32(np.float32(448) / amax)
+        diff = e4m3_code_lib(q_div) != e4m3_code_lib(q_mul)
+        if diff.any():
+            pick = cand[diff][:127]
+            g = np.full(128, pick[0], np.float32)
+            g[0] = amax
+            g[1:1 + pick.size] = pick
+            groups.append(g)
+    assert len(groups) == n_groups, "search for division-sensitive inputs failed"
+    return np.stack(groups)
+
+
+def pin_act_quant_division_exact(o):
+    """Brute force in exact rationals: s = RN32(amax/448), q = e4m3(RN32(x/s))."""
+    rng = np.random.default_rng(12)
+    rnd = rng.standard_normal((6, 128)).astype(np.float32) * np.float32(3)
+    rnd[2] *= np.float32(1e-30)                 # tiny values, fp32 subnormal quotients
+    rnd[3, :] = 0
+    rnd[3, 5] = -1.5                            # single nonzero
+    groups = np.concatenate([rnd, _division_sensitive_groups(rng, 6)])
+    xb = bf16_bits(groups).reshape(1, -1)
+    xq, sx = o.act_quant(xb)
+    xf = f32_of_bf16(xb).reshape(groups.shape)
+    for g in range(groups.shape[0]):
+        amax = max(Fraction(float(abs(v))) for v in xf[g])
+        s = f32_round(amax / 448)
+        assert sx[0, g] == np.float32(s), (g, sx[0, g], s)
+        want = []
+        for v in xf[g]:
+            if amax == 0:
+                want.append(0x80 if np.signbit(v) else 0)
+            else:
+                want.append(int(e4m3_code_lib(np.float32(f32_round(Fraction(float(v)) / Fraction(s))))))
+        got = xq[0, g * 128:(g + 1) * 128]
+        assert np.array_equal(got, np.array(want, np.uint8)), (g, np.nonzero(got != np.array(want))[0][:5])
+
+
+def pin_act_quant_invariants(o):
+    rng = np.random.default_rng(13)
+    M, K = 16, 1024
+    x = rng.standard_normal((M, K)).astype(np.float32) * np.float32(2.0)
+    x[3, 128:256] = 0.0                          # zero group
+    x[4, 256:384] = -0.0                         # negative-zero group
+    x[5, :128] = np.float32(1e-3) * x[5, :128]   # small group
+    xb = bf16_bits(x)
+    xq, sx = o.act_quant(xb)
+    xf = f32_of_bf16(xb)
+    dec = e4m3_values()[xq]
+    for m in range(M):
+        for g in range(K // 128):
+            sl = slice(g * 128, (g + 1) * 128)
+            grp, q, s = xf[m, sl], xq[m, sl], sx[m, g]
+            if not np.any(grp):
+                assert s == 0 and np.array_equal(q, np.where(np.signbit(grp), 0x80, 0).astype(np.uint8))
+                continue
+            assert s > 0 and (q & 0x7F).max() == 0x7E          # the amax element maps to 448
+            err = np.abs(grp.astype(np.float64) - dec[m, sl] * float(s))
+            bound = np.maximum(np.abs(grp) * 2.0 ** -4, float(s) * 2.0 ** -10)
+            assert np.all(err <= bound)
+            assert np.array_equal(q & 0x80, np.where(np.signbit(grp), 0x80, 0).astype(np.uint8))
+    # sign symmetry and power-of-two scaling
+    xq2, sx2 = o.act_quant(bf16_bits(-xf))
+    assert np.array_equal(sx2, sx) and np.array_equal(xq2 ^ 0x80, xq)
+    xq3, sx3 = o.act_quant(bf16_bits(xf * np.float32(2.0 ** 7)))
+    assert np.array_equal(sx3, sx * np.float32(2.0 ** 7)) and np.array_equal(xq3, xq)
+    # quantising gathered rows == gathering quantised rows
+    perm = rng.permutation(M)
+    xq4, sx4 = o.act_quant(xb[perm])
+    assert np.array_equal(xq4, xq[perm]) and np.array_equal(sx4, sx[perm])
+
+
+# ---------------------------------------------------------------------------
+# weight_quant / weight_dequant
+# ---------------------------------------------------------------------------
+
+
+def _block_closed_form(rng, N, K):
+    """w = 2^b[nb,kb] * d with each 128x128 block of d holding a +-448 in its
+    valid rows: s = 2^b and codes = d's codes, exactly."""
+    NB, KB = (N + 127) // 128, K // 128
+    codes = (rng.integers(0, 0x7E, size=(N, K)) | (rng.integers(0, 2, size=(N, K)) * 0x80)).astype(np.uint8)
+    b = rng.integers(-12, 6, size=(NB, KB))
+    for nb in range(NB):
+        for kb in range(KB):
+            r = rng.integers(nb * 128, min(N, nb * 128 + 128))
+            codes[r, kb * 128 + rng.integers(0, 128)] = 0x7E
+    scale = np.ldexp(np.ones((N, K)), np.repeat(np.repeat(b, 128, 0)[:N], 128, 1))
+    w = e4m3_values()[codes] * scale
+    return codes, b, w
+
+
+def pin_weight_quant_blocks(o):
+    rng = np.random.default_rng(14)
+    for N, K in ((256, 384), (576, 256), (130, 128)):
+        codes, b, w = _block_closed_form(rng, N, K)
+        wb = bf16_bits(w)
+        assert np.array_equal(f32_of_bf16(wb).astype(np.float64), w)
+        wq, sw = o.weight_quant(wb)
+        assert np.array_equal(sw, np.ldexp(np.ones(b.shape, np.float32), b).astype(np.float32)), (N, K)
+        assert np.array_equal(wq, codes), (N, K)
+
+
+def pin_weight_quant_identity(o):
+    """W = I (512x512): diagonal blocks s = RN32(1/448) with the diagonal at
+    code 0x7E; every other entry code 0 and off-diagonal blocks s = 0."""
+    w = bf16_bits(np.eye(512, dtype=np.float32))
+    wq, sw = o.weight_quant(w)
+    s_diag = np.float32(f32_round(Fraction(1, 448)))
+    assert np.array_equal(sw, np.where(np.eye(4, dtype=bool), s_diag, np.float32(0)))
+    assert np.array_equal(wq, np.where(np.eye(512, dtype=bool), 0x7E, 0).astype(np.uint8))
+
+
+def pin_weight_quant_ragged(o):
+    """N = 576: five row blocks; the last uses its 64 valid rows, which gives
+    the same codes and scales as zero-padding the weight to 640 rows."""
+    rng = np.random.default_rng(15)
+    w = bf16_bits(rng.standard_normal((576, 256)).astype(np.float32) * np.float32(0.02))
+    wq, sw = o.weight_quant(w)
+    assert sw.shape == (5, 2)
+    wpad = np.zeros((640, 256), np.uint16)
+    wpad[:576] = w
+    wq2, sw2 = o.weight_quant(wpad)
+    assert np.array_equal(sw, sw2) and np.array_equal(wq, wq2[:576]) and not np.any(wq2[576:])
+    wf = f32_of_bf16(w)
+    assert sw[4, 1] == np.float32(f32_round(Fraction(float(np.abs(wf[512:, 128:]).max())) / 448))
+
+
+def pin_weight_dequant(o):
+    rng = np.random.default_rng(16)
+    codes, b, w = _block_closed_form(rng, 256, 256)
+    sw = np.ldexp(np.ones(b.shape, np.float32), b).astype(np.float32)
+    back = o.weight_dequant(codes, sw)
+    assert np.array_equal(f32_of_bf16(back).astype(np.float64), w)   # exact for power-of-two scales
+    # general scales: one fp32 rounding of the exact product, then bf16 RNE
+    sw2 = (rng.uniform(0.5, 2.0, size=(2, 2)) * 1e-3).astype(np.float32)
+    back2 = o.weight_dequant(codes, sw2)
+    dec = e4m3_values()[codes]
+    s_full = np.repeat(np.repeat(sw2, 128, 0), 128, 1)
+    for (n, k) in zip(rng.integers(0, 256, 300), rng.integers(0, 256, 300)):
+        p = f32_round(Fraction(float(dec[n, k])) * Fraction(float(s_full[n, k])))
+        want = synth.to_bf16_bits(np.array([p], np.float32))[0]
+        assert back2[n, k] == want, (n, k)
+    # quantise -> dequantise stays within e4m3's relative step
+    wr = bf16_bits(rng.standard_normal((256, 256)).astype(np.float32) * np.float32(0.02))
+    wq, swr = o.weight_quant(wr)
+    wr2 = f32_of_bf16(o.weight_dequant(wq, swr)).astype(np.float64)
+    x = f32_of_bf16(wr).astype(np.float64)
+    s_full = np.repeat(np.repeat(swr, 128, 0), 128, 1).astype(np.float64)
+    assert np.all(np.abs(wr2 - x) <= np.maximum(np.abs(x) * (2.0 ** -4 + 2.0 ** -8), s_full * 2.0 ** -9))
+
+
+# ---------------------------------------------------------------------------
+# gemm
+# ---------------------------------------------------------------------------
+
+
+def _exact_gemm(xq, sx, wq, sw, m, n):
+    vals = e4m3_values()
+    K = xq.shape[1]
+    tot = Fraction(0)
+    for kb in range(K // 128):
+        bsum = Fraction(0)
+        for k in range(kb * 128, (kb + 1) * 128):
+            bsum += Fraction(float(vals[xq[m, k]])) * Fraction(float(vals[wq[n, k]]))
+        tot += Fraction(float(sx[m, kb])) * Fraction(float(sw[n // 128, kb])) * bsum
+    return tot
+
+
+def pin_gemm_bruteforce(o):
+    """Tiny shapes against exact rational arithmetic."""
+    rng = np.random.default_rng(17)
+    for (M, N, K) in ((3, 5, 128), (4, 130, 256), (2, 3, 384)):
+        xq = rng.integers(0, 0xFF, size=(M, K)).astype(np.uint8)
+        xq[(xq & 0x7F) == 0x7F] = 0x7E
+        wq = rng.integers(0, 0xFF, size=(N, K)).astype(np.uint8)
+        wq[(wq & 0x7F) == 0x7F] = 0x7E
+        sx = rng.uniform(1e-3, 1.0, size=(M, K // 128)).astype(np.float32)
+        sw = rng.uniform(1e-4, 1e-2, size=((N + 127) // 128, K // 128)).astype(np.float32)
+        y, L = o.gemm(xq, sx, wq, sw)
+        for m in range(M):
+            for n in list(range(min(N, 6))) + [N - 1]:
+                ex = _exact_gemm(xq, sx, wq, sw, m, n)
+                assert abs(Fraction(float(y[m, n])) - ex) <= Fraction(2) ** -45 * Fraction(float(L[m, n])) + Fraction(1, 10 ** 300), (M, N, K, m, n)
+
+
+def pin_gemm_rank1(o):
+    """Full path on closed-form inputs: x = 2^a_m c_k, w = 2^b_(n,kb) d_(n,k)
+    quantise losslessly, so y = sum_k 2^(a_m + b) c_k d_(n,k), in integers."""
+    rng = np.random.default_rng(18)
+    M, N, K = 8, 256, 384
+    ccodes = np.concatenate([_pos_codes_with_max(rng, 128) for _ in range(K // 128)])
+    a = rng.integers(-6, 6, size=M)
+    x = np.ldexp(e4m3_values()[ccodes][None, :], a[:, None])
+    dcodes, b, w = _block_closed_form(rng, N, K)
+    xq, sx = o.act_quant(bf16_bits(x))
+    wq, sw = o.weight_quant(bf16_bits(w))
+    y, L = o.gemm(xq, sx, wq, sw)
+    ci = (e4m3_values()[ccodes] * 512).astype(np.int64)          # e4m3 values are multiples of 2^-9
+    di = (e4m3_values()[dcodes] * 512).astype(np.int64)
+    for m in range(M):
+        for n in range(0, N, 17):
+            ex = Fraction(0)
+            for kb in range(K // 128):
+                sl = slice(kb * 128, (kb + 1) * 128)
+                ex += Fraction(int(np.dot(ci[sl], di[n, sl]))) * Fraction(2) ** int(a[m] + b[n // 128, kb] - 18)
+            assert Fraction(float(y[m, n])) == ex, (m, n)
+
+
+def pin_gemm_diag(o):
+    """W = diag(d) with e4m3 codes, power-of-two block scales:
+    y[m,n] = dec(xq[m,n]) sx[m,n/128] dec(d_n) sw[n/128,n/128], exactly."""
+    rng = np.random.default_rng(19)
+    M, K = 5, 256
+    xq = rng.integers(0, 0x7E, size=(M, K)).astype(np.uint8) | (rng.integers(0, 2, (M, K)) * 0x80).astype(np.uint8)
+    sx = rng.uniform(0.1, 10, size=(M, 2)).astype(np.float32)
+    d = rng.integers(0x30, 0x50, size=K).astype(np.uint8)
+    wq = np.zeros((K, K), np.uint8)
+    wq[np.arange(K), np.arange(K)] = d
+    sw = np.ldexp(np.ones((2, 2), np.float32), rng.integers(-3, 3, size=(2, 2))).astype(np.float32)
+    y, _ = o.gemm(xq, sx, wq, sw)
+    v = e4m3_values()
+    for m in range(M):
+        for n in range(K):
+            want = Fraction(float(v[xq[m, n]])) * Fraction(float(sx[m, n // 128])) * \
+                Fraction(float(v[d[n]])) * Fraction(float(sw[n // 128, n // 128]))
+            assert Fraction(float(y[m, n])) == want, (m, n)
+
+
+def pin_gemm_vs_dequant_matmul(o):
+    """The bf16 branch of linear(): dequantise both operands, one matmul."""
+    rng = np.random.default_rng(20)
+    case = synth.tiny(0)
+    xq, sx = o.act_quant(case.x)
+    wq, sw = o.weight_quant(case.w)
+    v = e4m3_values()
+    xd = v[xq] * np.repeat(sx.astype(np.float64), 128, 1)
+    wd = v[wq] * np.repeat(np.repeat(sw.astype(np.float64), 128, 0), 128, 1)[: wq.shape[0]]
+    ref = xd @ wd.T
+    y, L = o.gemm(xq, sx, wq, sw)
+    assert np.all(np.abs(y - ref) <= 1e-12 * L + 1e-300)
+    rows = rng.choice(xq.shape[0], 7, replace=False)
+    y2, _ = o.gemm(xq, sx, wq, sw, rows=rows)
+    assert np.array_equal(y2, y[rows])
+
+
+def pin_grouped(o):
+    """Grouped = the dense product per expert over its row range; empty
+    experts take no rows."""
+    rng = np.random.default_rng(21)
+    G, N, K = 5, 192, 256
+    counts = np.array([3, 0, 7, 1, 0])
+    off = synth.offsets_from_counts(counts)
+    T = int(off[-1])
+    xq = rng.integers(0, 0x7E, size=(T, K)).astype(np.uint8)
+    sx = rng.uniform(0.1, 1.0, size=(T, K // 128)).astype(np.float32)
+    wq = rng.integers(0, 0x7E, size=(G, N, K)).astype(np.uint8)
+    sw = rng.uniform(1e-3, 1e-2, size=(G, 2, K // 128)).astype(np.float32)
+    y, L = o.grouped_gemm(xq, sx, wq, sw, off)
+    for g in range(G):
+        r0, r1 = off[g], off[g + 1]
+        if r1 > r0:
+            yg, Lg = o.gemm(xq[r0:r1], sx[r0:r1], wq[g], sw[g])
+            assert np.array_equal(y[r0:r1], yg) and np.array_equal(L[r0:r1], Lg)
+    # one element against exact rationals
+    m, n = 5, 150
+    g = int(np.searchsorted(off, m, side="right") - 1)
+    ex = _exact_gemm(xq[off[g]:off[g + 1]], sx[off[g]:off[g + 1]], wq[g], sw[g], m - off[g], n)
+    assert abs(Fraction(float(y[m, n])) - ex) <= Fraction(2) ** -45 * Fraction(float(L[m, n]))
+
+
+ALL_PINS = [
+    pin_codec_midpoints,
+    pin_act_quant_rank1,
+    pin_act_quant_division_exact,
+    pin_act_quant_invariants,
+    pin_weight_quant_blocks,
+    pin_weight_quant_identity,
+    pin_weight_quant_ragged,
+    pin_weight_dequant,
+    pin_gemm_bruteforce,
+    pin_gemm_rank1,
+    pin_gemm_diag,
+    pin_gemm_vs_dequant_matmul,
+    pin_grouped,
+]

@@ -1,0 +1,25 @@
+"""Plant plausible mistakes in copies of the oracle (compiled with
+-DORC_MUTANT=k, CPU only) and require the pins to catch every one:
+  1 wrong e4m3 maximum in the scale (amax/447)
+  2 reciprocal multiply x*(448/amax) instead of x/s
+  3 ties rounded away from zero in the encoder
+  4 weight-scale grid read transposed
+  5 last K chunk dropped from the GEMM
+"""
+import pytest
+
+from oracle import Oracle
+from oracle_pins import ALL_PINS
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+def test_mutant_is_caught(mutant):
+    o = Oracle(mutant)
+    assert o.lib.orc_mutant_id() == mutant
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {mutant} passed every pin"
