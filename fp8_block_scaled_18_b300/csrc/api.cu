@@ -1,0 +1,169 @@
+// api.cu -- the C ABI declared in include/fp8bs.h: argument validation, then
+// one launch on the caller's stream.  Nothing here allocates device memory.
+#include "../../include/fp8bs.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+using namespace fp8bs;
+
+namespace {
+
+constexpr int64_t kMaxRows = (int64_t{1} << 31) - 1;   // TMA coordinates are int32
+constexpr int64_t kMaxGridY = 65535;
+constexpr int32_t kMaxGroups = 1024;                    // grouped GEMM: per-CTA tile table
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline fp8bs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
+
+inline fp8bs_status device(DeviceInfo* d) {
+    if (device_info(d) != cudaSuccess) return FP8BS_ERR_CUDA;
+    return FP8BS_OK;
+}
+
+inline cudaStream_t cs(fp8bs_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Shape checks common to the quantisers' K dimension.
+inline fp8bs_status check_k(int64_t K) {
+    if (K < 0) return FP8BS_ERR_INVALID_ARG;
+    if (K == 0 || K % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
+    if (K / 128 > (int64_t{1} << 31) - 1) return FP8BS_ERR_UNSUPPORTED;
+    return FP8BS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8bs_status fp8bs_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq,
+                             float* sx, int64_t lds, fp8bs_stream_t stream) {
+    if (M < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (M == 0) return FP8BS_OK;
+    if (!x || !xq || !sx) return FP8BS_ERR_INVALID_ARG;
+    if (ldx < K || ldq < K || lds < K / 128) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(sx) || ldx % 8 || ldq % 16 || lds % 4)
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_act_quant(x, M, K, ldx, xq, ldq, sx, lds, d, cs(stream)));
+}
+
+fp8bs_status fp8bs_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
+                                fp8bs_stream_t stream) {
+    if (N < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (N == 0) return FP8BS_OK;
+    if (!w || !wq || !sw) return FP8BS_ERR_INVALID_ARG;
+    if ((N + 127) / 128 > kMaxGridY) return FP8BS_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return FP8BS_ERR_MISALIGNED;
+    return from_cuda(launch_weight_quant(w, N, K, wq, sw, cs(stream)));
+}
+
+fp8bs_status fp8bs_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
+                                  fp8bs_stream_t stream) {
+    if (N < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (N == 0) return FP8BS_OK;
+    if (!w || !wq || !sw) return FP8BS_ERR_INVALID_ARG;
+    if ((N + 127) / 128 > kMaxGridY) return FP8BS_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return FP8BS_ERR_MISALIGNED;
+    return from_cuda(launch_weight_dequant(wq, sw, N, K, w, cs(stream)));
+}
+
+static fp8bs_status check_gemm_common(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* wq,
+                                      const float* sw, int64_t M, int64_t N, int64_t K, const uint16_t* y,
+                                      int64_t ldy) {
+    if (!xq || !sx || !wq || !sw || !y) return FP8BS_ERR_INVALID_ARG;
+    if (M > kMaxRows || N > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
+    if (lds < K / 128 || ldy < N) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(wq) || !aligned16(sx) || !aligned16(y) || lds % 4 || ldy % 8 ||
+        (reinterpret_cast<uintptr_t>(sw) & 3u))
+        return FP8BS_ERR_MISALIGNED;
+    return FP8BS_OK;
+}
+
+fp8bs_status fp8bs_gemm(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* wq, const float* sw,
+                        int64_t M, int64_t N, int64_t K, uint16_t* y, int64_t ldy, void* workspace,
+                        size_t ws_bytes, fp8bs_stream_t stream) {
+    if (M < 0 || N < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (M == 0 || N == 0) return FP8BS_OK;
+    if (fp8bs_status st = check_gemm_common(xq, sx, lds, wq, sw, M, N, K, y, ldy)) return st;
+    if (workspace && !aligned16(workspace)) return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    GemmArgs a{xq, sx, lds, wq, sw, M, N, K, y, ldy, nullptr, 0, workspace, workspace ? ws_bytes : 0};
+    return from_cuda(launch_gemm(a, d, cs(stream)));
+}
+
+size_t fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % 128) return 0;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess) return 0;
+    return gemm_workspace_size(M, N, K, d);
+}
+
+fp8bs_status fp8bs_grouped_gemm(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* wq,
+                                const float* sw, const int32_t* offsets_dev, int32_t G, int64_t total_M,
+                                int64_t N, int64_t K, uint16_t* y, int64_t ldy, fp8bs_stream_t stream) {
+    if (G < 0 || total_M < 0 || N < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (total_M == 0 || N == 0 || G == 0) return FP8BS_OK;
+    if (!offsets_dev) return FP8BS_ERR_INVALID_ARG;
+    if (G > kMaxGroups) return FP8BS_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(G) * N > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
+    if (fp8bs_status st = check_gemm_common(xq, sx, lds, wq, sw, total_M, N, K, y, ldy)) return st;
+    if (reinterpret_cast<uintptr_t>(offsets_dev) & 3u) return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    GemmArgs a{xq, sx, lds, wq, sw, total_M, N, K, y, ldy, offsets_dev, G, nullptr, 0};
+    return from_cuda(launch_gemm(a, d, cs(stream)));
+}
+
+fp8bs_status fp8bs_sync_status(fp8bs_stream_t stream) {
+    if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, d.err, sizeof(word), cudaMemcpyDeviceToHost, cs(stream)) != cudaSuccess)
+        return FP8BS_ERR_CUDA;
+    if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
+    if (word == 0) return FP8BS_OK;
+    if (cudaMemsetAsync(d.err, 0, sizeof(unsigned), cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
+    if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
+    return FP8BS_ERR_TIMEOUT;
+}
+
+const char* fp8bs_status_string(fp8bs_status status) {
+    switch (status) {
+        case FP8BS_OK: return "FP8BS_OK";
+        case FP8BS_ERR_INVALID_ARG: return "FP8BS_ERR_INVALID_ARG: null pointer or inconsistent size";
+        case FP8BS_ERR_UNSUPPORTED: return "FP8BS_ERR_UNSUPPORTED: K % 128 != 0 or size out of range";
+        case FP8BS_ERR_MISALIGNED: return "FP8BS_ERR_MISALIGNED: pointer or leading dimension not 16-byte aligned";
+        case FP8BS_ERR_CUDA: return "FP8BS_ERR_CUDA: CUDA runtime error";
+        case FP8BS_ERR_TIMEOUT: return "FP8BS_ERR_TIMEOUT: a kernel's bounded wait expired";
+    }
+    return "FP8BS: unknown status";
+}
+
+fp8bs_status fp8bs_e4m3_encode_f32(const float* v, int64_t n, uint8_t* q, fp8bs_stream_t stream) {
+    if (n < 0) return FP8BS_ERR_INVALID_ARG;
+    if (n == 0) return FP8BS_OK;
+    if (!v || !q) return FP8BS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(v) & 3u) return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_e4m3_encode(v, n, q, d, cs(stream)));
+}
+
+fp8bs_status fp8bs_debug_wait_timeout(uint64_t timeout_ns, fp8bs_stream_t stream) {
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull) return FP8BS_ERR_INVALID_ARG;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_wait_selftest(timeout_ns, d, cs(stream)));
+}
+
+int fp8bs_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,592 @@
+// gemm.cu -- block-scaled FP8 GEMM (dense and grouped) for sm_103a.
+//
+//   y[m,n] = bf16( sum_kb fp32(sx[m,kb] * sw[n/128,kb]) * P_kb[m,n] )
+//
+// ("DeepSeek-V3" repository overview, section "FP8 混合精度训练": fp8_gemm of
+// the per-token/128-channel quantised activations with the 128x128
+// block-quantised weights; fp32 promotion once per 128-wide K chunk after
+// four K=32 MMAs, after the Float8 paragraph of the 88811315.cn post and the
+// "FP8 量化" section of the qdgithub overview.)
+//
+// Design (one persistent CTA per SM, 384 threads, warp-specialised):
+//   warp 0      TMA producer: A (128 x 128 B) and B (BN x 128 B) tiles of one
+//               K chunk per pipeline stage, 128-byte swizzled, mbarrier
+//               completion by byte count.
+//   warp 1      TMEM owner and MMA issuer: per chunk, four
+//               tcgen05.mma.kind::f8f6f4 (M=128, N=BN, K=32) into one of two
+//               TMEM buffers of BN fp32 columns, then tcgen05.commit to free
+//               the smem stage and to publish the chunk.
+//   warps 4-11  promotion + epilogue: two warpgroups, each owning BN/2
+//               columns; thread = one row.  Per chunk: tcgen05.ld the raw
+//               chunk sum P_kb, acc += fp32(sx*sw) * P_kb in registers (one
+//               FFMA per element), release the TMEM buffer.  After the last
+//               chunk of a tile: round to bf16 and store (or store fp32
+//               partials for split-K).
+// The TMEM double buffer lets the tensor core run chunk kb+1 while the CUDA
+// cores promote chunk kb.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace {
+
+constexpr int BM = 128;           // tile rows (tokens) = TMEM lanes
+constexpr int BK = 128;           // K chunk = one scale block = 4 MMAs of K=32
+constexpr int UMMA_K = 32;
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;      // first promotion/epilogue warp
+constexpr int kEpiWarps = 8;
+constexpr int kGroupM = 16;       // dense raster: 16 m-tiles share a sweep over n
+constexpr int kMaxGroups = 1024;
+
+template <int BN, int STAGES>
+struct Layout {
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = STAGES * A_BYTES;
+    static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;   // full[S], empty[S], tfull[2], tempty[2], done
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_ABORT = OFF_TMEM + 4;
+    static constexpr int OFF_TABLE = (OFF_ABORT + 4 + 15) & ~15;  // grouped: tile prefix [G+1]
+    static constexpr int TABLE_BYTES = (kMaxGroups + 1) * 4;
+    static constexpr int BYTES = OFF_TABLE + TABLE_BYTES;
+    static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+    static_assert(TMEM_COLS <= 512, "two chunk buffers must fit in TMEM");
+};
+
+struct Params {
+    const float* sx;
+    int64_t lds;
+    const float* sw;
+    uint16_t* y;
+    int64_t ldy;
+    float* partial;          // split-K: fp32 [splits][M][N], else nullptr
+    const int32_t* offsets;  // grouped: device [G+1], else nullptr
+    int G;
+    int M, N, KB;
+    int MT, NT;              // dense: m-tiles, n-tiles
+    int splits, kps;         // dense split-K: number of splits, chunks per split
+    int num_tiles;           // dense: MT * NT * splits
+    unsigned* err;
+    uint64_t timeout_ns;
+};
+
+struct Tile {
+    int m0;      // first row of A / y
+    int m_end;   // one past the last valid row
+    int n0;      // first output column
+    int b_row;   // first row of the B operand (g * N + n0 for grouped)
+    int sw_row;  // weight-scale row of column n0 (g * NB + n0 / 128)
+    int kb0, kb1;
+    int split;
+};
+
+template <int BN>
+__device__ __forceinline__ Tile dense_tile(const Params& p, int t) {
+    Tile tl;
+    tl.split = t % p.splits;
+    t /= p.splits;
+    const int per_group = kGroupM * p.NT;
+    const int grp = t / per_group;
+    const int first_m = grp * kGroupM;
+    const int gm = min(p.MT - first_m, kGroupM);
+    const int local = t - grp * per_group;
+    const int mt = first_m + local % gm;
+    const int nt = local / gm;
+    tl.m0 = mt * BM;
+    tl.m_end = min(p.M, tl.m0 + BM);
+    tl.n0 = nt * BN;
+    tl.b_row = tl.n0;
+    tl.sw_row = tl.n0 / 128;
+    tl.kb0 = tl.split * p.kps;
+    tl.kb1 = min(p.KB, tl.kb0 + p.kps);
+    return tl;
+}
+
+// prefix[g] = number of tiles of experts < g; tile t belongs to the last
+// expert g with prefix[g] <= t (empty experts have prefix[g] == prefix[g+1]).
+template <int BN>
+__device__ __forceinline__ Tile grouped_tile(const Params& p, const int* prefix, int t) {
+    int lo = 0, hi = p.G;  // invariant: prefix[lo] <= t < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int g = lo;
+    const int r0 = min(max(__ldg(p.offsets + g), 0), p.M);
+    const int r1 = min(max(__ldg(p.offsets + g + 1), r0), p.M);
+    const int mtiles = max((r1 - r0 + BM - 1) / BM, 1);
+    const int local = t - prefix[g];
+    const int mt = local % mtiles;
+    const int nt = local / mtiles;
+    Tile tl;
+    tl.m0 = r0 + mt * BM;
+    tl.m_end = r1;
+    tl.n0 = nt * BN;
+    tl.b_row = g * p.N + tl.n0;
+    tl.sw_row = g * ((p.N + 127) / 128) + tl.n0 / 128;
+    tl.kb0 = 0;
+    tl.kb1 = p.KB;
+    tl.split = 0;
+    return tl;
+}
+
+// Warp-wide exclusive scan of per-expert tile counts into prefix[0..G].
+template <int BN>
+__device__ void build_tile_table(const Params& p, int* prefix, int lane) {
+    const int per = (p.G + 31) / 32;
+    const int g0 = lane * per;
+    const int nt = (p.N + BN - 1) / BN;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+        const int g = g0 + i;
+        if (g < p.G) {
+            const int r0 = min(max(__ldg(p.offsets + g), 0), p.M);
+            const int r1 = min(max(__ldg(p.offsets + g + 1), r0), p.M);
+            local += ((r1 - r0 + BM - 1) / BM) * nt;
+        }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+        const int g = g0 + i;
+        if (g < p.G) {
+            prefix[g] = run;
+            const int r0 = min(max(__ldg(p.offsets + g), 0), p.M);
+            const int r1 = min(max(__ldg(p.offsets + g + 1), r0), p.M);
+            run += ((r1 - r0 + BM - 1) / BM) * nt;
+        }
+    }
+    if (lane == 31) prefix[p.G] = incl;
+}
+
+// Wait used while draining in-flight async work before the CTA exits: it
+// ignores the abort flag (the work must land before its memory is released)
+// but keeps the time limit.
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+    int no_abort = 0;
+    WaitCtl c2{&no_abort, ctl.err, ctl.timeout_ns};
+    const bool ok = bounded_wait(bar, parity, c2);
+    __syncwarp();
+    return ok;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int BN, int STAGES, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ Params p) {
+    using L = Layout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t bar0 = sbase + L::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
+    int* prefix = reinterpret_cast<int*>(smem + L::OFF_TABLE);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), kEpiWarps);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
+    if (GROUPED && warp == 2) build_tile_table<BN>(p, prefix, lane);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_TMEM);
+    const int num_tiles = GROUPED ? prefix[p.G] : p.num_tiles;
+    const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
+
+    auto tile_of = [&](int t) { return GROUPED ? grouped_tile<BN>(p, prefix, t) : dense_tile<BN>(p, t); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+        }
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            const Tile tl = tile_of(t);
+            for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!warp_wait(empty_bar(s), ph ^ 1u, ctl)) { ok = false; break; }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(s), L::STAGE_BYTES);
+                    tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * BK, tl.m0);
+                    tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * BK, tl.b_row);
+                }
+                __syncwarp();
+            }
+        }
+        // Every issued load must land before the CTA's shared memory goes away.
+        const uint32_t first = it > STAGES ? it - STAGES : 0;
+        for (uint32_t j = first; j < it; ++j) drain_wait(full_bar(j % STAGES), (j / STAGES) & 1u, ctl);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+        uint32_t it = 0;
+        bool ok = true, issued = false;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            const Tile tl = tile_of(t);
+            for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t sph = (it / STAGES) & 1u;
+                const int b = it & 1;
+                const uint32_t bph = (it >> 1) & 1u;
+                if (!warp_wait(tempty_bar(b), bph ^ 1u, ctl)) { ok = false; break; }
+                if (!warp_wait(full_bar(s), sph, ctl)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t adesc = sdesc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+                    const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)  // +32 bytes along K = +2 in the address field
+                        umma_e4m3(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
+                    umma_commit(empty_bar(s));
+                    umma_commit(tfull_bar(b));
+                }
+                issued = true;
+                __syncwarp();
+            }
+        }
+        // All MMAs must finish before TMEM is released.
+        if (issued) {
+            if (lane == 0) umma_commit(done_bar);
+            __syncwarp();
+            drain_wait(done_bar, 0, ctl);
+        }
+    } else if (warp >= kEpiWarp0) {
+        // ------------------------------------------------------------ promotion + epilogue
+        constexpr int COLS = BN / 2;        // columns per warpgroup
+        constexpr int NCH = COLS / 32;      // 32-column TMEM loads per chunk
+        const int ew = warp - kEpiWarp0;
+        const int wg = ew >> 2;
+        const int quarter = warp & 3;       // TMEM lane quarter this warp may access
+        const int row = quarter * 32 + lane;
+        const int col0 = wg * COLS;
+        const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            const Tile tl = tile_of(t);
+            const int m = tl.m0 + row;
+            const bool row_ok = m < tl.m_end;
+            const float* sxr = p.sx + static_cast<int64_t>(row_ok ? m : 0) * p.lds;
+            const float* swr[NCH];
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+                swr[c] = p.sw + static_cast<int64_t>(tl.sw_row + (col0 + 32 * c) / 128) * p.KB;
+            float acc[COLS];
+#pragma unroll
+            for (int i = 0; i < COLS; ++i) acc[i] = 0.0f;
+
+            float sx_next = row_ok ? __ldg(sxr + tl.kb0) : 0.0f;
+            float sw_next[NCH];
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) sw_next[c] = __ldg(swr[c] + tl.kb0);
+
+            for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
+                const int b = it & 1;
+                const uint32_t bph = (it >> 1) & 1u;
+                const float sxv = sx_next;
+                float swv[NCH];
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) swv[c] = sw_next[c];
+                if (kb + 1 < tl.kb1) {
+                    sx_next = row_ok ? __ldg(sxr + kb + 1) : 0.0f;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) sw_next[c] = __ldg(swr[c] + kb + 1);
+                }
+                if (!warp_wait(tfull_bar(b), bph, ctl)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * BN + col0);
+#pragma unroll
+                for (int c = 0; c < NCH; c += 2) {
+                    uint32_t r[64];
+                    if (c + 1 < NCH) {
+                        tmem_ld_32x32b_x64(taddr + 32u * c, reinterpret_cast<uint32_t(&)[64]>(r));
+                    } else {
+                        tmem_ld_32x32b_x32(taddr + 32u * c, reinterpret_cast<uint32_t(&)[32]>(r));
+                    }
+                    const float f0 = __fmul_rn(sxv, swv[c]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc[32 * c + i] = __fmaf_rn(f0, __uint_as_float(r[i]), acc[32 * c + i]);
+                    if (c + 1 < NCH) {
+                        const float f1 = __fmul_rn(sxv, swv[c + 1]);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            acc[32 * (c + 1) + i] = __fmaf_rn(f1, __uint_as_float(r[32 + i]), acc[32 * (c + 1) + i]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(b));
+            }
+            if (!ok) break;
+            if (!row_ok) continue;
+            const int nbase = tl.n0 + col0;
+            if (p.partial == nullptr) {
+                uint16_t* yr = p.y + static_cast<int64_t>(m) * p.ldy;
+#pragma unroll
+                for (int v = 0; v < COLS / 8; ++v) {
+                    const int n = nbase + 8 * v;
+                    if (n + 8 <= p.N) {
+                        uint4 o;
+                        o.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
+                        o.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
+                        o.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
+                        o.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
+                        *reinterpret_cast<uint4*>(yr + n) = o;
+                    } else if (n < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (n + j < p.N) {
+                                const __nv_bfloat16 h = __float2bfloat16_rn(acc[8 * v + j]);
+                                yr[n + j] = *reinterpret_cast<const uint16_t*>(&h);
+                            }
+                    }
+                }
+            } else {
+                float* pr = p.partial + (static_cast<int64_t>(tl.split) * p.M + m) * p.N;
+#pragma unroll
+                for (int v = 0; v < COLS / 4; ++v) {
+                    const int n = nbase + 4 * v;
+                    if (n + 4 <= p.N && (p.N & 3) == 0) {
+                        *reinterpret_cast<float4*>(pr + n) =
+                            make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (n + j < p.N) pr[n + j] = acc[4 * v + j];
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+// Deterministic split-K reduction: y = bf16(sum over splits in order 0..S-1).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int splits, int M,
+                                                           int N, uint16_t* __restrict__ y, int64_t ldy) {
+    const int64_t nch = (N + 7) / 8;
+    const int64_t total = static_cast<int64_t>(M) * nch;
+    const bool vec = (N & 3) == 0;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = idx / nch;
+        const int n = static_cast<int>(idx - m * nch) * 8;
+        float s[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = 0.0f;
+        for (int sp = 0; sp < splits; ++sp) {
+            const float* src = part + (static_cast<int64_t>(sp) * M + m) * N + n;
+            if (vec && n + 8 <= N) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+                const float4 b = __ldg(reinterpret_cast<const float4*>(src + 4));
+                s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
+                s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (n + j < N) s[j] += src[j];
+            }
+        }
+        uint16_t* dst = y + m * ldy + n;
+        if (n + 8 <= N) {
+            uint4 o;
+            o.x = pack_bf16x2(s[0], s[1]);
+            o.y = pack_bf16x2(s[2], s[3]);
+            o.z = pack_bf16x2(s[4], s[5]);
+            o.w = pack_bf16x2(s[6], s[7]);
+            *reinterpret_cast<uint4*>(dst) = o;
+        } else {
+            for (int j = 0; j < 8; ++j)
+                if (n + j < N) {
+                    const __nv_bfloat16 h = __float2bfloat16_rn(s[j]);
+                    dst[j] = *reinterpret_cast<const uint16_t*>(&h);
+                }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// 2-D uint8 tensor [rows, inner] with the given row stride, boxes of
+// box_rows x 128 bytes, 128-byte swizzle, zero fill outside the tensor.
+cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
+                     uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+constexpr int kBN = 128;
+constexpr int kStages = 6;
+
+struct Plan {
+    int splits;
+    int kps;
+    size_t ws;
+};
+
+Plan dense_plan(int64_t M, int64_t N, int64_t K, int num_sms, size_t ws_cap) {
+    const int64_t KB = K / 128;
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
+    Plan pl{1, static_cast<int>(KB), 0};
+    if (tiles * 2 > num_sms || KB < 8) return pl;
+    int64_t splits = std::min<int64_t>(num_sms / tiles, KB / 4);
+    while (splits > 1) {
+        const int64_t kps = (KB + splits - 1) / splits;
+        const int64_t s = (KB + kps - 1) / kps;
+        const size_t ws = static_cast<size_t>(s) * static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+        if (ws <= ws_cap) return Plan{static_cast<int>(s), static_cast<int>(kps), ws};
+        --splits;
+    }
+    return pl;
+}
+
+template <int BN, int STAGES, bool GROUPED>
+cudaError_t ensure_smem_attr(int device) {
+    static std::mutex mu;
+    static bool done[64];
+    std::lock_guard<std::mutex> g(mu);
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (!done[device]) {
+        cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, STAGES, GROUPED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Layout<BN, STAGES>::ALLOC);
+        if (e != cudaSuccess) return e;
+        done[device] = true;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+    return dense_plan(M, N, K, dev.num_sms, ~size_t{0}).ws;
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+    constexpr int BN = kBN, STAGES = kStages;
+    const bool grouped = a.offsets != nullptr;
+    const int64_t b_rows = grouped ? static_cast<int64_t>(a.G) * a.N : a.N;
+    CUtensorMap tmA, tmB;
+    cudaError_t e;
+    if ((e = make_map(&tmA, a.xq, a.K, a.M, a.K, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&tmB, a.wq, a.K, b_rows, a.K, BN)) != cudaSuccess) return e;
+
+    Params p{};
+    p.sx = a.sx;
+    p.lds = a.lds;
+    p.sw = a.sw;
+    p.y = a.y;
+    p.ldy = a.ldy;
+    p.M = static_cast<int>(a.M);
+    p.N = static_cast<int>(a.N);
+    p.KB = static_cast<int>(a.K / 128);
+    p.err = dev.err;
+    p.timeout_ns = wait_timeout_ns();
+    using L = Layout<BN, STAGES>;
+    if (grouped) {
+        p.offsets = a.offsets;
+        p.G = a.G;
+        p.splits = 1;
+        p.kps = p.KB;
+        if ((e = ensure_smem_attr<BN, STAGES, true>(dev.device)) != cudaSuccess) return e;
+        fp8_gemm_kernel<BN, STAGES, true><<<dev.num_sms, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
+        return cudaGetLastError();
+    }
+    const Plan pl = dense_plan(a.M, a.N, a.K, dev.num_sms, a.workspace ? a.ws_bytes : 0);
+    p.MT = static_cast<int>((a.M + BM - 1) / BM);
+    p.NT = static_cast<int>((a.N + BN - 1) / BN);
+    p.splits = pl.splits;
+    p.kps = pl.kps;
+    p.num_tiles = p.MT * p.NT * p.splits;
+    p.partial = pl.splits > 1 ? static_cast<float*>(a.workspace) : nullptr;
+    if ((e = ensure_smem_attr<BN, STAGES, false>(dev.device)) != cudaSuccess) return e;
+    const int grid = std::min(p.num_tiles, dev.num_sms);
+    fp8_gemm_kernel<BN, STAGES, false><<<grid, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (pl.splits > 1) {
+        const int64_t work = a.M * ((a.N + 7) / 8);
+        const int blocks = static_cast<int>(std::min<int64_t>((work + 255) / 256, dev.num_sms * 8));
+        splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(p.partial, pl.splits, p.M, p.N, a.y, a.ldy);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
+}  // namespace fp8bs

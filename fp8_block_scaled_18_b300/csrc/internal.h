@@ -1,0 +1,56 @@
+// internal.h -- launchers shared between the C-ABI shim (api.cu) and the
+// kernel translation units.  Arguments are validated by the shim before any
+// launcher runs.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fp8bs {
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    unsigned* err;  // device address of this device's status word
+};
+
+// Per-device facts, filled once per device under a lock (status.cu).
+cudaError_t device_info(DeviceInfo* out);
+
+// Nanoseconds a pipeline wait may take before the kernel gives up
+// (FP8BS_WAIT_TIMEOUT_NS in the environment overrides the default of 2 s).
+uint64_t wait_timeout_ns();
+
+cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq,
+                             float* sx, int64_t lds, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
+                                cudaStream_t stream);
+cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
+                                  cudaStream_t stream);
+cudaError_t launch_e4m3_encode(const float* v, int64_t n, uint8_t* q, const DeviceInfo& dev,
+                               cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, const DeviceInfo& dev, cudaStream_t stream);
+
+// Dense and grouped GEMM (gemm.cu).
+struct GemmArgs {
+    const uint8_t* xq;
+    const float* sx;
+    int64_t lds;
+    const uint8_t* wq;
+    const float* sw;
+    int64_t M, N, K;
+    uint16_t* y;
+    int64_t ldy;
+    // grouped only
+    const int32_t* offsets;  // device [G+1] or nullptr for a dense GEMM
+    int32_t G;
+    // dense split-K scratch
+    void* workspace;
+    size_t ws_bytes;
+};
+
+size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
+cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace fp8bs

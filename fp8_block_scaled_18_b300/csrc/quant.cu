@@ -1,0 +1,259 @@
+// quant.cu -- the HBM-bound kernels: act_quant (1x128 groups), weight_quant
+// (128x128 blocks), weight_dequant, and the elementwise e4m3 encoder.
+//
+// Quantisation rule ("DeepSeek-V3" repository overview, section
+// "FP8 混合精度训练"): s = amax / 448 over the group or block (fp32, IEEE
+// round-to-nearest division), code = e4m3(x / s) with round-to-nearest-even
+// and saturation at +-448; an all-zero group has s = 0 and +-0 codes.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace {
+
+constexpr float kE4M3Max = 448.0f;
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Code of one element given its group's amax and scale.
+__device__ __forceinline__ float quotient(float x, float s) { return __fdiv_rn(x, s); }
+
+// Encode 8 fp32 values (x / s) into 8 e4m3 bytes (little-endian in a uint2).
+// zero_group: every code is +-0 with the input's sign.
+__device__ __forceinline__ uint2 encode8(const float (&x)[8], float s, bool zero_group) {
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t lo, hi;
+        if (zero_group) {
+            uint32_t b[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = (__float_as_uint(x[4 * h + j]) >> 24) & 0x80u;
+            lo = b[0] | (b[1] << 8);
+            hi = b[2] | (b[3] << 8);
+        } else {
+            lo = cvt_e4m3x2(quotient(x[4 * h + 0], s), quotient(x[4 * h + 1], s));
+            hi = cvt_e4m3x2(quotient(x[4 * h + 2], s), quotient(x[4 * h + 3], s));
+        }
+        w[h] = lo | (hi << 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
+    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x);
+    x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z);
+    x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ float absmax8(const float (&x)[8], float m) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(x[j]));
+    return m;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------- act_quant
+//
+// Eight lanes own one 128-channel group: lane j of the team loads channels
+// [8j, 8j+8) and [64+8j, 64+8j+8) (two 16-byte loads; each load instruction
+// of the team covers 128 contiguous bytes), the amax is reduced over the team
+// with three xor-shuffles, and each lane writes its 16 codes as two 8-byte
+// stores.  A warp handles four groups per step; grid-stride over all groups.
+__global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, int64_t KB,
+                                                       int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
+                                                       float* __restrict__ sx, int64_t lds,
+                                                       int64_t total_groups) {
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & 7;
+    const int team = lane >> 3;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+
+    for (int64_t base = warp * 4; base < total_groups; base += nwarps * 4) {
+        const int64_t g = base + team;
+        const bool valid = g < total_groups;
+        float a[8], b[8];
+        int64_t m = 0, kb = 0;
+        float amax = 0.0f;
+        if (valid) {
+            m = g / KB;
+            kb = g - m * KB;
+            const uint16_t* p = x + m * ldx + kb * 128;
+            unpack8(ld_stream(p + sub * 8), a);
+            unpack8(ld_stream(p + 64 + sub * 8), b);
+            amax = absmax8(b, absmax8(a, 0.0f));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        if (valid) {
+            const float s = __fdiv_rn(amax, kE4M3Max);
+            const bool zero = (amax == 0.0f);
+            uint8_t* q = xq + m * ldq + kb * 128;
+            *reinterpret_cast<uint2*>(q + sub * 8) = encode8(a, s, zero);
+            *reinterpret_cast<uint2*>(q + 64 + sub * 8) = encode8(b, s, zero);
+            if (sub == 0) sx[m * lds + kb] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- weight_quant
+//
+// One 256-thread CTA per 128x128 block.  Thread t reads the 16-byte chunk
+// (t % 16) of rows (t / 16) + 16 j, j = 0..7 (each warp load covers two full
+// 256-byte row segments), block amax via warp shuffles and shared memory.
+__global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
+                                                          uint8_t* __restrict__ wq, float* __restrict__ sw) {
+    __shared__ float warp_max[8];
+    const int kb = blockIdx.x, nb = blockIdx.y;
+    const int64_t KB = K / 128;
+    const int t = threadIdx.x;
+    const int chunk = t & 15;
+    const int r0 = t >> 4;
+    float v[8][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 16 * j;
+        if (n < N) {
+            unpack8(ld_stream(w + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8), v[j]);
+            amax = absmax8(v[j], amax);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((t & 31) == 0) warp_max[t >> 5] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
+    const float s = __fdiv_rn(amax, kE4M3Max);
+    const bool zero = (amax == 0.0f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 16 * j;
+        if (n < N)
+            *reinterpret_cast<uint2*>(wq + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8) =
+                encode8(v[j], s, zero);
+    }
+    if (t == 0) sw[static_cast<int64_t>(nb) * KB + kb] = s;
+}
+
+// ---------------------------------------------------------------- weight_dequant
+//
+// One 256-thread CTA per 128x128 block: thread t decodes the 16-byte chunk
+// (t % 8) of rows (t / 8) + 32 j, j = 0..3: w = bf16_rne(fp32(dec(q)) * s).
+__global__ void __launch_bounds__(256) weight_dequant_kernel(const uint8_t* __restrict__ wq,
+                                                            const float* __restrict__ sw, int64_t N,
+                                                            int64_t K, uint16_t* __restrict__ w) {
+    const int kb = blockIdx.x, nb = blockIdx.y;
+    const int64_t KB = K / 128;
+    const int t = threadIdx.x;
+    const int chunk = t & 7;
+    const int r0 = t >> 3;
+    const float s = sw[static_cast<int64_t>(nb) * KB + kb];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 32 * j;
+        if (n >= N) continue;
+        const int64_t off = n * K + static_cast<int64_t>(kb) * 128 + chunk * 16;
+        const uint4 q = ld_stream(wq + off);
+        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+        uint32_t out[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f01 = cvt_e4m3x2_to_f32(static_cast<uint16_t>(words[i] & 0xFFFFu));
+            const float2 f23 = cvt_e4m3x2_to_f32(static_cast<uint16_t>(words[i] >> 16));
+            const __nv_bfloat162 b01 = __floats2bfloat162_rn(__fmul_rn(f01.x, s), __fmul_rn(f01.y, s));
+            const __nv_bfloat162 b23 = __floats2bfloat162_rn(__fmul_rn(f23.x, s), __fmul_rn(f23.y, s));
+            out[2 * i] = *reinterpret_cast<const uint32_t*>(&b01);
+            out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&b23);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(w + off);
+        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+}
+
+// ---------------------------------------------------------------- diagnostics
+
+__global__ void e4m3_encode_kernel(const float* __restrict__ v, int64_t n, uint8_t* __restrict__ q) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        q[i] = static_cast<uint8_t>(cvt_e4m3x2(v[i], 0.0f) & 0xFFu);
+}
+
+// One warp waits on a barrier that nothing completes, using the same bounded
+// wait as the GEMM pipeline, and records DEVERR_SELFTEST when it gives up.
+__global__ void wait_selftest_kernel(unsigned* err, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    __shared__ unsigned local_err;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        local_err = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    WaitCtl ctl{&abort_flag, &local_err, timeout_ns};
+    const bool ok = bounded_wait(smem_u32(&bar), 0, ctl);
+    __syncwarp();
+    if (!ok && threadIdx.x == 0) atomicOr(err, DEVERR_SELFTEST);
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq,
+                             float* sx, int64_t lds, const DeviceInfo& dev, cudaStream_t stream) {
+    const int64_t KB = K / 128;
+    const int64_t groups = M * KB;
+    const int64_t warps_needed = (groups + 3) / 4;
+    const int64_t blocks_needed = (warps_needed + 7) / 8;
+    const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 8;  // 8 x 256 threads per SM
+    const int blocks = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
+    act_quant_kernel<<<blocks, 256, 0, stream>>>(x, KB, ldx, xq, ldq, sx, lds, groups);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
+                                cudaStream_t stream) {
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
+    weight_quant_kernel<<<grid, 256, 0, stream>>>(w, N, K, wq, sw);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
+                                  cudaStream_t stream) {
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
+    weight_dequant_kernel<<<grid, 256, 0, stream>>>(wq, sw, N, K, w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_encode(const float* v, int64_t n, uint8_t* q, const DeviceInfo& dev,
+                               cudaStream_t stream) {
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    e4m3_encode_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(v, n, q);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, const DeviceInfo& dev, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(dev.err, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

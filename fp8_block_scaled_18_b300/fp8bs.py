@@ -1,0 +1,210 @@
+"""ctypes binding of libfp8bs.so -- the same call names as include/fp8bs.h.
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (torch provides device memory and
+streams); outputs not passed in are allocated here with torch.  Importing this
+module raises ImportError if the library has not been built
+(``python -m fp8_block_scaled_18_b300.build``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libfp8bs.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fp8bs.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m fp8_block_scaled_18_b300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_P, _I64, _I32, _SZ, _U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_uint64
+_ST = ctypes.c_int
+
+_SIGS = {
+    "fp8bs_act_quant": (_ST, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
+    "fp8bs_weight_quant": (_ST, [_P, _I64, _I64, _P, _P, _P]),
+    "fp8bs_weight_dequant": (_ST, [_P, _P, _I64, _I64, _P, _P]),
+    "fp8bs_gemm": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P]),
+    "fp8bs_gemm_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "fp8bs_grouped_gemm": (_ST, [_P, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
+    "fp8bs_sync_status": (_ST, [_P]),
+    "fp8bs_status_string": (ctypes.c_char_p, [_ST]),
+    "fp8bs_e4m3_encode_f32": (_ST, [_P, _I64, _P, _P]),
+    "fp8bs_debug_wait_timeout": (_ST, [_U64, _P]),
+    "fp8bs_version": (ctypes.c_int, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+FP8BS_OK = 0
+FP8BS_ERR_INVALID_ARG = 1
+FP8BS_ERR_UNSUPPORTED = 2
+FP8BS_ERR_MISALIGNED = 3
+FP8BS_ERR_CUDA = 4
+FP8BS_ERR_TIMEOUT = 5
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {fp8bs_status_string(status)}")
+
+
+def declared_symbols() -> list[str]:
+    """Every function name include/fp8bs.h declares."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"\b(fp8bs_[a-z0-9_]+)\s*\(", text)))
+
+
+def fp8bs_status_string(status: int) -> str:
+    return lib.fp8bs_status_string(status).decode()
+
+
+def fp8bs_version() -> int:
+    return lib.fp8bs_version()
+
+
+def _check(status: int, call: str) -> None:
+    if status != FP8BS_OK:
+        raise Fp8bsError(status, call)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _rows_stride(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+# bf16 tensors are passed as their bit patterns; both torch.bfloat16 and
+# int16/uint16 views are accepted.
+def _bf16_ptr(t: torch.Tensor, name: str) -> int:
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must be bfloat16 (or its 16-bit bit pattern)")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.data_ptr()
+
+
+def fp8bs_act_quant(x: torch.Tensor, xq: Optional[torch.Tensor] = None, sx: Optional[torch.Tensor] = None,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """x [M, K] bf16 -> (xq [M, K] uint8 e4m3, sx [M, lds] fp32)."""
+    M, K = x.shape
+    ldx = _rows_stride(x, "x")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((M, max(4, ((K // 128) + 3) // 4 * 4)), dtype=torch.float32, device=x.device)
+    _check(lib.fp8bs_act_quant(_bf16_ptr(x, "x"), M, K, ldx, _dev(xq, torch.uint8, "xq"),
+                               _rows_stride(xq, "xq"), _dev(sx, torch.float32, "sx"),
+                               _rows_stride(sx, "sx"), _stream(stream)), "fp8bs_act_quant")
+    return xq, sx
+
+
+def fp8bs_weight_quant(w: torch.Tensor, wq: Optional[torch.Tensor] = None, sw: Optional[torch.Tensor] = None,
+                       stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """w [N, K] bf16 (dense) -> (wq [N, K] uint8, sw [ceil(N/128), K/128] fp32)."""
+    N, K = w.shape
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if sw is None:
+        sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device)
+    _check(lib.fp8bs_weight_quant(_bf16_ptr(w, "w"), N, K, _dev(wq, torch.uint8, "wq"),
+                                  _dev(sw, torch.float32, "sw"), _stream(stream)), "fp8bs_weight_quant")
+    return wq, sw
+
+
+def fp8bs_weight_dequant(wq: torch.Tensor, sw: torch.Tensor, w: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """(wq [N, K] uint8, sw) -> w [N, K] bf16."""
+    N, K = wq.shape
+    if w is None:
+        w = torch.empty((N, K), dtype=torch.bfloat16, device=wq.device)
+    _check(lib.fp8bs_weight_dequant(_dev(wq, torch.uint8, "wq"), _dev(sw, torch.float32, "sw"), N, K,
+                                    _bf16_ptr(w, "w"), _stream(stream)), "fp8bs_weight_dequant")
+    return w
+
+
+def _out_rows(M: int, N: int, device) -> torch.Tensor:
+    """bf16 [M, N] output whose row stride is padded to a multiple of 8."""
+    ld = (N + 7) // 8 * 8
+    y = torch.empty((M, ld), dtype=torch.bfloat16, device=device)
+    return y if ld == N else y[:, :N]
+
+
+def fp8bs_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib.fp8bs_gemm_workspace_size(M, N, K))
+
+
+def fp8bs_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
+               y: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """y [M, N] bf16 = fp8_gemm(xq, sx, wq, sw); workspace: optional uint8 CUDA
+    tensor for the split-K plan (see fp8bs_gemm_workspace_size)."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    if y is None:
+        y = _out_rows(M, N, xq.device)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_dev(workspace, torch.uint8, "workspace"),
+                                                            workspace.numel())
+    _check(lib.fp8bs_gemm(_dev(xq, torch.uint8, "xq"), _dev(sx, torch.float32, "sx"), _rows_stride(sx, "sx"),
+                          _dev(wq, torch.uint8, "wq"), _dev(sw, torch.float32, "sw"), M, N, K,
+                          _bf16_ptr(y, "y"), _rows_stride(y, "y"), ws_ptr, ws_bytes, _stream(stream)),
+           "fp8bs_gemm")
+    return y
+
+
+def fp8bs_grouped_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
+                       offsets: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """xq [T, K], wq [G, N, K], sw [G, ceil(N/128), K/128], offsets int32 [G+1]
+    on the device -> y [T, N] bf16."""
+    T, K = xq.shape
+    G, N, _ = wq.shape
+    if y is None:
+        y = _out_rows(T, N, xq.device)
+    _check(lib.fp8bs_grouped_gemm(_dev(xq, torch.uint8, "xq"), _dev(sx, torch.float32, "sx"),
+                                  _rows_stride(sx, "sx"), _dev(wq, torch.uint8, "wq"),
+                                  _dev(sw, torch.float32, "sw"), _dev(offsets, torch.int32, "offsets"), G, T,
+                                  N, K, _bf16_ptr(y, "y"), _rows_stride(y, "y"), _stream(stream)),
+           "fp8bs_grouped_gemm")
+    return y
+
+
+def fp8bs_sync_status(stream=None) -> int:
+    """Synchronise and return (not raise) the library status."""
+    return lib.fp8bs_sync_status(_stream(stream))
+
+
+def fp8bs_e4m3_encode_f32(v: torch.Tensor, q: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    if q is None:
+        q = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    _check(lib.fp8bs_e4m3_encode_f32(_dev(v, torch.float32, "v"), v.numel(), _dev(q, torch.uint8, "q"),
+                                     _stream(stream)), "fp8bs_e4m3_encode_f32")
+    return q
+
+
+def fp8bs_debug_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(lib.fp8bs_debug_wait_timeout(timeout_ns, _stream(stream)), "fp8bs_debug_wait_timeout")

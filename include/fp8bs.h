@@ -1,0 +1,157 @@
+/*
+ * fp8bs.h -- C ABI of the FP8 (e4m3) block-scaled linear layer for B300
+ * (sm_103a).  Library: libfp8bs.so.
+ *
+ * The operation is the FP8 branch of DeepSeek-V3's linear(), as printed in the
+ * "DeepSeek-V3" repository overview (pomoai hub), section "FP8 混合精度训练":
+ *   x, scale = act_quant(x, block_size, scale_fmt)
+ *   y = fp8_gemm(x, scale, weight, weight.scale)
+ * with weights stored as float8 e4m3 in 128x128 blocks, one fp32 scale per
+ * block ("weight_scale_inv"), activations quantised at run time per token per
+ * 128 channels, and weight_dequant(weight, weight.scale) as the bf16 branch.
+ * fp32 promotion once per 128-wide K chunk follows the Float8 paragraph of the
+ * 88811315.cn post on DeepSeek v3 (fp32 accumulation after a fixed number of
+ * FP8 multiply-adds) and the qdgithub overview's "FP8 量化" section (blockwise
+ * FP8 compute, dequantisation on CUDA cores).
+ *
+ * Conventions shared by every call
+ *   - bf16 values travel as uint16_t bit patterns; e4m3 codes as uint8_t (OCP
+ *     E4M3: bias 7, no infinities, 0x7F/0xFF NaN, largest finite 448).
+ *   - Every scale is the dequantisation multiplier: value ~= dec(code) * s,
+ *     with s = amax / 448 (fp32, IEEE round-to-nearest division) over the
+ *     group or block, and code = e4m3(x / s) rounded to nearest-even with
+ *     saturation at +-448.  An all-zero group/block gets s = 0 and +-0 codes.
+ *   - K must be a multiple of 128.  Row-major everywhere ("ld*" = row stride
+ *     in elements).  All pointers are DEVICE pointers owned by the caller; the
+ *     library keeps none of them after the call returns and allocates no
+ *     device memory in any call (it holds one small static status word per
+ *     device).
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *     Argument errors are returned synchronously and launch nothing.  Errors
+ *     inside a kernel (a bounded pipeline wait that expired) are recorded in
+ *     the device status word and reported by fp8bs_sync_status().
+ *   - M (or total rows) == 0 is a no-op returning FP8BS_OK.
+ *   - Thread-safe: calls keep no mutable host state except per-device caches
+ *     filled once under a lock.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* fp8bs_stream_t;
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size */
+    FP8BS_ERR_UNSUPPORTED = 2,  /* K % 128 != 0, size beyond the 32-bit index range, no sm_103 device */
+    FP8BS_ERR_MISALIGNED = 3,   /* pointer or leading dimension breaks the 16-byte rule */
+    FP8BS_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    FP8BS_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (see fp8bs_sync_status) */
+} fp8bs_status;
+
+/* act_quant: per row m and group g of 128 channels (per token, per 128
+ * channels -- "FP8 混合精度训练", dynamic activation quantisation).
+ *   x  [M, K] bf16, row stride ldx (ldx % 8 == 0, x 16-byte aligned)
+ *   xq [M, K] e4m3, row stride ldq (ldq % 16 == 0, 16-byte aligned)
+ *   sx [M, lds] fp32, sx[m*lds + g] = amax_g / 448 for g < K/128
+ *      (lds >= K/128, lds % 4 == 0, 16-byte aligned); columns >= K/128 untouched. */
+fp8bs_status fp8bs_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                             uint8_t* xq, int64_t ldq, float* sx, int64_t lds,
+                             fp8bs_stream_t stream);
+
+/* weight_quant: per 128x128 block (nb, kb) of w ("以 128×128 分块存储", one
+ * fp32 weight_scale_inv per block).  The last row block may be ragged
+ * (N % 128 != 0); its amax is taken over its valid rows.
+ *   w  [N, K] bf16, dense (row stride K), 16-byte aligned
+ *   wq [N, K] e4m3, dense, 16-byte aligned
+ *   sw [ceil(N/128), K/128] fp32, dense. */
+fp8bs_status fp8bs_weight_quant(const uint16_t* w, int64_t N, int64_t K,
+                                uint8_t* wq, float* sw, fp8bs_stream_t stream);
+
+/* weight_dequant (the bf16 branch of linear(); also the FP8->BF16 checkpoint
+ * cast): w[n,k] = bf16_rne(fp32(dec(wq[n,k])) * sw[n/128, k/128]).
+ *   wq [N, K] e4m3 dense, sw [ceil(N/128), K/128] fp32 dense, w [N, K] bf16 dense;
+ *   wq and w 16-byte aligned. */
+fp8bs_status fp8bs_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K,
+                                  uint16_t* w, fp8bs_stream_t stream);
+
+/* fp8_gemm ("y = fp8_gemm(x, scale, weight, weight.scale)"):
+ *   y[m,n] = bf16_rne( sum_kb fp32( sx[m,kb] * sw[n/128,kb] ) * P_kb[m,n] )
+ *   P_kb[m,n] = sum over the 128 k of chunk kb of dec(xq[m,k]) * dec(wq[n,k]),
+ * accumulated by the tensor cores in fp32 and promoted (scaled and added in
+ * fp32) once per chunk.  Any fp32 summation order is allowed: results satisfy
+ * |y - y_exact| <= 2^-8 |y_exact| + 1e-4 sum_k |a_k b_k| elementwise.
+ *   xq [M, K] e4m3, row stride K (dense), 16-byte aligned
+ *   sx [M, lds] fp32 (lds >= K/128, lds % 4 == 0), 16-byte aligned
+ *   wq [N, K] e4m3 dense ("TN": both operands K-major), 16-byte aligned
+ *   sw [ceil(N/128), K/128] fp32 dense
+ *   y  [M, N] bf16, row stride ldy (ldy >= N, ldy % 8 == 0), 16-byte aligned
+ *   workspace: optional device scratch for the split-K path used when M is
+ *     small; may be NULL (then no split).  fp8bs_gemm_workspace_size() gives
+ *     the size that enables the fastest plan; a smaller buffer selects fewer
+ *     splits.  Contents on entry are ignored; the caller must not use it
+ *     concurrently from another call. */
+fp8bs_status fp8bs_gemm(const uint8_t* xq, const float* sx, int64_t lds,
+                        const uint8_t* wq, const float* sw,
+                        int64_t M, int64_t N, int64_t K,
+                        uint16_t* y, int64_t ldy,
+                        void* workspace, size_t ws_bytes, fp8bs_stream_t stream);
+
+/* Bytes of workspace that let fp8bs_gemm pick its fastest plan for this shape
+ * on the current device (0 when no split is used). */
+size_t fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* grouped fp8_gemm for MoE experts (256 routed experts, top-8 -- "MoE 架构详解"):
+ * for each expert g, rows offsets[g] .. offsets[g+1]-1 of xq/sx/y are
+ * multiplied by expert g's weight, exactly as fp8bs_gemm.
+ *   xq [total_M, K] e4m3 dense, sx [total_M, lds] fp32 (as fp8bs_gemm)
+ *   wq [G, N, K] e4m3 dense, sw [G, ceil(N/128), K/128] fp32 dense
+ *   offsets_dev: DEVICE int32 [G+1], non-decreasing, offsets[0] = 0,
+ *     offsets[G] = total_M (read on the device: no host synchronisation).
+ *     A violation is undefined behaviour of the kernel (rows may be skipped
+ *     or written twice) but never an out-of-bounds access: every row index
+ *     is clamped to [0, total_M).
+ *   y  [total_M, N] bf16, row stride ldy (ldy % 8 == 0). */
+fp8bs_status fp8bs_grouped_gemm(const uint8_t* xq, const float* sx, int64_t lds,
+                                const uint8_t* wq, const float* sw,
+                                const int32_t* offsets_dev, int32_t G, int64_t total_M,
+                                int64_t N, int64_t K, uint16_t* y, int64_t ldy,
+                                fp8bs_stream_t stream);
+
+/* Synchronise `stream`, then report and clear this device's status word:
+ * FP8BS_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,
+ * FP8BS_ERR_CUDA if the stream reports a CUDA error, else FP8BS_OK. */
+fp8bs_status fp8bs_sync_status(fp8bs_stream_t stream);
+
+/* Static, human-readable name of a status. */
+const char* fp8bs_status_string(fp8bs_status status);
+
+/* --- diagnostics -------------------------------------------------------- */
+
+/* The e4m3 encoder the quantisers use, applied elementwise: q[i] = e4m3(v[i])
+ * (round to nearest-even, saturate to +-448, NaN -> NaN code).  For testing
+ * the device conversion against the format definition.  v, q device arrays
+ * of n elements (any alignment). */
+fp8bs_status fp8bs_e4m3_encode_f32(const float* v, int64_t n, uint8_t* q, fp8bs_stream_t stream);
+
+/* Launch a one-warp kernel that waits, with the library's bounded wait, on a
+ * barrier nothing ever completes, giving up after timeout_ns nanoseconds.
+ * The next fp8bs_sync_status() must then report FP8BS_ERR_TIMEOUT.  Exercises
+ * the failure path without faulting or hanging the GPU. */
+fp8bs_status fp8bs_debug_wait_timeout(uint64_t timeout_ns, fp8bs_stream_t stream);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int fp8bs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

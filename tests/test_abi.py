@@ -1,0 +1,94 @@
+"""Host-only checks of the C-ABI library: it loads, exports every declared
+symbol, and rejects bad arguments before touching any device."""
+import ctypes
+
+import pytest
+
+fp8bs = pytest.importorskip("fp8_block_scaled_18_b300.fp8bs")
+lib = fp8bs.lib
+
+A = 0x10000  # a 16-byte-aligned fake address; validation fails before any use
+
+
+def test_exports_every_declared_symbol():
+    names = fp8bs.declared_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    for required in ("fp8bs_act_quant", "fp8bs_weight_quant", "fp8bs_weight_dequant", "fp8bs_gemm",
+                     "fp8bs_grouped_gemm", "fp8bs_sync_status", "fp8bs_status_string"):
+        assert required in names
+
+
+def test_status_strings_and_version():
+    for s in range(6):
+        assert fp8bs.fp8bs_status_string(s).startswith("FP8BS")
+    assert fp8bs.fp8bs_status_string(99) == "FP8BS: unknown status"
+    assert fp8bs.fp8bs_version() == (0 << 16) | (1 << 8)
+
+
+def test_act_quant_validation():
+    f = lib.fp8bs_act_quant
+    assert f(A, -1, 128, 128, A, 128, A, 4, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert f(A, 4, 100, 128, A, 128, A, 4, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    assert f(A, 4, 0, 128, A, 128, A, 4, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    assert f(A, 0, 128, 128, A, 128, A, 4, None) == fp8bs.FP8BS_OK          # empty: no-op
+    assert f(None, 4, 128, 128, A, 128, A, 4, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert f(A, 4, 256, 128, A, 256, A, 4, None) == fp8bs.FP8BS_ERR_INVALID_ARG  # ldx < K
+    assert f(A, 4, 256, 256, A, 256, A, 1, None) == fp8bs.FP8BS_ERR_INVALID_ARG  # lds < K/128
+    assert f(A + 2, 4, 128, 128, A, 128, A, 4, None) == fp8bs.FP8BS_ERR_MISALIGNED
+    assert f(A, 4, 128, 132, A, 128, A, 4, None) == fp8bs.FP8BS_ERR_MISALIGNED   # ldx % 8
+    assert f(A, 4, 128, 128, A, 136, A, 4, None) == fp8bs.FP8BS_ERR_MISALIGNED   # ldq % 16
+    assert f(A, 4, 128, 128, A, 128, A, 6, None) == fp8bs.FP8BS_ERR_MISALIGNED   # lds % 4
+
+
+def test_weight_calls_validation():
+    assert lib.fp8bs_weight_quant(A, 10, 129, A, A, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    assert lib.fp8bs_weight_quant(A, -5, 128, A, A, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert lib.fp8bs_weight_quant(A, 0, 128, A, A, None) == fp8bs.FP8BS_OK
+    assert lib.fp8bs_weight_quant(A + 8, 10, 128, A, A, None) == fp8bs.FP8BS_ERR_MISALIGNED
+    assert lib.fp8bs_weight_quant(A, 128 * 65536, 128, A, A, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    assert lib.fp8bs_weight_dequant(A, A, 10, 64, A, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    assert lib.fp8bs_weight_dequant(A, None, 10, 128, A, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert lib.fp8bs_weight_dequant(A, A, 10, 128, A + 4, None) == fp8bs.FP8BS_ERR_MISALIGNED
+
+
+def test_gemm_validation():
+    g = lib.fp8bs_gemm
+    assert g(A, A, 4, A, A, 4, 8, 200, A, 8, None, 0, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    assert g(A, A, 4, A, A, -4, 8, 128, A, 8, None, 0, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert g(A, A, 4, A, A, 0, 8, 128, A, 8, None, 0, None) == fp8bs.FP8BS_OK
+    assert g(A, A, 4, A, A, 4, 0, 128, A, 8, None, 0, None) == fp8bs.FP8BS_OK
+    assert g(A, A, 4, None, A, 4, 8, 128, A, 8, None, 0, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert g(A, A, 4, A, A, 4, 16, 128, A, 8, None, 0, None) == fp8bs.FP8BS_ERR_INVALID_ARG  # ldy < N
+    assert g(A, A, 4, A, A, 4, 8, 128, A, 12, None, 0, None) == fp8bs.FP8BS_ERR_MISALIGNED  # ldy % 8
+    assert g(A, A, 2, A, A, 4, 8, 128, A, 8, None, 0, None) == fp8bs.FP8BS_ERR_MISALIGNED   # lds % 4
+    assert g(A + 1, A, 4, A, A, 4, 8, 128, A, 8, None, 0, None) == fp8bs.FP8BS_ERR_MISALIGNED
+    assert g(A, A, 4, A, A, 4, 8, 128, A, 8, A + 4, 64, None) == fp8bs.FP8BS_ERR_MISALIGNED
+    assert g(A, A, 4, A, A, 1 << 31, 8, 128, A, 8, None, 0, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+
+
+def test_grouped_validation():
+    gg = lib.fp8bs_grouped_gemm
+    assert gg(A, A, 4, A, A, None, 4, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert gg(A, A, 4, A, A, A, -1, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert gg(A, A, 4, A, A, A, 4, 0, 8, 128, A, 8, None) == fp8bs.FP8BS_OK
+    assert gg(A, A, 4, A, A, A, 2000, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    assert gg(A, A, 4, A, A, A + 2, 4, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_MISALIGNED
+    assert gg(A, A, 4, A, A, A, 4, 16, 8, 136, A, 8, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+
+
+def test_debug_calls_validation():
+    assert lib.fp8bs_debug_wait_timeout(0, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert lib.fp8bs_e4m3_encode_f32(A, -1, A, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert lib.fp8bs_e4m3_encode_f32(A, 0, A, None) == fp8bs.FP8BS_OK
+
+
+def test_valid_call_without_a_device_fails_loudly():
+    """On a machine with no GPU a well-formed call reports FP8BS_ERR_CUDA:
+    there is no CPU path to fall back to."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.fp8bs_act_quant(A, 4, 128, 128, A, 128, A, 4, None) == fp8bs.FP8BS_ERR_CUDA
+    assert lib.fp8bs_gemm_workspace_size(1, 1536, 7168) == 0
