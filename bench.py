@@ -1,0 +1,657 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 (e4m3) block-scaled linear layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload kv_down]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One step = one pass of the whole path over one batch of synthetic input:
+dense workloads run weight_quant(W), act_quant(X), fp8_gemm and
+weight_dequant(Wq); the MoE workload runs act_quant over the expert-grouped
+token rows and the grouped fp8_gemm (expert weights quantised once, before
+timing).  The default workload is the MLA KV down-projection
+(X [4096,7168] x W [576,7168]).
+
+Timing: W warm-up steps, then exactly K steps captured in CUDA graphs and
+replayed between CUDA events, bracketed by a barrier and a synchronize; the
+inputs rotate over enough buffer sets that the data touched between two uses
+of a set exceeds the 126 MB L2.  Per-kernel times come from graphs holding K
+launches of that kernel alone.  Under torchrun each rank runs its own
+replica (the layer needs no exchange); rank 0 prints one JSON line with the
+whole-job value (units of all ranks / max time over ranks).
+
+--impl reference times the CPU oracle (plain C, test infrastructure) on a
+bounded sample of the same workload instead -- the only arm that runs it,
+besides the cpu_baseline leg of our own line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio: 4.5 PFLOP/s fp8 vs 2.25 PFLOP/s bf16
+METRIC = "fp8_gemm TFLOP/s & % of dense FP8 peak; act_quant GB/s & % of HBM peak"
+
+
+# ---------------------------------------------------------------- helpers
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="kv_down",
+                    help="kv_down | tiny | q_down_m<M> | large_square | moe")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, world
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device: str = "cpu") -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device: str = "cpu") -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("quant.cu", "gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "fp8_block_scaled_18_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_sources_sha()
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("src_sha") == sha:
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks + throttle reasons every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self) -> dict:
+        rows = []
+        self.file.seek(0)
+        for line in self.file:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workloads
+
+class DenseWork:
+    """weight_quant(W) -> act_quant(X) -> fp8_gemm -> weight_dequant(Wq)."""
+
+    def __init__(self, case, device):
+        import torch
+        from fp8_block_scaled_18_b300 import fp8bs as F
+        self.F = F
+        self.case = case
+        self.M, self.N, self.K = case.shape
+        M, N, K = self.M, self.N, self.K
+        self.x_host = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16)
+        self.w_host = torch.from_numpy(case.w.view(np.int16)).view(torch.bfloat16)
+        per_set = 2 * M * K + 2 * N * K + M * K + 4 * M * (K // 128) + N * K + 2 * M * N + 2 * N * K
+        self.R = max(1, min(8, math.ceil(2 * L2_BYTES / per_set) + 1)) if per_set < 2 * L2_BYTES else 1
+        lds = max(4, (K // 128 + 3) // 4 * 4)
+        ws_bytes = F.fp8bs_gemm_workspace_size(M, N, K)
+        self.sets = []
+        for _ in range(self.R):
+            s = dict(x=self.x_host.to(device), w=self.w_host.to(device),
+                     xq=torch.empty((M, K), dtype=torch.uint8, device=device),
+                     sx=torch.empty((M, lds), dtype=torch.float32, device=device),
+                     wq=torch.empty((N, K), dtype=torch.uint8, device=device),
+                     sw=torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device),
+                     y=torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=device)[:, :N],
+                     wd=torch.empty((N, K), dtype=torch.bfloat16, device=device),
+                     ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None)
+            self.sets.append(s)
+        self.set_bytes = per_set
+        self.gemm_launches = 2 if ws_bytes else 1
+        self.flops = 2.0 * M * N * K
+        nb, kb = (N + 127) // 128, K // 128
+        self.kernels = {
+            # name: (callable(set), launches, algorithmic bytes or flops, bound)
+            "weight_quant": (lambda s: F.fp8bs_weight_quant(s["w"], wq=s["wq"], sw=s["sw"]), 1,
+                             3.0 * N * K + 4.0 * nb * kb, "hbm"),
+            "act_quant": (lambda s: F.fp8bs_act_quant(s["x"], xq=s["xq"], sx=s["sx"]), 1,
+                          3.0 * M * K + 4.0 * M * kb, "hbm"),
+            "fp8_gemm": (lambda s: F.fp8bs_gemm(s["xq"], s["sx"], s["wq"], s["sw"], y=s["y"], workspace=s["ws"]),
+                         self.gemm_launches, self.flops, "tensor"),
+            "weight_dequant": (lambda s: F.fp8bs_weight_dequant(s["wq"], s["sw"], w=s["wd"]), 1,
+                               3.0 * N * K + 4.0 * nb * kb, "hbm"),
+        }
+        self.order = ["weight_quant", "act_quant", "fp8_gemm", "weight_dequant"]
+
+    def step(self, i):
+        s = self.sets[i % self.R]
+        for k in self.order:
+            self.kernels[k][0](s)
+
+    def launches_per_step(self):
+        return sum(self.kernels[k][1] for k in self.order)
+
+    # e2e: host (pinned) bf16 X and W in, bf16 Y out, through the public calls
+    def e2e_setup(self):
+        self.xp = self.x_host.pin_memory()
+        self.wp = self.w_host.pin_memory()
+        import torch
+        self.yp = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.xp.numel() * 2 + self.wp.numel() * 2
+        self.d2h = self.yp.numel() * 2
+
+    def e2e_step(self, i):
+        s = self.sets[i % self.R]
+        s["x"].copy_(self.xp, non_blocking=True)
+        s["w"].copy_(self.wp, non_blocking=True)
+        self.step(i)
+        self.yp.copy_(s["y"], non_blocking=True)
+
+    def config(self):
+        return {"workload": self.case.name, "M": self.M, "N": self.N, "K": self.K,
+                "step": "weight_quant+act_quant+fp8_gemm+weight_dequant",
+                "l2": f"inputs rotate over {self.R} buffer sets of {self.set_bytes / 1e6:.0f} MB (> 126 MB L2)"
+                      if self.R > 1 else "working set larger than the 126 MB L2"}
+
+
+class MoEWork:
+    """act_quant over the expert-grouped rows -> grouped fp8_gemm."""
+
+    def __init__(self, device):
+        import torch
+        from fp8_block_scaled_18_b300 import fp8bs as F
+        from fp8_block_scaled_18_b300 import synth
+        self.F = F
+        case = synth.moe()
+        self.case = case
+        G, N, K = case.n_experts, case.n, case.k
+        self.G, self.N, self.K = G, N, K
+        self.T = int(case.offsets[-1])
+        x_rows = case.x_rows
+        self.x_host = torch.from_numpy(x_rows.view(np.int16)).view(torch.bfloat16)
+        self.x = self.x_host.to(device)
+        self.wq = torch.empty((G, N, K), dtype=torch.uint8, device=device)
+        self.sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device=device)
+        for g in range(G):
+            F.fp8bs_weight_quant(synth.expert_weight(case, g, device), wq=self.wq[g], sw=self.sw[g])
+        self.off = torch.from_numpy(case.offsets).to(device)
+        lds = (K // 128 + 3) // 4 * 4
+        self.xq = torch.empty((self.T, K), dtype=torch.uint8, device=device)
+        self.sx = torch.empty((self.T, lds), dtype=torch.float32, device=device)
+        self.y = torch.empty((self.T, N), dtype=torch.bfloat16, device=device)
+        self.R = 1
+        counts = np.diff(case.offsets)
+        self.flops = 2.0 * self.T * N * K
+        gbytes = G * N * K + 4.0 * G * (N // 128) * (K // 128) + self.T * K + 4.0 * self.T * (K // 128) \
+            + 2.0 * self.T * N
+        self.kernels = {
+            "act_quant": (lambda s: F.fp8bs_act_quant(self.x, xq=self.xq, sx=self.sx), 1,
+                          3.0 * self.T * K + 4.0 * self.T * (K // 128), "hbm"),
+            "grouped_gemm": (lambda s: F.fp8bs_grouped_gemm(self.xq, self.sx, self.wq, self.sw, self.off, y=self.y),
+                             1, gbytes, "hbm"),
+        }
+        self.order = ["act_quant", "grouped_gemm"]
+        self.grouped_flops = self.flops
+        self.experts_nonempty = int((counts > 0).sum())
+
+    def step(self, i):
+        for k in self.order:
+            self.kernels[k][0](None)
+
+    def launches_per_step(self):
+        return 2
+
+    def e2e_setup(self):
+        import torch
+        self.xp = self.x_host.pin_memory()
+        self.offp = torch.from_numpy(self.case.offsets).pin_memory()
+        self.yp = torch.empty((self.T, self.N), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.xp.numel() * 2 + self.offp.numel() * 4
+        self.d2h = self.yp.numel() * 2
+
+    def e2e_step(self, i):
+        self.x.copy_(self.xp, non_blocking=True)
+        self.off.copy_(self.offp, non_blocking=True)
+        self.step(i)
+        self.yp.copy_(self.y, non_blocking=True)
+
+    def config(self):
+        return {"workload": "moe_grouped", "tokens": 4096, "experts": self.G, "top_k": 8, "rows": self.T,
+                "N": self.N, "K": self.K, "step": "act_quant+grouped_fp8_gemm (expert weights pre-quantised)",
+                "l2": "working set (3.76 GB of expert weights) larger than the 126 MB L2"}
+
+
+def make_work(name: str, device):
+    from fp8_block_scaled_18_b300 import synth
+    if name == "moe":
+        return MoEWork(device)
+    if name == "kv_down":
+        return DenseWork(synth.kv_down(), device)
+    if name == "tiny":
+        return DenseWork(synth.tiny(), device)
+    if name == "large_square":
+        return DenseWork(synth.large_square(), device)
+    if name.startswith("q_down_m"):
+        return DenseWork(synth.q_down(int(name[len("q_down_m"):])), device)
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ---------------------------------------------------------------- timing
+
+def capture(fn, count: int, start: int = 0):
+    """CUDA graph of `count` consecutive calls fn(start), fn(start+1), ..."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(count):
+            fn(start + i)
+    return g
+
+
+def replay_timed(graphs, world, device):
+    """Replay graphs between events, bracketed by barrier + synchronize.
+    Returns milliseconds (max over ranks)."""
+    import torch
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for g in graphs:
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1), world, device)
+
+
+def chunked_graphs(fn, total: int, chunk: int = 200):
+    graphs = []
+    done = 0
+    while done < total:
+        n = min(chunk, total - done)
+        graphs.append(capture(fn, n, done))
+        done += n
+    return graphs
+
+
+def run_ours(args, rank, local, world):
+    import torch
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    from fp8_block_scaled_18_b300 import fp8bs as F
+
+    peaks, peaks_src = load_peaks()
+    work = make_work(args.workload, device)
+    # eager warm-up (also loads modules and sets kernel attributes before capture)
+    for i in range(max(3, work.R)):
+        work.step(i)
+    st = F.fp8bs_sync_status()
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: {F.fp8bs_status_string(st)}")
+
+    K, W = args.steps, max(3, args.warmup)
+    step_graphs = chunked_graphs(work.step, K)
+    warm_graphs = chunked_graphs(work.step, W)
+    kernel_graphs = {k: chunked_graphs(lambda i, k=k: work.kernels[k][0](work.sets[i % work.R]
+                                                                         if hasattr(work, "sets") else None), K)
+                     for k in work.order}
+
+    with ClockSampler(local) as clocks:
+        # soak: ~1 s of steps so the clock record covers sustained load
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for g in warm_graphs:
+                g.replay()
+            torch.cuda.synchronize()
+        for g in warm_graphs:  # W untimed warm-up steps
+            g.replay()
+        step_ms = replay_timed(step_graphs, world, device)
+        kernel_ms = {k: replay_timed(kernel_graphs[k], world, device) for k in work.order}
+    clock = clocks.summary()
+    st = F.fp8bs_sync_status()
+    if st != 0:
+        raise SystemExit(f"device status after timing: {F.fp8bs_status_string(st)}")
+
+    ms_per_step = step_ms / K
+    total_flops = sum_over_ranks(work.flops * K, world, device)
+    value = total_flops / (step_ms * 1e-3) / 1e12
+
+    # per-kernel roofline rows
+    hbm_peak = float(peaks["hbm_gbs"])
+    fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
+    kernels = {}
+    for k in work.order:
+        _, launches, units, bound = work.kernels[k]
+        per_call_s = kernel_ms[k] / K * 1e-3
+        if bound == "tensor":
+            ach, peak, unit = units / per_call_s / 1e12, fp8_peak, "TFLOP/s"
+        else:
+            ach, peak, unit = units / per_call_s / 1e9, hbm_peak, "GB/s"
+        kernels[k] = {"us_per_call": round(per_call_s * 1e6, 3), "launches_per_call": launches,
+                      "achieved": round(ach, 2), "unit": unit, "bound": bound,
+                      "frac": round(ach / peak, 4), "share": round(kernel_ms[k] / sum(kernel_ms.values()), 4)}
+    if "fp8_gemm" in kernels:
+        kernels["fp8_gemm"]["tflops"] = kernels["fp8_gemm"]["achieved"]
+    dom = max(work.order, key=lambda k: kernel_ms[k])
+    _, launches, units, bound = work.kernels[dom]
+    dom_s = kernel_ms[dom] / K * 1e-3
+    if bound == "tensor":
+        roof = {"bound": "tensor", "achieved": units / dom_s / 1e12, "peak": fp8_peak, "unit": "TFLOP/s"}
+        peak_note = f"{peaks_src} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio)"
+    else:
+        roof = {"bound": "hbm", "achieved": units / dom_s / 1e9, "peak": hbm_peak, "unit": "GB/s"}
+        peak_note = f"{peaks_src} HBM copy bandwidth"
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(dom, work.config()["workload"])
+    roof["kernel"] = dom
+    roof["peak_source"] = peak_note
+    roof["algorithmic_per_launch"] = units
+    for key in ("achieved", "peak", "frac"):
+        roof[key] = round(roof[key], 4)
+
+    # end to end through the public calls with pinned host buffers
+    work.e2e_setup()
+    for i in range(W):
+        work.e2e_step(i)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        work.e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 MMA, fp32 promote, bf16 out", "data": "synthetic (seeded numpy / torch RNG)",
+        "config": {**work.config(), "parallelism": f"replicas{world}", "timing": "CUDA graphs of K steps"},
+        "roofline": roof, "kernels": kernels,
+        "act_quant_gbs": kernels.get("act_quant", {}).get("achieved"),
+        "act_quant_hbm_frac": kernels.get("act_quant", {}).get("frac"),
+        "clocks": clock,
+        "e2e": {"value": round(e2e_value, 4), "unit": "TFLOP/s", "h2d_bytes_per_step": work.h2d,
+                "d2h_bytes_per_step": work.d2h, "api": "fp8bs_* C ABI via the Python binding, eager, pinned host"},
+        "gpu_launches": K * work.launches_per_step(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- oracle legs
+
+def oracle_sample_step(orc, case, rows):
+    """One bounded oracle pass: weight_quant + act_quant(rows) + gemm(rows) +
+    weight_dequant for a dense case; returns the GEMM flops done."""
+    wq, sw = orc.weight_quant(case.w)
+    xq, sx = orc.act_quant(case.x[rows])
+    orc.gemm(xq, sx, wq, sw)
+    orc.weight_dequant(wq, sw)
+    return 2.0 * len(rows) * case.w.shape[0] * case.x.shape[1]
+
+
+def oracle_moe_step(orc, case, experts, x_rows, rows_per_expert):
+    import torch
+    from fp8_block_scaled_18_b300 import synth
+    flops = 0.0
+    for g in experts:
+        r0, r1 = int(case.offsets[g]), int(case.offsets[g + 1])
+        rows = np.arange(r0, min(r1, r0 + rows_per_expert))
+        wb = synth.expert_weight(case, g, "cpu").view(torch.int16).numpy().view(np.uint16)
+        wq, sw = orc.weight_quant(wb)
+        xq, sx = orc.act_quant(x_rows[rows])
+        orc.gemm(xq, sx, wq, sw)
+        flops += 2.0 * len(rows) * case.n * case.k
+    return flops
+
+
+def make_case(workload: str):
+    from fp8_block_scaled_18_b300 import synth
+    if workload == "kv_down":
+        return synth.kv_down()
+    if workload == "tiny":
+        return synth.tiny()
+    if workload == "large_square":
+        return synth.large_square()
+    if workload.startswith("q_down_m"):
+        return synth.q_down(int(workload[len("q_down_m"):]))
+    raise SystemExit(f"unknown workload {workload}")
+
+
+def oracle_rows_for(orc, case, seconds: float) -> int:
+    """Rows of a dense case whose oracle pass takes about `seconds`
+    (fixed weight-side cost + per-row GEMM cost, measured on 1 and 5 rows)."""
+    M = case.x.shape[0]
+    t0 = time.perf_counter()
+    oracle_sample_step(orc, case, np.array([0]))
+    t1 = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle_sample_step(orc, case, np.arange(5) % M)
+    t5 = time.perf_counter() - t0
+    per_row = max((t5 - t1) / 4, 1e-4)
+    fixed = max(t1 - per_row, 0.0)
+    return int(max(1, min(M, (seconds - fixed) / per_row)))
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(workload: str, seconds: float) -> dict:
+    """The oracle as it stands, single-threaded C, on a bounded sample."""
+    from fp8_block_scaled_18_b300 import synth
+    from oracle import Oracle
+    orc = Oracle()
+    if workload == "moe":
+        case = synth.moe()
+        counts = np.diff(case.offsets)
+        x_rows = case.x_rows
+        experts = np.nonzero(counts)[0]
+        t0 = time.perf_counter()
+        flops, n = 0.0, 0
+        while time.perf_counter() - t0 < seconds and n < len(experts):
+            flops += oracle_moe_step(orc, case, [experts[n]], x_rows, 32)
+            n += 1
+        dt = time.perf_counter() - t0
+        sample = f"{n} experts x <=32 rows: weight_quant of the expert, act_quant, gemm"
+    else:
+        case = make_case(workload)
+        M = case.x.shape[0]
+        rows = oracle_rows_for(orc, case, seconds)
+        sel = np.linspace(0, M - 1, rows).astype(np.int64)
+        t0 = time.perf_counter()
+        flops = oracle_sample_step(orc, case, sel)
+        dt = time.perf_counter() - t0
+        sample = (f"{rows} of {M} rows: weight_quant(W) + act_quant(rows) + gemm(rows) + weight_dequant(W), "
+                  f"TFLOP/s over the sampled GEMM work")
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "host_cores_available": cpu_cores(),
+            "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+
+
+def run_reference(args, rank, local, world):
+    """The base contract's reference arm for this build: the CPU oracle, timed
+    as it stands on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    from fp8_block_scaled_18_b300 import synth
+    from oracle import Oracle
+    orc = Oracle()
+    K, W = args.steps, max(3, args.warmup)
+    budget = 150.0  # seconds for the whole run
+    if args.workload == "moe":
+        case = synth.moe()
+        counts = np.diff(case.offsets)
+        x_rows = case.x_rows
+        experts = np.nonzero(counts)[0]
+        t0 = time.perf_counter()
+        oracle_moe_step(orc, case, experts[:1], x_rows, 1)
+        one = time.perf_counter() - t0
+        rows = max(1, int(budget / (K + W) / max(one, 1e-3)))
+        step = lambda i: oracle_moe_step(orc, case, [experts[i % len(experts)]], x_rows, rows)  # noqa: E731
+        sample = f"one expert per step (weight_quant, act_quant and gemm of <= {rows} rows)"
+        cfg = {"workload": "moe_grouped"}
+    else:
+        case = make_case(args.workload)
+        M = case.x.shape[0]
+        rows = oracle_rows_for(orc, case, budget / (K + W))
+        step = lambda i: oracle_sample_step(orc, case, (np.arange(rows) + i * rows) % M)  # noqa: E731
+        sample = (f"{rows} of {M} rows per step: weight_quant(W) + act_quant(rows) + gemm(rows) + "
+                  f"weight_dequant(W)")
+        M_, N_, K_ = case.shape
+        cfg = {"workload": case.name, "M": M_, "N": N_, "K": K_}
+    for i in range(W):
+        step(i)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for i in range(K):
+        flops += step(i)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": dt / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp64 oracle (fp32 quantisation)", "data": "synthetic", "impl": "reference",
+            "config": {**cfg, "parallelism": "cpu oracle, rank 0"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle", "cores": 1,
+                             "host_cores_available": cpu_cores(), "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, local, world = dist_env()
+    if world != args.gpus and world != 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, local, world)
+    else:
+        run_ours(args, rank, local, world)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
