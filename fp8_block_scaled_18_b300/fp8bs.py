@@ -33,6 +33,7 @@ _SIGS = {
     "fp8bs_weight_dequant": (_ST, [_P, _P, _I64, _I64, _P, _P]),
     "fp8bs_gemm": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P]),
     "fp8bs_gemm_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "fp8bs_gemm_noalloc": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm": (_ST, [_P, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_sync_status": (_ST, [_P]),
     "fp8bs_status_string": (ctypes.c_char_p, [_ST]),
@@ -174,6 +175,19 @@ def fp8bs_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.T
                           _dev(wq, torch.uint8, "wq"), _dev(sw, torch.float32, "sw"), M, N, K,
                           _bf16_ptr(y, "y"), _rows_stride(y, "y"), ws_ptr, ws_bytes, _stream(stream)),
            "fp8bs_gemm")
+    return y
+
+
+def fp8bs_gemm_noalloc(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
+                       y: torch.Tensor, stream=None) -> torch.Tensor:
+    """fp8bs_gemm for callers that cannot allocate: the library takes its
+    split-K scratch from a fixed device array; y must be supplied."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _check(lib.fp8bs_gemm_noalloc(_dev(xq, torch.uint8, "xq"), _dev(sx, torch.float32, "sx"),
+                                  _rows_stride(sx, "sx"), _dev(wq, torch.uint8, "wq"),
+                                  _dev(sw, torch.float32, "sw"), M, N, K, _bf16_ptr(y, "y"),
+                                  _rows_stride(y, "y"), _stream(stream)), "fp8bs_gemm_noalloc")
     return y
 
 

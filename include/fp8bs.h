@@ -24,8 +24,8 @@
  *   - K must be a multiple of 128.  Row-major everywhere ("ld*" = row stride
  *     in elements).  All pointers are DEVICE pointers owned by the caller; the
  *     library keeps none of them after the call returns and allocates no
- *     device memory in any call (it holds one small static status word per
- *     device).
+ *     device memory in any call (it holds a small static status word per
+ *     device, and the fixed scratch array of fp8bs_gemm_noalloc).
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
  *     Argument errors are returned synchronously and launch nothing.  Errors
  *     inside a kernel (a bounded pipeline wait that expired) are recorded in
@@ -124,6 +124,28 @@ fp8bs_status fp8bs_grouped_gemm(const uint8_t* xq, const float* sx, int64_t lds,
                                 const int32_t* offsets_dev, int32_t G, int64_t total_M,
                                 int64_t N, int64_t K, uint16_t* y, int64_t ldy,
                                 fp8bs_stream_t stream);
+
+/* fp8_gemm for callers that cannot allocate device memory -- code running
+ * inside an allocator's or memory pool's own callback, plugin hosts that pass
+ * a library only its input and output buffers, and latency-critical paths
+ * that must not trigger a (possibly synchronising) device allocation.  The
+ * DeepSeek-V3 pages have no counterpart: this is an interface for such
+ * callers, computing exactly what fp8bs_gemm computes.
+ * Same arguments and results as fp8bs_gemm without the workspace: the
+ * split-K scratch of the small-M plan comes from a fixed array of
+ * FP8BS_NOALLOC_SCRATCH_BYTES inside the library's device image (every device
+ * that loads the library holds it until the process exits).  Returns
+ * FP8BS_ERR_UNSUPPORTED, launching nothing, when the shape's plan needs more
+ * scratch than that (fp8bs_gemm_workspace_size(M, N, K) > the maximum).
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls on a device share the array: calls whose kernels overlap on the GPU
+ * race and must be serialised by the caller.  Allocates nothing. */
+#define FP8BS_NOALLOC_SCRATCH_BYTES (16u << 20)
+fp8bs_status fp8bs_gemm_noalloc(const uint8_t* xq, const float* sx, int64_t lds,
+                                const uint8_t* wq, const float* sw,
+                                int64_t M, int64_t N, int64_t K,
+                                uint16_t* y, int64_t ldy, fp8bs_stream_t stream);
 
 /* Synchronise `stream`, then report and clear this device's status word:
  * FP8BS_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,
