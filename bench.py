@@ -60,6 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of untimed steps before the warm-up, so the clock record sees sustained load")
     return ap.parse_args(argv)
 
 
@@ -410,7 +412,7 @@ def run_ours(args, rank, local, world):
 
     with ClockSampler(local) as clocks:
         # soak: ~1 s of steps so the clock record covers sustained load
-        t_end = time.time() + 1.0
+        t_end = time.time() + args.soak
         while time.time() < t_end:
             for g in warm_graphs:
                 g.replay()

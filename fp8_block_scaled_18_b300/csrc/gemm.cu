@@ -8,22 +8,29 @@
 // four K=32 MMAs, after the Float8 paragraph of the 88811315.cn post and the
 // "FP8 量化" section of the qdgithub overview.)
 //
-// Design (one persistent CTA per SM, 384 threads, warp-specialised):
+// Design (one persistent CTA per SM, 384 threads = 3 warpgroups, warp-specialised):
 //   warp 0      TMA producer: A (128 x 128 B) and B (BN x 128 B) tiles of one
 //               K chunk per pipeline stage, 128-byte swizzled, mbarrier
 //               completion by byte count.
 //   warp 1      TMEM owner and MMA issuer: per chunk, four
-//               tcgen05.mma.kind::f8f6f4 (M=128, N=BN, K=32) into one of two
-//               TMEM buffers of BN fp32 columns, then tcgen05.commit to free
-//               the smem stage and to publish the chunk.
+//               tcgen05.mma.kind::f8f6f4 (M=128, N=BN, K=32) into one of
+//               512/BN TMEM buffers of BN fp32 columns, then tcgen05.commit to
+//               free the smem stage and to publish the chunk.
 //   warps 4-11  promotion + epilogue: two warpgroups, each owning BN/2
-//               columns; thread = one row.  Per chunk: tcgen05.ld the raw
+//               columns; thread = one row (TMEM lane).
+// With BN = 256 every promotion thread keeps 128 fp32 accumulators, so the
+// warpgroups rebalance registers after set-up (setmaxnreg): the TMA/MMA
+// warpgroup drops to kRegsSetup, the promotion warpgroups rise to kRegsPromo.
+// Per SM sub-partition (one set-up warp + two promotion warps) that is
+// kRegsSetup + 2 * kRegsPromo = 3 * kRegsLaunch registers per lane, exactly
+// what the launch reserved; the host refuses the kernel unless its compiled
+// register count is kRegsLaunch.  Per chunk: tcgen05.ld the raw
 //               chunk sum P_kb, acc += fp32(sx*sw) * P_kb in registers (one
 //               FFMA per element), release the TMEM buffer.  After the last
 //               chunk of a tile: round to bf16 and store (or store fp32
 //               partials for split-K).
-// The TMEM double buffer lets the tensor core run chunk kb+1 while the CUDA
-// cores promote chunk kb.
+// The TMEM buffers let the tensor core run up to 512/BN - 1 chunks ahead of
+// the CUDA cores that promote them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -42,6 +49,10 @@ constexpr int BK = 128;           // K chunk = one scale block = 4 MMAs of K=32
 constexpr int UMMA_K = 32;
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;      // first promotion/epilogue warp
+constexpr int kRegsLaunch = 168;  // 65536 / 384, rounded down to a multiple of 8
+constexpr int kRegsSetup = 56;
+constexpr int kRegsPromo = 224;
+static_assert(kRegsSetup + 2 * kRegsPromo == 3 * kRegsLaunch, "register split must match the launch");
 constexpr int kEpiWarps = 8;
 constexpr int kGroupM = 16;       // dense raster: 16 m-tiles share a sweep over n
 constexpr int kMaxGroups = 1024;
@@ -53,17 +64,18 @@ struct Layout {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
-    static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;   // full[S], empty[S], tfull[2], tempty[2], done
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int NBUF = 512 / BN;                       // TMEM chunk buffers (all 512 columns)
+    static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;   // full[S], empty[S], tfull[NBUF], tempty[NBUF], done
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_TABLE = (OFF_ABORT + 4 + 15) & ~15;  // grouped: tile prefix [G+1]
     static constexpr int TABLE_BYTES = (kMaxGroups + 1) * 4;
     static constexpr int BYTES = OFF_TABLE + TABLE_BYTES;
     static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
-    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr uint32_t TMEM_COLS = NBUF * BN;
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
-    static_assert(TMEM_COLS <= 512, "two chunk buffers must fit in TMEM");
+    static_assert(NBUF >= 2 && TMEM_COLS == 512, "chunk buffers fill TMEM");
 };
 
 struct Params {
@@ -209,9 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar0 = sbase + L::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    constexpr int NBUF = L::NBUF;
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + NBUF + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 2 * NBUF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
     int* prefix = reinterpret_cast<int*>(smem + L::OFF_TABLE);
 
@@ -220,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NBUF; ++b) {
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), kEpiWarps);
         }
@@ -229,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
-    if (GROUPED && warp == 2) build_tile_table<BN>(p, prefix, lane);
+    if (GROUPED && warp == kEpiWarp0) build_tile_table<BN>(p, prefix, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -237,9 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_tiles = GROUPED ? prefix[p.G] : p.num_tiles;
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
 
+
     auto tile_of = [&](int t) { return GROUPED ? grouped_tile<BN>(p, prefix, t) : dense_tile<BN>(p, t); };
 
-    if (warp == 0) {
+    if (warp < kEpiWarp0) {
+      if (BN > 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSetup));
+      if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
@@ -274,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t sph = (it / STAGES) & 1u;
-                const int b = it & 1;
-                const uint32_t bph = (it >> 1) & 1u;
+                const int b = it % NBUF;
+                const uint32_t bph = (it / NBUF) & 1u;
                 if (!warp_wait(tempty_bar(b), bph ^ 1u, ctl)) { ok = false; break; }
                 if (!warp_wait(full_bar(s), sph, ctl)) { ok = false; break; }
                 tc_fence_after();
@@ -299,8 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             drain_wait(done_bar, 0, ctl);
         }
-    } else if (warp >= kEpiWarp0) {
+      }
+    } else {
         // ------------------------------------------------------------ promotion + epilogue
+        if (BN > 128) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
         constexpr int COLS = BN / 2;        // columns per warpgroup
         constexpr int NCH = COLS / 32;      // 32-column TMEM loads per chunk
         const int ew = warp - kEpiWarp0;
@@ -316,10 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int m = tl.m0 + row;
             const bool row_ok = m < tl.m_end;
             const float* sxr = p.sx + static_cast<int64_t>(row_ok ? m : 0) * p.lds;
+            // weight-scale row of each 32-column slice (a slice never straddles
+            // a 128-column block); slices past N read row 0 and are never stored
             const float* swr[NCH];
 #pragma unroll
-            for (int c = 0; c < NCH; ++c)
-                swr[c] = p.sw + static_cast<int64_t>(tl.sw_row + (col0 + 32 * c) / 128) * p.KB;
+            for (int c = 0; c < NCH; ++c) {
+                const bool in_n = tl.n0 + col0 + 32 * c < p.N;
+                swr[c] = p.sw + static_cast<int64_t>(in_n ? tl.sw_row + (col0 + 32 * c) / 128 : 0) * p.KB;
+            }
             float acc[COLS];
 #pragma unroll
             for (int i = 0; i < COLS; ++i) acc[i] = 0.0f;
@@ -330,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < NCH; ++c) sw_next[c] = __ldg(swr[c] + tl.kb0);
 
             for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
-                const int b = it & 1;
-                const uint32_t bph = (it >> 1) & 1u;
+                const int b = it % NBUF;
+                const uint32_t bph = (it / NBUF) & 1u;
                 const float sxv = sx_next;
                 float swv[NCH];
 #pragma unroll
@@ -345,23 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * BN + col0);
 #pragma unroll
-                for (int c = 0; c < NCH; c += 2) {
-                    uint32_t r[64];
-                    if (c + 1 < NCH) {
-                        tmem_ld_32x32b_x64(taddr + 32u * c, reinterpret_cast<uint32_t(&)[64]>(r));
-                    } else {
-                        tmem_ld_32x32b_x32(taddr + 32u * c, reinterpret_cast<uint32_t(&)[32]>(r));
-                    }
-                    const float f0 = __fmul_rn(sxv, swv[c]);
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + 32u * c, r);
+                    const float f = __fmul_rn(sxv, swv[c]);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        acc[32 * c + i] = __fmaf_rn(f0, __uint_as_float(r[i]), acc[32 * c + i]);
-                    if (c + 1 < NCH) {
-                        const float f1 = __fmul_rn(sxv, swv[c + 1]);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[32 * (c + 1) + i] = __fmaf_rn(f1, __uint_as_float(r[32 + i]), acc[32 * (c + 1) + i]);
-                    }
+                        acc[32 * c + i] = __fmaf_rn(f, __uint_as_float(r[i]), acc[32 * c + i]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -492,8 +504,8 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-constexpr int kBN = 128;
-constexpr int kStages = 6;
+constexpr int kBN = 256;
+constexpr int kStages = 4;
 
 struct Plan {
     int splits;
@@ -518,14 +530,23 @@ Plan dense_plan(int64_t M, int64_t N, int64_t K, int num_sms, size_t ws_cap) {
 }
 
 template <int BN, int STAGES, bool GROUPED>
-cudaError_t ensure_smem_attr(int device) {
+cudaError_t ensure_kernel_ready(int device) {
     static std::mutex mu;
     static bool done[64];
     std::lock_guard<std::mutex> g(mu);
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!done[device]) {
-        cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, STAGES, GROUPED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+        auto* k = fp8_gemm_kernel<BN, STAGES, GROUPED>;
+        if (BN > 128) {
+            // The setmaxnreg split assumes exactly kRegsLaunch registers per
+            // thread at launch; any other count could leave a warpgroup
+            // waiting for registers that never free up.
+            cudaFuncAttributes attr;
+            cudaError_t e = cudaFuncGetAttributes(&attr, k);
+            if (e != cudaSuccess) return e;
+            if (attr.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
+        }
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Layout<BN, STAGES>::ALLOC);
         if (e != cudaSuccess) return e;
         done[device] = true;
@@ -565,7 +586,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
         p.G = a.G;
         p.splits = 1;
         p.kps = p.KB;
-        if ((e = ensure_smem_attr<BN, STAGES, true>(dev.device)) != cudaSuccess) return e;
+        if ((e = ensure_kernel_ready<BN, STAGES, true>(dev.device)) != cudaSuccess) return e;
         fp8_gemm_kernel<BN, STAGES, true><<<dev.num_sms, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
         return cudaGetLastError();
     }
@@ -576,7 +597,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
     p.kps = pl.kps;
     p.num_tiles = p.MT * p.NT * p.splits;
     p.partial = pl.splits > 1 ? static_cast<float*>(a.workspace) : nullptr;
-    if ((e = ensure_smem_attr<BN, STAGES, false>(dev.device)) != cudaSuccess) return e;
+    if ((e = ensure_kernel_ready<BN, STAGES, false>(dev.device)) != cudaSuccess) return e;
     const int grid = std::min(p.num_tiles, dev.num_sms);
     fp8_gemm_kernel<BN, STAGES, false><<<grid, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -18,12 +18,40 @@ constexpr float kE4M3Max = 448.0f;
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// Code of one element given its group's amax and scale.
-__device__ __forceinline__ float quotient(float x, float s) { return __fdiv_rn(x, s); }
+// The quotient RN32(x / s) of one element, given its group's scale s and
+// r = RN32(1 / s).  Markstein's correction step (P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): q0 = RN(x r), rem = x - s q0 (exact with one fused
+// multiply-add), q = RN(q0 + rem r).  The result is re-signed from x so that
+// -0 stays -0.  Groups whose scale is so small that 1/s could overflow use the
+// IEEE division instead (`exact_div`).  Bit-exactness against RN32(x / s) is
+// checked exhaustively over every bf16 amax and every bf16 x with |x| <= amax.
+__device__ __forceinline__ float quotient(float x, float s, float r, bool exact_div) {
+    if (exact_div) return __fdiv_rn(x, s);
+    const float q0 = __fmul_rn(x, r);
+    const float rem = __fmaf_rn(-q0, s, x);
+    const float q = __fmaf_rn(rem, r, q0);
+    return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// Scale-side constants of one group: r = RN(1/s); the reciprocal path is used
+// only while 1/s stays far from overflow (s >= 2^-100).
+struct GroupScale {
+    float s, r;
+    bool exact_div;
+};
+
+__device__ __forceinline__ GroupScale group_scale(float amax) {
+    GroupScale g;
+    g.s = __fdiv_rn(amax, kE4M3Max);
+    g.exact_div = !(g.s >= 7.888609052210118e-31f);  // 2^-100; also true for s == 0
+    g.r = g.exact_div ? 0.0f : __frcp_rn(g.s);
+    return g;
+}
 
 // Encode 8 fp32 values (x / s) into 8 e4m3 bytes (little-endian in a uint2).
 // zero_group: every code is +-0 with the input's sign.
-__device__ __forceinline__ uint2 encode8(const float (&x)[8], float s, bool zero_group) {
+__device__ __forceinline__ uint2 encode8(const float (&x)[8], const GroupScale& gs, bool zero_group) {
     uint32_t w[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -35,8 +63,10 @@ __device__ __forceinline__ uint2 encode8(const float (&x)[8], float s, bool zero
             lo = b[0] | (b[1] << 8);
             hi = b[2] | (b[3] << 8);
         } else {
-            lo = cvt_e4m3x2(quotient(x[4 * h + 0], s), quotient(x[4 * h + 1], s));
-            hi = cvt_e4m3x2(quotient(x[4 * h + 2], s), quotient(x[4 * h + 3], s));
+            lo = cvt_e4m3x2(quotient(x[4 * h + 0], gs.s, gs.r, gs.exact_div),
+                            quotient(x[4 * h + 1], gs.s, gs.r, gs.exact_div));
+            hi = cvt_e4m3x2(quotient(x[4 * h + 2], gs.s, gs.r, gs.exact_div),
+                            quotient(x[4 * h + 3], gs.s, gs.r, gs.exact_div));
         }
         w[h] = lo | (hi << 16);
     }
@@ -99,12 +129,12 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
         if (valid) {
-            const float s = __fdiv_rn(amax, kE4M3Max);
+            const GroupScale gs = group_scale(amax);
             const bool zero = (amax == 0.0f);
             uint8_t* q = xq + m * ldq + kb * 128;
-            *reinterpret_cast<uint2*>(q + sub * 8) = encode8(a, s, zero);
-            *reinterpret_cast<uint2*>(q + 64 + sub * 8) = encode8(b, s, zero);
-            if (sub == 0) sx[m * lds + kb] = s;
+            *reinterpret_cast<uint2*>(q + sub * 8) = encode8(a, gs, zero);
+            *reinterpret_cast<uint2*>(q + 64 + sub * 8) = encode8(b, gs, zero);
+            if (sub == 0) sx[m * lds + kb] = gs.s;
         }
     }
 }
@@ -122,15 +152,18 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __res
     const int t = threadIdx.x;
     const int chunk = t & 15;
     const int r0 = t >> 4;
-    float v[8][8];
+    uint4 raw[8];  // the block stays in registers as packed bf16 (32 registers)
     float amax = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 16 * j;
-        if (n < N) {
-            unpack8(ld_stream(w + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8), v[j]);
-            amax = absmax8(v[j], amax);
-        }
+        raw[j] = n < N ? ld_stream(w + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float v[8];
+        unpack8(raw[j], v);
+        amax = absmax8(v, amax);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -139,16 +172,19 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __res
     amax = warp_max[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
-    const float s = __fdiv_rn(amax, kE4M3Max);
+    const GroupScale gs = group_scale(amax);
     const bool zero = (amax == 0.0f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 16 * j;
-        if (n < N)
+        if (n < N) {
+            float v[8];
+            unpack8(raw[j], v);
             *reinterpret_cast<uint2*>(wq + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8) =
-                encode8(v[j], s, zero);
+                encode8(v, gs, zero);
+        }
     }
-    if (t == 0) sw[static_cast<int64_t>(nb) * KB + kb] = s;
+    if (t == 0) sw[static_cast<int64_t>(nb) * KB + kb] = gs.s;
 }
 
 // ---------------------------------------------------------------- weight_dequant

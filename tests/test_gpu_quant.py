@@ -165,3 +165,52 @@ def test_e4m3_encoder_exhaustive(F, orc):
         ok = (got == want) | (nan_in & ((got & 0x7F) == 0x7F))
         bad = np.nonzero(~ok)[0]
         assert bad.size == 0, [(hex(int(bits[i])), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+def _every_pair_batches(elems_per_batch=1 << 27):
+    """Groups [amax, x_1 .. x_127] covering, for every positive finite bf16
+    amax, every bf16 x (both signs) with |x| <= amax; yielded in batches of
+    rows of 1024 elements (8 groups)."""
+    codes = np.arange(0x0001, 0x7F80, dtype=np.uint32)   # positive finite bf16, increasing value
+    pending, size = [], 0
+    for c in codes:
+        mags = np.arange(0, c + 1, dtype=np.uint32)
+        xs = np.concatenate([mags, mags | 0x8000]).astype(np.uint16)
+        n_groups = -(-xs.size // 127)
+        g = np.zeros((n_groups, 128), np.uint16)
+        g[:, 0] = c
+        g[:, 1:].reshape(-1)[: xs.size] = xs
+        pending.append(g)
+        size += g.size
+        if size >= elems_per_batch:
+            yield _rows_of_1024(pending)
+            pending, size = [], 0
+    if pending:
+        yield _rows_of_1024(pending)
+
+
+def _rows_of_1024(groups):
+    flat = np.concatenate(groups).reshape(-1)
+    pad = (-flat.size) % 1024
+    if pad:
+        flat = np.concatenate([flat, np.zeros(pad, np.uint16)])
+    return flat.reshape(-1, 1024)
+
+
+def test_act_quant_every_amax_x_pair(F, orc):
+    """Exhaustive over the quantisers' arithmetic domain: for every positive
+    finite bf16 amax and every bf16 x with |x| <= amax (about 1.07e9 pairs),
+    the device codes and scales equal the oracle's RN32(x / (amax/448))
+    encoding bit for bit.  The group's other members do not enter x's code,
+    so this covers every input of act_quant and weight_quant."""
+    total = 0
+    for xb in _every_pair_batches():
+        x = dev_bf16(xb)
+        xq, sx = F.fp8bs_act_quant(x)
+        assert F.fp8bs_sync_status() == 0
+        xq_ref, sx_ref = orc.act_quant(xb, lds=sx.shape[1])
+        assert_bits_equal(host(xq), xq_ref, "xq")
+        assert_bits_equal(host(sx)[:, :8], sx_ref[:, :8], "sx")
+        total += xb.size
+        del x, xq, sx
+    assert total > 1_000_000_000
