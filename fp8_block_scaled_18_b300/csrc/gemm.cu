@@ -105,11 +105,14 @@ struct Tile {
     int split;
 };
 
-template <int BN>
+template <int BN, bool SPLITK>
 __device__ __forceinline__ Tile dense_tile(const Params& p, int t) {
     Tile tl;
-    tl.split = t % p.splits;
-    t /= p.splits;
+    tl.split = 0;
+    if (SPLITK) {
+        tl.split = t % p.splits;
+        t /= p.splits;
+    }
     const int per_group = kGroupM * p.NT;
     const int grp = t / per_group;
     const int first_m = grp * kGroupM;
@@ -122,8 +125,8 @@ __device__ __forceinline__ Tile dense_tile(const Params& p, int t) {
     tl.n0 = nt * BN;
     tl.b_row = tl.n0;
     tl.sw_row = tl.n0 / 128;
-    tl.kb0 = tl.split * p.kps;
-    tl.kb1 = min(p.KB, tl.kb0 + p.kps);
+    tl.kb0 = SPLITK ? tl.split * p.kps : 0;
+    tl.kb1 = SPLITK ? min(p.KB, tl.kb0 + p.kps) : p.KB;
     return tl;
 }
 
@@ -205,7 +208,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int BN, int STAGES, bool GROUPED>
+// MODE: how tiles map to work.
+enum : int { kDense = 0, kDenseSplitK = 1, kGrouped = 2 };
+
+template <int BN, int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ Params p) {
@@ -242,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
+    constexpr bool GROUPED = MODE == kGrouped;
+    constexpr bool SPLITK = MODE == kDenseSplitK;
     if (GROUPED && warp == kEpiWarp0) build_tile_table<BN>(p, prefix, lane);
     tc_fence_before();
     __syncthreads();
@@ -251,7 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
 
 
-    auto tile_of = [&](int t) { return GROUPED ? grouped_tile<BN>(p, prefix, t) : dense_tile<BN>(p, t); };
+    auto tile_of = [&](int t) {
+        return GROUPED ? grouped_tile<BN>(p, prefix, t) : dense_tile<BN, SPLITK>(p, t);
+    };
 
     if (warp < kEpiWarp0) {
       if (BN > 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSetup));
@@ -334,46 +344,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int m = tl.m0 + row;
             const bool row_ok = m < tl.m_end;
             const float* sxr = p.sx + static_cast<int64_t>(row_ok ? m : 0) * p.lds;
-            // weight-scale row of each 32-column slice (a slice never straddles
-            // a 128-column block); slices past N read row 0 and are never stored
-            const float* swr[NCH];
+            // weight-scale row of this warpgroup's columns: they lie inside one
+            // 128-column block; a warpgroup entirely past N reads row 0 and
+            // stores nothing
+            const bool wg_in_n = tl.n0 + col0 < p.N;
+            const float* swr = p.sw + static_cast<int64_t>(wg_in_n ? tl.sw_row + col0 / 128 : 0) * p.KB;
+            // running sums as packed fp32 pairs: acc[j] = (column 2j, column 2j+1)
+            uint64_t acc[COLS / 2];
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                const bool in_n = tl.n0 + col0 + 32 * c < p.N;
-                swr[c] = p.sw + static_cast<int64_t>(in_n ? tl.sw_row + (col0 + 32 * c) / 128 : 0) * p.KB;
-            }
-            float acc[COLS];
-#pragma unroll
-            for (int i = 0; i < COLS; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
 
             float sx_next = row_ok ? __ldg(sxr + tl.kb0) : 0.0f;
-            float sw_next[NCH];
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) sw_next[c] = __ldg(swr[c] + tl.kb0);
+            float sw_next = __ldg(swr + tl.kb0);
 
             for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
                 const int b = it % NBUF;
                 const uint32_t bph = (it / NBUF) & 1u;
-                const float sxv = sx_next;
-                float swv[NCH];
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) swv[c] = sw_next[c];
+                const float f = __fmul_rn(sx_next, sw_next);  // fp32(sx * sw) of this chunk
                 if (kb + 1 < tl.kb1) {
                     sx_next = row_ok ? __ldg(sxr + kb + 1) : 0.0f;
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) sw_next[c] = __ldg(swr[c] + kb + 1);
+                    sw_next = __ldg(swr + kb + 1);
                 }
                 if (!warp_wait(tfull_bar(b), bph, ctl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * BN + col0);
+                // promotion: acc += f * P_kb, slice by slice of 32 columns; the
+                // TMEM load of slice c+1 overlaps the FMAs of slice c
+                const uint64_t f2 = pack_f32x2(f, f);
+                uint64_t bufA[16], bufB[16];  // slices alternate between two buffers
+                tmem_ld_x32_pairs(taddr, bufA);
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + 32u * c, r);
-                    const float f = __fmul_rn(sxv, swv[c]);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc[32 * c + i] = __fmaf_rn(f, __uint_as_float(r[i]), acc[32 * c + i]);
+                    uint64_t(&a)[16] = *reinterpret_cast<uint64_t(*)[16]>(&acc[16 * c]);
+                    uint64_t(&cur)[16] = (c & 1) ? bufB : bufA;
+                    uint64_t(&nxt)[16] = (c & 1) ? bufA : bufB;
+                    if (c + 1 < NCH)
+                        tmem_ld_x32_pairs_fma(taddr + 32u * (c + 1), nxt, a, cur, f2);
+                    else
+                        fma_pairs(a, cur, f2);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -382,23 +390,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (!row_ok) continue;
             const int nbase = tl.n0 + col0;
-            if (p.partial == nullptr) {
+            if (!SPLITK) {
                 uint16_t* yr = p.y + static_cast<int64_t>(m) * p.ldy;
 #pragma unroll
                 for (int v = 0; v < COLS / 8; ++v) {
                     const int n = nbase + 8 * v;
                     if (n + 8 <= p.N) {
                         uint4 o;
-                        o.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
-                        o.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
-                        o.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
-                        o.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
+                        o.x = pack_bf16x2(lo_f32(acc[4 * v + 0]), hi_f32(acc[4 * v + 0]));
+                        o.y = pack_bf16x2(lo_f32(acc[4 * v + 1]), hi_f32(acc[4 * v + 1]));
+                        o.z = pack_bf16x2(lo_f32(acc[4 * v + 2]), hi_f32(acc[4 * v + 2]));
+                        o.w = pack_bf16x2(lo_f32(acc[4 * v + 3]), hi_f32(acc[4 * v + 3]));
                         *reinterpret_cast<uint4*>(yr + n) = o;
                     } else if (n < p.N) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             if (n + j < p.N) {
-                                const __nv_bfloat16 h = __float2bfloat16_rn(acc[8 * v + j]);
+                                const uint64_t pr = acc[4 * v + j / 2];
+                                const __nv_bfloat16 h = __float2bfloat16_rn((j & 1) ? hi_f32(pr) : lo_f32(pr));
                                 yr[n + j] = *reinterpret_cast<const uint16_t*>(&h);
                             }
                     }
@@ -408,13 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int v = 0; v < COLS / 4; ++v) {
                     const int n = nbase + 4 * v;
+                    const float q[4] = {lo_f32(acc[2 * v]), hi_f32(acc[2 * v]), lo_f32(acc[2 * v + 1]),
+                                        hi_f32(acc[2 * v + 1])};
                     if (n + 4 <= p.N && (p.N & 3) == 0) {
-                        *reinterpret_cast<float4*>(pr + n) =
-                            make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+                        *reinterpret_cast<float4*>(pr + n) = make_float4(q[0], q[1], q[2], q[3]);
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            if (n + j < p.N) pr[n + j] = acc[4 * v + j];
+                            if (n + j < p.N) pr[n + j] = q[j];
                     }
                 }
             }
@@ -505,6 +515,7 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
 }
 
 constexpr int kBN = 256;
+static_assert(kBN == 128 || kBN == 256, "a promotion warpgroup's columns must sit in one 128-column scale block");
 constexpr int kStages = 4;
 
 struct Plan {
@@ -529,14 +540,14 @@ Plan dense_plan(int64_t M, int64_t N, int64_t K, int num_sms, size_t ws_cap) {
     return pl;
 }
 
-template <int BN, int STAGES, bool GROUPED>
+template <int BN, int STAGES, int MODE>
 cudaError_t ensure_kernel_ready(int device) {
     static std::mutex mu;
     static bool done[64];
     std::lock_guard<std::mutex> g(mu);
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!done[device]) {
-        auto* k = fp8_gemm_kernel<BN, STAGES, GROUPED>;
+        auto* k = fp8_gemm_kernel<BN, STAGES, MODE>;
         if (BN > 128) {
             // The setmaxnreg split assumes exactly kRegsLaunch registers per
             // thread at launch; any other count could leave a warpgroup
@@ -586,8 +597,8 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
         p.G = a.G;
         p.splits = 1;
         p.kps = p.KB;
-        if ((e = ensure_kernel_ready<BN, STAGES, true>(dev.device)) != cudaSuccess) return e;
-        fp8_gemm_kernel<BN, STAGES, true><<<dev.num_sms, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
+        if ((e = ensure_kernel_ready<BN, STAGES, kGrouped>(dev.device)) != cudaSuccess) return e;
+        fp8_gemm_kernel<BN, STAGES, kGrouped><<<dev.num_sms, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
         return cudaGetLastError();
     }
     const Plan pl = dense_plan(a.M, a.N, a.K, dev.num_sms, a.workspace ? a.ws_bytes : 0);
@@ -597,9 +608,14 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
     p.kps = pl.kps;
     p.num_tiles = p.MT * p.NT * p.splits;
     p.partial = pl.splits > 1 ? static_cast<float*>(a.workspace) : nullptr;
-    if ((e = ensure_kernel_ready<BN, STAGES, false>(dev.device)) != cudaSuccess) return e;
     const int grid = std::min(p.num_tiles, dev.num_sms);
-    fp8_gemm_kernel<BN, STAGES, false><<<grid, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
+    if (pl.splits > 1) {
+        if ((e = ensure_kernel_ready<BN, STAGES, kDenseSplitK>(dev.device)) != cudaSuccess) return e;
+        fp8_gemm_kernel<BN, STAGES, kDenseSplitK><<<grid, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
+    } else {
+        if ((e = ensure_kernel_ready<BN, STAGES, kDense>(dev.device)) != cudaSuccess) return e;
+        fp8_gemm_kernel<BN, STAGES, kDense><<<grid, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (pl.splits > 1) {
         const int64_t work = a.M * ((a.N + 7) / 8);

@@ -198,6 +198,112 @@ __device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+// Load 32 consecutive fp32 TMEM columns of this warp's 32 lanes as 16
+// packed pairs (column 2j in the low half of p[j]) and wait for them.
+__device__ __forceinline__ void tmem_ld_x32_pairs(uint32_t taddr, uint64_t (&p)[16]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<32>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// acc[j] += f2 * cur[j] on packed fp32 pairs (fma.rn.f32x2: two IEEE
+// fused multiply-adds) while the next 32 TMEM columns load into nxt; the
+// load is waited for before the block ends, so nxt is complete on return.
+__device__ __forceinline__ void tmem_ld_x32_pairs_fma(uint32_t taddr_next, uint64_t (&nxt)[16], uint64_t (&acc)[16],
+                                                      const uint64_t (&cur)[16], uint64_t f2) {
+    asm volatile(
+        "{\n\t.reg .b32 t<32>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%49];\n\t"
+        "fma.rn.f32x2 %16, %48, %32, %16;\n\t"
+        "fma.rn.f32x2 %17, %48, %33, %17;\n\t"
+        "fma.rn.f32x2 %18, %48, %34, %18;\n\t"
+        "fma.rn.f32x2 %19, %48, %35, %19;\n\t"
+        "fma.rn.f32x2 %20, %48, %36, %20;\n\t"
+        "fma.rn.f32x2 %21, %48, %37, %21;\n\t"
+        "fma.rn.f32x2 %22, %48, %38, %22;\n\t"
+        "fma.rn.f32x2 %23, %48, %39, %23;\n\t"
+        "fma.rn.f32x2 %24, %48, %40, %24;\n\t"
+        "fma.rn.f32x2 %25, %48, %41, %25;\n\t"
+        "fma.rn.f32x2 %26, %48, %42, %26;\n\t"
+        "fma.rn.f32x2 %27, %48, %43, %27;\n\t"
+        "fma.rn.f32x2 %28, %48, %44, %28;\n\t"
+        "fma.rn.f32x2 %29, %48, %45, %29;\n\t"
+        "fma.rn.f32x2 %30, %48, %46, %30;\n\t"
+        "fma.rn.f32x2 %31, %48, %47, %31;\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "}"
+        : "=l"(nxt[0]), "=l"(nxt[1]), "=l"(nxt[2]), "=l"(nxt[3]), "=l"(nxt[4]), "=l"(nxt[5]), "=l"(nxt[6]), "=l"(nxt[7]), "=l"(nxt[8]), "=l"(nxt[9]), "=l"(nxt[10]), "=l"(nxt[11]), "=l"(nxt[12]), "=l"(nxt[13]), "=l"(nxt[14]), "=l"(nxt[15]), "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
+        : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(cur[8]), "l"(cur[9]), "l"(cur[10]), "l"(cur[11]), "l"(cur[12]), "l"(cur[13]), "l"(cur[14]), "l"(cur[15]), "l"(f2), "r"(taddr_next)
+        : "memory");
+}
+
+// acc[j] += f2 * cur[j] on packed fp32 pairs.
+__device__ __forceinline__ void fma_pairs(uint64_t (&acc)[16], const uint64_t (&cur)[16], uint64_t f2) {
+    asm volatile(
+        "fma.rn.f32x2 %0, %32, %16, %0;\n\t"
+        "fma.rn.f32x2 %1, %32, %17, %1;\n\t"
+        "fma.rn.f32x2 %2, %32, %18, %2;\n\t"
+        "fma.rn.f32x2 %3, %32, %19, %3;\n\t"
+        "fma.rn.f32x2 %4, %32, %20, %4;\n\t"
+        "fma.rn.f32x2 %5, %32, %21, %5;\n\t"
+        "fma.rn.f32x2 %6, %32, %22, %6;\n\t"
+        "fma.rn.f32x2 %7, %32, %23, %7;\n\t"
+        "fma.rn.f32x2 %8, %32, %24, %8;\n\t"
+        "fma.rn.f32x2 %9, %32, %25, %9;\n\t"
+        "fma.rn.f32x2 %10, %32, %26, %10;\n\t"
+        "fma.rn.f32x2 %11, %32, %27, %11;\n\t"
+        "fma.rn.f32x2 %12, %32, %28, %12;\n\t"
+        "fma.rn.f32x2 %13, %32, %29, %13;\n\t"
+        "fma.rn.f32x2 %14, %32, %30, %14;\n\t"
+        "fma.rn.f32x2 %15, %32, %31, %15;\n\t"
+        ""
+        : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
+        : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(cur[8]), "l"(cur[9]), "l"(cur[10]), "l"(cur[11]), "l"(cur[12]), "l"(cur[13]), "l"(cur[14]), "l"(cur[15]), "l"(f2));
+}
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
 // ---------------------------------------------------------------- e4m3
 
 // Two fp32 -> packed e4m3x2, round to nearest-even, saturating to +-448
