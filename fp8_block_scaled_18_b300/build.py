@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfp8bs.so")
-SOURCES = ["status.cu", "quant.cu", "gemm.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["status.cu", "tmap.cu", "quant.cu", "gemm.cu", "api.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -65,7 +65,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 raise RuntimeError(f"nvcc failed on {src}")
     if force or not _newer(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-Xlinker", "-z,defs", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

@@ -57,7 +57,9 @@ fp8bs_status fp8bs_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t
     if (!w || !wq || !sw) return FP8BS_ERR_INVALID_ARG;
     if ((N + 127) / 128 > kMaxGridY) return FP8BS_ERR_UNSUPPORTED;
     if (!aligned16(w) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return FP8BS_ERR_MISALIGNED;
-    return from_cuda(launch_weight_quant(w, N, K, wq, sw, cs(stream)));
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_weight_quant(w, N, K, wq, sw, d, cs(stream)));
 }
 
 fp8bs_status fp8bs_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
@@ -68,7 +70,9 @@ fp8bs_status fp8bs_weight_dequant(const uint8_t* wq, const float* sw, int64_t N,
     if (!w || !wq || !sw) return FP8BS_ERR_INVALID_ARG;
     if ((N + 127) / 128 > kMaxGridY) return FP8BS_ERR_UNSUPPORTED;
     if (!aligned16(w) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return FP8BS_ERR_MISALIGNED;
-    return from_cuda(launch_weight_dequant(wq, sw, N, K, w, cs(stream)));
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_weight_dequant(wq, sw, N, K, w, d, cs(stream)));
 }
 
 static fp8bs_status check_gemm_common(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* wq,

@@ -32,7 +32,6 @@
 // The TMEM buffers let the tensor core run up to 512/BN - 1 chunks ahead of
 // the CUDA cores that promote them.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -485,33 +484,11 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            f = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }();
-    return fn;
-}
-
 // 2-D uint8 tensor [rows, inner] with the given row stride, boxes of
 // box_rows x 128 bytes, 128-byte swizzle, zero fill outside the tensor.
 cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
                      uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {stride_bytes};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return make_tmap_2d(map, base, 1, inner, rows, stride_bytes, BK, box_rows, true);
 }
 
 constexpr int kBN = 256;

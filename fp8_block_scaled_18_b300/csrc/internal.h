@@ -3,6 +3,7 @@
 // launcher runs.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -22,12 +23,20 @@ cudaError_t device_info(DeviceInfo* out);
 // (FP8BS_WAIT_TIMEOUT_NS in the environment overrides the default of 2 s).
 uint64_t wait_timeout_ns();
 
+// Encode a 2-D TMA descriptor over a row-major tensor [rows, inner] of
+// elem_bytes-sized elements (1 or 2) with the given row stride in bytes;
+// boxes of box_rows x box_inner elements; swizzle128 selects the 128-byte
+// swizzle (the MMA operand layout), else no swizzle.  Reads outside the
+// tensor fill with zeros.  (tmap.cu)
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
+                         uint64_t stride_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+
 cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq,
                              float* sx, int64_t lds, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
-                                cudaStream_t stream);
+                                const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
-                                  cudaStream_t stream);
+                                  const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_e4m3_encode(const float* v, int64_t n, uint8_t* q, const DeviceInfo& dev,
                                cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, const DeviceInfo& dev, cudaStream_t stream);

@@ -18,24 +18,33 @@ constexpr float kE4M3Max = 448.0f;
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// The quotient RN32(x / s) of one element, given its group's scale s and
-// r = RN32(1 / s).  Markstein's correction step (P. Markstein, "Computation
-// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
-// Dev. 34(1), 1990): q0 = RN(x r), rem = x - s q0 (exact with one fused
-// multiply-add), q = RN(q0 + rem r).  The result is re-signed from x so that
-// -0 stays -0.  Groups whose scale is so small that 1/s could overflow use the
-// IEEE division instead (`exact_div`).  Bit-exactness against RN32(x / s) is
-// checked exhaustively over every bf16 amax and every bf16 x with |x| <= amax.
-__device__ __forceinline__ float quotient(float x, float s, float r, bool exact_div) {
-    if (exact_div) return __fdiv_rn(x, s);
-    const float q0 = __fmul_rn(x, r);
-    const float rem = __fmaf_rn(-q0, s, x);
-    const float q = __fmaf_rn(rem, r, q0);
-    return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+// Packed fp32 pairs (low half = first element): two IEEE round-to-nearest
+// operations per instruction, bit-identical to the scalar ones.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
-// Scale-side constants of one group: r = RN(1/s); the reciprocal path is used
-// only while 1/s stays far from overflow (s >= 2^-100).
+// Scale-side constants of one group or block.  s = RN32(amax / 448) and
+// r = RN32(1 / s).  The quotients use Markstein's correction step
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with y = RN(1/b),
+// q0 = RN(a y), rem = a - b q0 (exact with one fused multiply-add) and
+// q = RN(q0 + rem y) equals RN(a / b).  s itself is formed that way from
+// the constant RN32(1/448) = 0x3b124925.  Groups whose amax is below 2^-100
+// (where subnormal intermediates could break the argument) use IEEE
+// division throughout (`exact_div`).  Bit-exactness of every code and scale
+// against RN32 division is checked exhaustively over every bf16 amax and
+// every bf16 x with |x| <= amax.
 struct GroupScale {
     float s, r;
     bool exact_div;
@@ -43,47 +52,64 @@ struct GroupScale {
 
 __device__ __forceinline__ GroupScale group_scale(float amax) {
     GroupScale g;
-    g.s = __fdiv_rn(amax, kE4M3Max);
-    g.exact_div = !(g.s >= 7.888609052210118e-31f);  // 2^-100; also true for s == 0
-    g.r = g.exact_div ? 0.0f : __frcp_rn(g.s);
+    g.exact_div = !(amax >= 7.888609052210118e-31f);  // 2^-100; also true for amax == 0
+    if (g.exact_div) {
+        g.s = __fdiv_rn(amax, kE4M3Max);
+        g.r = 0.0f;
+    } else {
+        const float inv448 = __uint_as_float(0x3b124925u);
+        const float q0 = __fmul_rn(amax, inv448);
+        const float rem = __fmaf_rn(-q0, kE4M3Max, amax);
+        g.s = __fmaf_rn(rem, inv448, q0);
+        g.r = __frcp_rn(g.s);
+    }
     return g;
 }
 
-// Encode 8 fp32 values (x / s) into 8 e4m3 bytes (little-endian in a uint2).
-// zero_group: every code is +-0 with the input's sign.
-__device__ __forceinline__ uint2 encode8(const float (&x)[8], const GroupScale& gs, bool zero_group) {
-    uint32_t w[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t lo, hi;
-        if (zero_group) {
-            uint32_t b[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = (__float_as_uint(x[4 * h + j]) >> 24) & 0x80u;
-            lo = b[0] | (b[1] << 8);
-            hi = b[2] | (b[3] << 8);
-        } else {
-            lo = cvt_e4m3x2(quotient(x[4 * h + 0], gs.s, gs.r, gs.exact_div),
-                            quotient(x[4 * h + 1], gs.s, gs.r, gs.exact_div));
-            hi = cvt_e4m3x2(quotient(x[4 * h + 2], gs.s, gs.r, gs.exact_div),
-                            quotient(x[4 * h + 3], gs.s, gs.r, gs.exact_div));
-        }
-        w[h] = lo | (hi << 16);
-    }
-    return make_uint2(w[0], w[1]);
-}
-
-__device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
-    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x);
-    x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z);
-    x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-}
-
-__device__ __forceinline__ float absmax8(const float (&x)[8], float m) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(x[j]));
+// Largest |x| over 8 bf16 values held as bit patterns: for non-negative
+// IEEE patterns integer order equals value order, so the maximum of
+// (bits & 0x7fff) per 16-bit half is the amax's bit pattern.
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4& v, uint32_t m) {
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
     return m;
+}
+__device__ __forceinline__ float bits_to_amax(uint32_t m2) {
+    return __uint_as_float((m2 > (m2 << 16) ? m2 & 0xFFFF0000u : m2 << 16));
+}
+
+// Encode 8 bf16 values (bit patterns in `raw`, element j in half j of the
+// words) into 8 e4m3 codes (little-endian in a uint2): code = e4m3(RN32(x/s)),
+// round to nearest-even with saturation (cvt.rn.satfinite).  The sign of
+// each code is OR-ed in from the input's sign bit, which keeps -0 as 0x80
+// (a nonzero quotient already carries x's sign).  zero_group (amax == 0):
+// every code is +-0.
+__device__ __forceinline__ uint2 encode8(const uint4& raw, const GroupScale& g, bool zero_group) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint32_t sign0 = __byte_perm(w[0], w[1], 0x7531) & 0x80808080u;
+    const uint32_t sign1 = __byte_perm(w[2], w[3], 0x7531) & 0x80808080u;
+    if (zero_group) return make_uint2(sign0, sign1);
+    uint32_t c[4];
+    if (g.exact_div) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            c[i] = cvt_e4m3x2(__fdiv_rn(bf16_lo(w[i]), g.s), __fdiv_rn(bf16_hi(w[i]), g.s));
+    } else {
+        const uint64_t r2 = f2(g.r, g.r);
+        const uint64_t ns2 = f2(-g.s, -g.s);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint64_t x2 = f2(bf16_lo(w[i]), bf16_hi(w[i]));
+            const uint64_t q0 = f2_mul(x2, r2);
+            const uint64_t rem = f2_fma(q0, ns2, x2);  // x - s q0, exact
+            const uint64_t q = f2_fma(rem, r2, q0);
+            c[i] = cvt_e4m3x2(__uint_as_float(static_cast<uint32_t>(q)),
+                              __uint_as_float(static_cast<uint32_t>(q >> 32)));
+        }
+    }
+    return make_uint2((c[0] | (c[1] << 16)) | sign0, (c[2] | (c[3] << 16)) | sign1);
 }
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -114,21 +140,21 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
     for (int64_t base = warp * 4; base < total_groups; base += nwarps * 4) {
         const int64_t g = base + team;
         const bool valid = g < total_groups;
-        float a[8], b[8];
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
         int64_t m = 0, kb = 0;
-        float amax = 0.0f;
         if (valid) {
             m = g / KB;
             kb = g - m * KB;
             const uint16_t* p = x + m * ldx + kb * 128;
-            unpack8(ld_stream(p + sub * 8), a);
-            unpack8(ld_stream(p + 64 + sub * 8), b);
-            amax = absmax8(b, absmax8(a, 0.0f));
+            a = ld_stream(p + sub * 8);
+            b = ld_stream(p + 64 + sub * 8);
         }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        uint32_t amax2 = absmax_bits8(b, absmax_bits8(a, 0u));
+        amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, 1));
+        amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, 2));
+        amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, 4));
         if (valid) {
+            const float amax = bits_to_amax(amax2);
             const GroupScale gs = group_scale(amax);
             const bool zero = (amax == 0.0f);
             uint8_t* q = xq + m * ldq + kb * 128;
@@ -153,23 +179,19 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __res
     const int chunk = t & 15;
     const int r0 = t >> 4;
     uint4 raw[8];  // the block stays in registers as packed bf16 (32 registers)
-    float amax = 0.0f;
+    uint32_t amax2 = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 16 * j;
         raw[j] = n < N ? ld_stream(w + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float v[8];
-        unpack8(raw[j], v);
-        amax = absmax8(v, amax);
-    }
+    for (int j = 0; j < 8; ++j) amax2 = absmax_bits8(raw[j], amax2);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if ((t & 31) == 0) warp_max[t >> 5] = amax;
+    for (int o = 16; o > 0; o >>= 1) amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, o));
+    if ((t & 31) == 0) warp_max[t >> 5] = bits_to_amax(amax2);
     __syncthreads();
-    amax = warp_max[0];
+    float amax = warp_max[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
     const GroupScale gs = group_scale(amax);
@@ -177,12 +199,9 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __res
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 16 * j;
-        if (n < N) {
-            float v[8];
-            unpack8(raw[j], v);
+        if (n < N)
             *reinterpret_cast<uint2*>(wq + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8) =
-                encode8(v, gs, zero);
-        }
+                encode8(raw[j], gs, zero);
     }
     if (t == 0) sw[static_cast<int64_t>(nb) * KB + kb] = gs.s;
 }
@@ -265,14 +284,14 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ld
 }
 
 cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
-                                cudaStream_t stream) {
+                                const DeviceInfo&, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
     weight_quant_kernel<<<grid, 256, 0, stream>>>(w, N, K, wq, sw);
     return cudaGetLastError();
 }
 
 cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
-                                  cudaStream_t stream) {
+                                  const DeviceInfo&, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
     weight_dequant_kernel<<<grid, 256, 0, stream>>>(wq, sw, N, K, w);
     return cudaGetLastError();
