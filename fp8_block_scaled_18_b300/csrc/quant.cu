@@ -122,44 +122,54 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 
 // ---------------------------------------------------------------- act_quant
 //
-// Eight lanes own one 128-channel group: lane j of the team loads channels
-// [8j, 8j+8) and [64+8j, 64+8j+8) (two 16-byte loads; each load instruction
-// of the team covers 128 contiguous bytes), the amax is reduced over the team
-// with three xor-shuffles, and each lane writes its 16 codes as two 8-byte
-// stores.  A warp handles four groups per step; grid-stride over all groups.
+// Four lanes own one 128-channel group: lane j of the team loads the 16-byte
+// chunks j, j+4, j+8, j+12 of the group (each load instruction of the team
+// covers 64 contiguous bytes), the amax is reduced over the team with two
+// xor-shuffles, and each lane writes its 32 codes as four 8-byte stores.  A
+// warp handles eight groups per step; grid-stride over all groups.  Four
+// lanes per group (rather than more) keeps the per-group work -- the
+// shuffles and the scale -- small against the 32 elements each lane encodes.
+constexpr int kAqTeam = 4;
+constexpr int kAqGroupsPerWarp = 32 / kAqTeam;
+
 __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, int64_t KB,
                                                        int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
                                                        float* __restrict__ sx, int64_t lds,
                                                        int64_t total_groups) {
     const int lane = threadIdx.x & 31;
-    const int sub = lane & 7;
-    const int team = lane >> 3;
+    const int sub = lane & (kAqTeam - 1);
+    const int team = lane / kAqTeam;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
 
-    for (int64_t base = warp * 4; base < total_groups; base += nwarps * 4) {
+    for (int64_t base = warp * kAqGroupsPerWarp; base < total_groups; base += nwarps * kAqGroupsPerWarp) {
         const int64_t g = base + team;
         const bool valid = g < total_groups;
-        uint4 a = make_uint4(0, 0, 0, 0), b = a;
+        uint4 v[4];
         int64_t m = 0, kb = 0;
         if (valid) {
             m = g / KB;
             kb = g - m * KB;
             const uint16_t* p = x + m * ldx + kb * 128;
-            a = ld_stream(p + sub * 8);
-            b = ld_stream(p + 64 + sub * 8);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = ld_stream(p + (sub + kAqTeam * i) * 8);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
         }
-        uint32_t amax2 = absmax_bits8(b, absmax_bits8(a, 0u));
+        uint32_t amax2 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) amax2 = absmax_bits8(v[i], amax2);
         amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, 1));
         amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, 2));
-        amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, 4));
         if (valid) {
             const float amax = bits_to_amax(amax2);
             const GroupScale gs = group_scale(amax);
             const bool zero = (amax == 0.0f);
             uint8_t* q = xq + m * ldq + kb * 128;
-            *reinterpret_cast<uint2*>(q + sub * 8) = encode8(a, gs, zero);
-            *reinterpret_cast<uint2*>(q + 64 + sub * 8) = encode8(b, gs, zero);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint2*>(q + (sub + kAqTeam * i) * 8) = encode8(v[i], gs, zero);
             if (sub == 0) sx[m * lds + kb] = gs.s;
         }
     }
@@ -167,38 +177,44 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
 
 // ---------------------------------------------------------------- weight_quant
 //
-// One 256-thread CTA per 128x128 block.  Thread t reads the 16-byte chunk
-// (t % 16) of rows (t / 16) + 16 j, j = 0..7 (each warp load covers two full
+// 512 threads per block: each thread has four 16-byte loads in flight, which
+// keeps small weights (a few hundred blocks) from being latency-bound.
+constexpr int kWqThreads = 512;
+constexpr int kWqRowStep = kWqThreads / 16;          // rows between a thread's loads
+constexpr int kWqRowsPerThread = 128 / kWqRowStep;
+//
+// One CTA per 128x128 block.  Thread t reads the 16-byte chunk (t % 16) of
+// rows (t / 16) + kWqRowStep j (each warp load covers two full
 // 256-byte row segments), block amax via warp shuffles and shared memory.
-__global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
+__global__ void __launch_bounds__(kWqThreads) weight_quant_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                           uint8_t* __restrict__ wq, float* __restrict__ sw) {
-    __shared__ float warp_max[8];
+    __shared__ float warp_max[kWqThreads / 32];
     const int kb = blockIdx.x, nb = blockIdx.y;
     const int64_t KB = K / 128;
     const int t = threadIdx.x;
     const int chunk = t & 15;
     const int r0 = t >> 4;
-    uint4 raw[8];  // the block stays in registers as packed bf16 (32 registers)
+    uint4 raw[kWqRowsPerThread];  // the block stays in registers as packed bf16
     uint32_t amax2 = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 16 * j;
+    for (int j = 0; j < kWqRowsPerThread; ++j) {
+        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + kWqRowStep * j;
         raw[j] = n < N ? ld_stream(w + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax2 = absmax_bits8(raw[j], amax2);
+    for (int j = 0; j < kWqRowsPerThread; ++j) amax2 = absmax_bits8(raw[j], amax2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, o));
     if ((t & 31) == 0) warp_max[t >> 5] = bits_to_amax(amax2);
     __syncthreads();
     float amax = warp_max[0];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
+    for (int i = 1; i < kWqThreads / 32; ++i) amax = fmaxf(amax, warp_max[i]);
     const GroupScale gs = group_scale(amax);
     const bool zero = (amax == 0.0f);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 16 * j;
+    for (int j = 0; j < kWqRowsPerThread; ++j) {
+        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + kWqRowStep * j;
         if (n < N)
             *reinterpret_cast<uint2*>(wq + n * K + static_cast<int64_t>(kb) * 128 + chunk * 8) =
                 encode8(raw[j], gs, zero);
@@ -207,10 +223,13 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------- weight_dequant
+constexpr int kDqThreads = 512;
+constexpr int kDqRowStep = kDqThreads / 8;
+constexpr int kDqRowsPerThread = 128 / kDqRowStep;
 //
-// One 256-thread CTA per 128x128 block: thread t decodes the 16-byte chunk
-// (t % 8) of rows (t / 8) + 32 j, j = 0..3: w = bf16_rne(fp32(dec(q)) * s).
-__global__ void __launch_bounds__(256) weight_dequant_kernel(const uint8_t* __restrict__ wq,
+// One CTA per 128x128 block: thread t decodes the 16-byte chunk (t % 8) of
+// rows (t / 8) + kDqRowStep j: w = bf16_rne(fp32(dec(q)) * s).
+__global__ void __launch_bounds__(kDqThreads) weight_dequant_kernel(const uint8_t* __restrict__ wq,
                                                             const float* __restrict__ sw, int64_t N,
                                                             int64_t K, uint16_t* __restrict__ w) {
     const int kb = blockIdx.x, nb = blockIdx.y;
@@ -220,8 +239,8 @@ __global__ void __launch_bounds__(256) weight_dequant_kernel(const uint8_t* __re
     const int r0 = t >> 3;
     const float s = sw[static_cast<int64_t>(nb) * KB + kb];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + 32 * j;
+    for (int j = 0; j < kDqRowsPerThread; ++j) {
+        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + kDqRowStep * j;
         if (n >= N) continue;
         const int64_t off = n * K + static_cast<int64_t>(kb) * 128 + chunk * 16;
         const uint4 q = ld_stream(wq + off);
@@ -275,7 +294,7 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ld
                              float* sx, int64_t lds, const DeviceInfo& dev, cudaStream_t stream) {
     const int64_t KB = K / 128;
     const int64_t groups = M * KB;
-    const int64_t warps_needed = (groups + 3) / 4;
+    const int64_t warps_needed = (groups + kAqGroupsPerWarp - 1) / kAqGroupsPerWarp;
     const int64_t blocks_needed = (warps_needed + 7) / 8;
     const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 8;  // 8 x 256 threads per SM
     const int blocks = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
@@ -286,14 +305,14 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ld
 cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
                                 const DeviceInfo&, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
-    weight_quant_kernel<<<grid, 256, 0, stream>>>(w, N, K, wq, sw);
+    weight_quant_kernel<<<grid, kWqThreads, 0, stream>>>(w, N, K, wq, sw);
     return cudaGetLastError();
 }
 
 cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
                                   const DeviceInfo&, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
-    weight_dequant_kernel<<<grid, 256, 0, stream>>>(wq, sw, N, K, w);
+    weight_dequant_kernel<<<grid, kDqThreads, 0, stream>>>(wq, sw, N, K, w);
     return cudaGetLastError();
 }
 
