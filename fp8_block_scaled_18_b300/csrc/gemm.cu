@@ -63,7 +63,7 @@ struct Layout {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
-    static constexpr int NBUF = 512 / BN;                       // TMEM chunk buffers (all 512 columns)
+    static constexpr int NBUF = 512 / BN;                       // TMEM chunk buffers
     static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;   // full[S], empty[S], tfull[NBUF], tempty[NBUF], done
     static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
@@ -72,9 +72,9 @@ struct Layout {
     static constexpr int TABLE_BYTES = (kMaxGroups + 1) * 4;
     static constexpr int BYTES = OFF_TABLE + TABLE_BYTES;
     static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
-    static constexpr uint32_t TMEM_COLS = NBUF * BN;
+    static constexpr uint32_t TMEM_COLS = 512;                  // allocation: a power of two
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
-    static_assert(NBUF >= 2 && TMEM_COLS == 512, "chunk buffers fill TMEM");
+    static_assert(NBUF >= 2 && NBUF * BN <= 512, "two or more chunk buffers must fit in TMEM");
 };
 
 struct Params {
@@ -83,35 +83,33 @@ struct Params {
     const float* sw;
     uint16_t* y;
     int64_t ldy;
-    float* partial;          // split-K: fp32 [splits][M][N], else nullptr
     const int32_t* offsets;  // grouped: device [G+1], else nullptr
     int G;
     int M, N, KB;
     int MT, NT;              // dense: m-tiles, n-tiles
-    int splits, kps;         // dense split-K: number of splits, chunks per split
-    int num_tiles;           // dense: MT * NT * splits
+    int num_tiles;           // dense: MT * NT (x splits for split-K)
+    // split-K: each tile's K chunks are cut into `splits` ranges of `kps`
+    // chunks; split s writes fp32 partial sums to partial[s][M][N]
+    int splits, kps;
+    float* partial;
     unsigned* err;
     uint64_t timeout_ns;
 };
 
 struct Tile {
+    int tile;    // tile index
     int m0;      // first row of A / y
     int m_end;   // one past the last valid row
     int n0;      // first output column
     int b_row;   // first row of the B operand (g * N + n0 for grouped)
-    int sw_row;  // weight-scale row of column n0 (g * NB + n0 / 128)
-    int kb0, kb1;
-    int split;
+    int sw_base; // first weight-scale row of the operand (g * NB for grouped, else 0)
+    int kb0, kb1;  // chunk range of this piece of the tile
 };
 
-template <int BN, bool SPLITK>
+template <int BN>
 __device__ __forceinline__ Tile dense_tile(const Params& p, int t) {
     Tile tl;
-    tl.split = 0;
-    if (SPLITK) {
-        tl.split = t % p.splits;
-        t /= p.splits;
-    }
+    tl.tile = t;
     const int per_group = kGroupM * p.NT;
     const int grp = t / per_group;
     const int first_m = grp * kGroupM;
@@ -123,9 +121,9 @@ __device__ __forceinline__ Tile dense_tile(const Params& p, int t) {
     tl.m_end = min(p.M, tl.m0 + BM);
     tl.n0 = nt * BN;
     tl.b_row = tl.n0;
-    tl.sw_row = tl.n0 / 128;
-    tl.kb0 = SPLITK ? tl.split * p.kps : 0;
-    tl.kb1 = SPLITK ? min(p.KB, tl.kb0 + p.kps) : p.KB;
+    tl.sw_base = 0;
+    tl.kb0 = 0;
+    tl.kb1 = p.KB;
     return tl;
 }
 
@@ -146,14 +144,14 @@ __device__ __forceinline__ Tile grouped_tile(const Params& p, const int* prefix,
     const int mt = local % mtiles;
     const int nt = local / mtiles;
     Tile tl;
+    tl.tile = t;
     tl.m0 = r0 + mt * BM;
     tl.m_end = r1;
     tl.n0 = nt * BN;
     tl.b_row = g * p.N + tl.n0;
-    tl.sw_row = g * ((p.N + 127) / 128) + tl.n0 / 128;
+    tl.sw_base = g * ((p.N + 127) / 128);
     tl.kb0 = 0;
     tl.kb1 = p.KB;
-    tl.split = 0;
     return tl;
 }
 
@@ -202,13 +200,37 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, const 
     return ok;
 }
 
+// MODE: how tiles map to work.
+enum : int { kDense = 0, kSplitK = 1, kGrouped = 2 };
+
+// Walks the work of one CTA: tiles strided over the grid; for split-K the
+// work unit is (tile, split) and covers the split's range of K chunks.
+template <int BN, int MODE>
+struct WorkCursor {
+    int t;
+    __device__ __forceinline__ void begin(const Params&) { t = blockIdx.x; }
+    __device__ __forceinline__ bool next(const Params& p, const int* prefix, int num_tiles, Tile& tl) {
+        if (t >= num_tiles) return false;
+        if (MODE == kGrouped) {
+            tl = grouped_tile<BN>(p, prefix, t);
+        } else if (MODE == kSplitK) {
+            const int split = t % p.splits;
+            tl = dense_tile<BN>(p, t / p.splits);
+            tl.tile = split;  // for split-K the piece's index is its split
+            tl.kb0 = split * p.kps;
+            tl.kb1 = min(p.KB, tl.kb0 + p.kps);
+        } else {
+            tl = dense_tile<BN>(p, t);
+        }
+        t += gridDim.x;
+        return true;
+    }
+};
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
-
-// MODE: how tiles map to work.
-enum : int { kDense = 0, kDenseSplitK = 1, kGrouped = 2 };
 
 template <int BN, int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -248,7 +270,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
     constexpr bool GROUPED = MODE == kGrouped;
-    constexpr bool SPLITK = MODE == kDenseSplitK;
     if (GROUPED && warp == kEpiWarp0) build_tile_table<BN>(p, prefix, lane);
     tc_fence_before();
     __syncthreads();
@@ -258,9 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
 
 
-    auto tile_of = [&](int t) {
-        return GROUPED ? grouped_tile<BN>(p, prefix, t) : dense_tile<BN, SPLITK>(p, t);
-    };
 
     if (warp < kEpiWarp0) {
       if (BN > 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSetup));
@@ -272,8 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            const Tile tl = tile_of(t);
+        WorkCursor<BN, MODE> wc;
+        wc.begin(p);
+        Tile tl;
+        while (ok && wc.next(p, prefix, num_tiles, tl)) {
             for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
@@ -294,8 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
         uint32_t it = 0;
         bool ok = true, issued = false;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            const Tile tl = tile_of(t);
+        WorkCursor<BN, MODE> wc;
+        wc.begin(p);
+        Tile tl;
+        while (ok && wc.next(p, prefix, num_tiles, tl)) {
             for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t sph = (it / STAGES) & 1u;
@@ -329,7 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ promotion + epilogue
         if (BN > 128) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
         constexpr int COLS = BN / 2;        // columns per warpgroup
-        constexpr int NCH = COLS / 32;      // 32-column TMEM loads per chunk
+        // TMEM slice width: 16 columns when the warpgroup holds 128 columns
+        // (keeps the two staging buffers within the register budget), else 32
+        constexpr int SW = COLS >= 128 ? 16 : 32;
+        constexpr int NCH = COLS / SW;      // TMEM slices per chunk
+        constexpr int SP = SW / 2;          // packed pairs per slice
+        // With BN = 256 or 128 a warpgroup's columns sit in one 128-column
+        // scale block; with BN = 192 its three slices may straddle two.
+        constexpr bool SLICE_SCALES = (128 % COLS) != 0;  // (implies SW = 32)
+        constexpr int NSC = SLICE_SCALES ? NCH : 1;  // distinct weight scales per chunk
         const int ew = warp - kEpiWarp0;
         const int wg = ew >> 2;
         const int quarter = warp & 3;       // TMEM lane quarter this warp may access
@@ -338,49 +368,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            const Tile tl = tile_of(t);
+        WorkCursor<BN, MODE> wc;
+        wc.begin(p);
+        Tile tl;
+        while (ok && wc.next(p, prefix, num_tiles, tl)) {
             const int m = tl.m0 + row;
             const bool row_ok = m < tl.m_end;
             const float* sxr = p.sx + static_cast<int64_t>(row_ok ? m : 0) * p.lds;
-            // weight-scale row of this warpgroup's columns: they lie inside one
-            // 128-column block; a warpgroup entirely past N reads row 0 and
-            // stores nothing
-            const bool wg_in_n = tl.n0 + col0 < p.N;
-            const float* swr = p.sw + static_cast<int64_t>(wg_in_n ? tl.sw_row + col0 / 128 : 0) * p.KB;
+            // weight-scale row of each 32-column slice (a slice never straddles a
+            // 128-column block); slices past N read row 0 and store nothing
+            const float* swr[NSC];
+#pragma unroll
+            for (int c = 0; c < NSC; ++c) {
+                const int n = tl.n0 + col0 + SW * c;
+                swr[c] = p.sw + static_cast<int64_t>(n < p.N ? tl.sw_base + n / 128 : 0) * p.KB;
+            }
             // running sums as packed fp32 pairs: acc[j] = (column 2j, column 2j+1)
             uint64_t acc[COLS / 2];
 #pragma unroll
             for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
 
             float sx_next = row_ok ? __ldg(sxr + tl.kb0) : 0.0f;
-            float sw_next = __ldg(swr + tl.kb0);
+            float sw_next[NSC];
+#pragma unroll
+            for (int c = 0; c < NSC; ++c) sw_next[c] = __ldg(swr[c] + tl.kb0);
 
             for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
                 const int b = it % NBUF;
                 const uint32_t bph = (it / NBUF) & 1u;
-                const float f = __fmul_rn(sx_next, sw_next);  // fp32(sx * sw) of this chunk
+                uint64_t f2[NSC];  // fp32(sx * sw) of this chunk per distinct scale, as a packed pair
+#pragma unroll
+                for (int c = 0; c < NSC; ++c) {
+                    const float f = __fmul_rn(sx_next, sw_next[c]);
+                    f2[c] = pack_f32x2(f, f);
+                }
                 if (kb + 1 < tl.kb1) {
                     sx_next = row_ok ? __ldg(sxr + kb + 1) : 0.0f;
-                    sw_next = __ldg(swr + kb + 1);
+#pragma unroll
+                    for (int c = 0; c < NSC; ++c) sw_next[c] = __ldg(swr[c] + kb + 1);
                 }
                 if (!warp_wait(tfull_bar(b), bph, ctl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * BN + col0);
                 // promotion: acc += f * P_kb, slice by slice of 32 columns; the
                 // TMEM load of slice c+1 overlaps the FMAs of slice c
-                const uint64_t f2 = pack_f32x2(f, f);
-                uint64_t bufA[16], bufB[16];  // slices alternate between two buffers
-                tmem_ld_x32_pairs(taddr, bufA);
+                uint64_t bufA[SP], bufB[SP];  // slices alternate between two buffers
+                if constexpr (SW == 16) tmem_ld_x16_pairs(taddr, bufA); else tmem_ld_x32_pairs(taddr, bufA);
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
-                    uint64_t(&a)[16] = *reinterpret_cast<uint64_t(*)[16]>(&acc[16 * c]);
-                    uint64_t(&cur)[16] = (c & 1) ? bufB : bufA;
-                    uint64_t(&nxt)[16] = (c & 1) ? bufA : bufB;
-                    if (c + 1 < NCH)
-                        tmem_ld_x32_pairs_fma(taddr + 32u * (c + 1), nxt, a, cur, f2);
-                    else
-                        fma_pairs(a, cur, f2);
+                    uint64_t(&a)[SP] = *reinterpret_cast<uint64_t(*)[SP]>(&acc[SP * c]);
+                    uint64_t(&cur)[SP] = (c & 1) ? bufB : bufA;
+                    uint64_t(&nxt)[SP] = (c & 1) ? bufA : bufB;
+                    const uint64_t fc = f2[SLICE_SCALES ? c : 0];
+                    if (c + 1 < NCH) {
+                        if constexpr (SW == 16)
+                            tmem_ld_x16_pairs_fma(taddr + SW * (c + 1), nxt, a, cur, fc);
+                        else
+                            tmem_ld_x32_pairs_fma(taddr + SW * (c + 1), nxt, a, cur, fc);
+                    } else {
+                        fma_pairs(a, cur, fc);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -389,7 +436,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (!row_ok) continue;
             const int nbase = tl.n0 + col0;
-            if (!SPLITK) {
+            if (MODE == kSplitK) {
+                float* pr = p.partial + (static_cast<int64_t>(tl.tile) * p.M + m) * p.N;
+#pragma unroll
+                for (int v = 0; v < COLS / 4; ++v) {
+                    const int n = nbase + 4 * v;
+                    const float q[4] = {lo_f32(acc[2 * v]), hi_f32(acc[2 * v]), lo_f32(acc[2 * v + 1]),
+                                        hi_f32(acc[2 * v + 1])};
+                    if (n + 4 <= p.N && (p.N & 3) == 0) {
+                        *reinterpret_cast<float4*>(pr + n) = make_float4(q[0], q[1], q[2], q[3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (n + j < p.N) pr[n + j] = q[j];
+                    }
+                }
+            } else {
                 uint16_t* yr = p.y + static_cast<int64_t>(m) * p.ldy;
 #pragma unroll
                 for (int v = 0; v < COLS / 8; ++v) {
@@ -409,21 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const __nv_bfloat16 h = __float2bfloat16_rn((j & 1) ? hi_f32(pr) : lo_f32(pr));
                                 yr[n + j] = *reinterpret_cast<const uint16_t*>(&h);
                             }
-                    }
-                }
-            } else {
-                float* pr = p.partial + (static_cast<int64_t>(tl.split) * p.M + m) * p.N;
-#pragma unroll
-                for (int v = 0; v < COLS / 4; ++v) {
-                    const int n = nbase + 4 * v;
-                    const float q[4] = {lo_f32(acc[2 * v]), hi_f32(acc[2 * v]), lo_f32(acc[2 * v + 1]),
-                                        hi_f32(acc[2 * v + 1])};
-                    if (n + 4 <= p.N && (p.N & 3) == 0) {
-                        *reinterpret_cast<float4*>(pr + n) = make_float4(q[0], q[1], q[2], q[3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (n + j < p.N) pr[n + j] = q[j];
                     }
                 }
             }
@@ -491,28 +538,50 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return make_tmap_2d(map, base, 1, inner, rows, stride_bytes, BK, box_rows, true);
 }
 
-constexpr int kBN = 256;
-static_assert(kBN == 128 || kBN == 256, "a promotion warpgroup's columns must sit in one 128-column scale block");
-constexpr int kStages = 4;
+// Tile widths: 256 columns (N = 256 MMAs) in general; 192 when N is a
+// multiple of 192 but not of 256 (e.g. 576), which wastes no columns.
+// Stages: as many 128-K stages as fit in shared memory next to the tables.
+constexpr int kStages256 = 4;  // (16 + 32) KB per stage
+constexpr int kStages192 = 5;  // (16 + 24) KB per stage
+
+int pick_bn(int64_t N) { return (N % 256 != 0 && N % 192 == 0) ? 192 : 256; }
 
 struct Plan {
-    int splits;
-    int kps;
-    size_t ws;
+    int bn;
+    int mode;      // kDense or kSplitK
+    int grid;
+    int splits, kps;
+    int64_t tiles;
+    size_t ws;     // workspace bytes the plan uses
 };
 
+// Split-K when the tiles occupy less than half of the SMs (small M): each
+// tile's 128-K chunks are cut into up to num_sms / tiles ranges of at least
+// two chunks, the partial sums go to the workspace, and a second kernel adds
+// them in split order.  Otherwise one CTA per tile (persistent).
 Plan dense_plan(int64_t M, int64_t N, int64_t K, int num_sms, size_t ws_cap) {
+    Plan pl{};
+    pl.bn = pick_bn(N);
     const int64_t KB = K / 128;
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
-    Plan pl{1, static_cast<int>(KB), 0};
-    if (tiles * 2 > num_sms || KB < 8) return pl;
-    int64_t splits = std::min<int64_t>(num_sms / tiles, KB / 4);
-    while (splits > 1) {
+    pl.tiles = ((M + BM - 1) / BM) * ((N + pl.bn - 1) / pl.bn);
+    pl.mode = kDense;
+    pl.splits = 1;
+    pl.kps = static_cast<int>(KB);
+    pl.grid = static_cast<int>(std::min<int64_t>(pl.tiles, num_sms));
+    pl.ws = 0;
+    if (pl.tiles * 2 > num_sms || KB < 4) return pl;
+    for (int64_t splits = std::min<int64_t>(num_sms / pl.tiles, KB / 2); splits > 1; --splits) {
         const int64_t kps = (KB + splits - 1) / splits;
         const int64_t s = (KB + kps - 1) / kps;
         const size_t ws = static_cast<size_t>(s) * static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
-        if (ws <= ws_cap) return Plan{static_cast<int>(s), static_cast<int>(kps), ws};
-        --splits;
+        if (ws <= ws_cap) {
+            pl.mode = kSplitK;
+            pl.splits = static_cast<int>(s);
+            pl.kps = static_cast<int>(kps);
+            pl.grid = static_cast<int>(std::min<int64_t>(pl.tiles * s, num_sms));
+            pl.ws = ws;
+            return pl;
+        }
     }
     return pl;
 }
@@ -525,21 +594,30 @@ cudaError_t ensure_kernel_ready(int device) {
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!done[device]) {
         auto* k = fp8_gemm_kernel<BN, STAGES, MODE>;
-        if (BN > 128) {
-            // The setmaxnreg split assumes exactly kRegsLaunch registers per
-            // thread at launch; any other count could leave a warpgroup
-            // waiting for registers that never free up.
-            cudaFuncAttributes attr;
-            cudaError_t e = cudaFuncGetAttributes(&attr, k);
-            if (e != cudaSuccess) return e;
-            if (attr.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
-        }
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Layout<BN, STAGES>::ALLOC);
+        // The setmaxnreg split assumes exactly kRegsLaunch registers per
+        // thread at launch; any other count could leave a warpgroup waiting
+        // for registers that never free up.
+        cudaFuncAttributes attr;
+        cudaError_t e = cudaFuncGetAttributes(&attr, k);
+        if (e != cudaSuccess) return e;
+        if (attr.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BN, STAGES>::ALLOC);
         if (e != cudaSuccess) return e;
         done[device] = true;
     }
     return cudaSuccess;
+}
+
+template <int BN, int STAGES, int MODE>
+cudaError_t launch_mode(const GemmArgs& a, Params& p, int grid, const DeviceInfo& dev, cudaStream_t stream) {
+    const int64_t b_rows = MODE == kGrouped ? static_cast<int64_t>(a.G) * a.N : a.N;
+    CUtensorMap tmA, tmB;
+    cudaError_t e;
+    if ((e = make_map(&tmA, a.xq, a.K, a.M, a.K, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&tmB, a.wq, a.K, b_rows, a.K, BN)) != cudaSuccess) return e;
+    if ((e = ensure_kernel_ready<BN, STAGES, MODE>(dev.device)) != cudaSuccess) return e;
+    fp8_gemm_kernel<BN, STAGES, MODE><<<grid, kThreads, Layout<BN, STAGES>::ALLOC, stream>>>(tmA, tmB, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -549,14 +627,6 @@ size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, const DeviceInfo& de
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-    constexpr int BN = kBN, STAGES = kStages;
-    const bool grouped = a.offsets != nullptr;
-    const int64_t b_rows = grouped ? static_cast<int64_t>(a.G) * a.N : a.N;
-    CUtensorMap tmA, tmB;
-    cudaError_t e;
-    if ((e = make_map(&tmA, a.xq, a.K, a.M, a.K, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&tmB, a.wq, a.K, b_rows, a.K, BN)) != cudaSuccess) return e;
-
     Params p{};
     p.sx = a.sx;
     p.lds = a.lds;
@@ -568,39 +638,30 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
     p.KB = static_cast<int>(a.K / 128);
     p.err = dev.err;
     p.timeout_ns = wait_timeout_ns();
-    using L = Layout<BN, STAGES>;
-    if (grouped) {
+    if (a.offsets != nullptr) {
         p.offsets = a.offsets;
         p.G = a.G;
-        p.splits = 1;
-        p.kps = p.KB;
-        if ((e = ensure_kernel_ready<BN, STAGES, kGrouped>(dev.device)) != cudaSuccess) return e;
-        fp8_gemm_kernel<BN, STAGES, kGrouped><<<dev.num_sms, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
-        return cudaGetLastError();
+        return launch_mode<256, kStages256, kGrouped>(a, p, dev.num_sms, dev, stream);
     }
     const Plan pl = dense_plan(a.M, a.N, a.K, dev.num_sms, a.workspace ? a.ws_bytes : 0);
     p.MT = static_cast<int>((a.M + BM - 1) / BM);
-    p.NT = static_cast<int>((a.N + BN - 1) / BN);
+    p.NT = static_cast<int>((a.N + pl.bn - 1) / pl.bn);
     p.splits = pl.splits;
     p.kps = pl.kps;
-    p.num_tiles = p.MT * p.NT * p.splits;
-    p.partial = pl.splits > 1 ? static_cast<float*>(a.workspace) : nullptr;
-    const int grid = std::min(p.num_tiles, dev.num_sms);
-    if (pl.splits > 1) {
-        if ((e = ensure_kernel_ready<BN, STAGES, kDenseSplitK>(dev.device)) != cudaSuccess) return e;
-        fp8_gemm_kernel<BN, STAGES, kDenseSplitK><<<grid, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
-    } else {
-        if ((e = ensure_kernel_ready<BN, STAGES, kDense>(dev.device)) != cudaSuccess) return e;
-        fp8_gemm_kernel<BN, STAGES, kDense><<<grid, kThreads, L::ALLOC, stream>>>(tmA, tmB, p);
-    }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (pl.splits > 1) {
+    p.num_tiles = static_cast<int>(pl.tiles * pl.splits);
+    cudaError_t e;
+    if (pl.mode == kSplitK) {
+        p.partial = static_cast<float*>(a.workspace);
+        e = pl.bn == 192 ? launch_mode<192, kStages192, kSplitK>(a, p, pl.grid, dev, stream)
+                         : launch_mode<256, kStages256, kSplitK>(a, p, pl.grid, dev, stream);
+        if (e != cudaSuccess) return e;
         const int64_t work = a.M * ((a.N + 7) / 8);
         const int blocks = static_cast<int>(std::min<int64_t>((work + 255) / 256, dev.num_sms * 8));
         splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(p.partial, pl.splits, p.M, p.N, a.y, a.ldy);
         return cudaGetLastError();
     }
-    return cudaSuccess;
+    return pl.bn == 192 ? launch_mode<192, kStages192, kDense>(a, p, pl.grid, dev, stream)
+                        : launch_mode<256, kStages256, kDense>(a, p, pl.grid, dev, stream);
 }
 
 }  // namespace fp8bs

@@ -298,6 +298,74 @@ __device__ __forceinline__ void fma_pairs(uint64_t (&acc)[16], const uint64_t (&
         : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(cur[8]), "l"(cur[9]), "l"(cur[10]), "l"(cur[11]), "l"(cur[12]), "l"(cur[13]), "l"(cur[14]), "l"(cur[15]), "l"(f2));
 }
 
+// Load 16 consecutive fp32 TMEM columns of this warp's 32 lanes as 8
+// packed pairs (column 2j in the low half of p[j]) and wait for them.
+__device__ __forceinline__ void tmem_ld_x16_pairs(uint32_t taddr, uint64_t (&p)[8]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<16>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7])
+        : "r"(taddr)
+        : "memory");
+}
+
+// acc[j] += f2 * cur[j] on packed fp32 pairs (fma.rn.f32x2: two IEEE
+// fused multiply-adds) while the next 16 TMEM columns load into nxt; the
+// load is waited for before the block ends, so nxt is complete on return.
+__device__ __forceinline__ void tmem_ld_x16_pairs_fma(uint32_t taddr_next, uint64_t (&nxt)[8], uint64_t (&acc)[8],
+                                                      const uint64_t (&cur)[8], uint64_t f2) {
+    asm volatile(
+        "{\n\t.reg .b32 t<16>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15}, [%25];\n\t"
+        "fma.rn.f32x2 %8, %24, %16, %8;\n\t"
+        "fma.rn.f32x2 %9, %24, %17, %9;\n\t"
+        "fma.rn.f32x2 %10, %24, %18, %10;\n\t"
+        "fma.rn.f32x2 %11, %24, %19, %11;\n\t"
+        "fma.rn.f32x2 %12, %24, %20, %12;\n\t"
+        "fma.rn.f32x2 %13, %24, %21, %13;\n\t"
+        "fma.rn.f32x2 %14, %24, %22, %14;\n\t"
+        "fma.rn.f32x2 %15, %24, %23, %15;\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "}"
+        : "=l"(nxt[0]), "=l"(nxt[1]), "=l"(nxt[2]), "=l"(nxt[3]), "=l"(nxt[4]), "=l"(nxt[5]), "=l"(nxt[6]), "=l"(nxt[7]), "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7])
+        : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(f2), "r"(taddr_next)
+        : "memory");
+}
+
+// acc[j] += f2 * cur[j] on 8 packed fp32 pairs.
+__device__ __forceinline__ void fma_pairs(uint64_t (&acc)[8], const uint64_t (&cur)[8], uint64_t f2) {
+    asm volatile(
+        "fma.rn.f32x2 %0, %16, %8, %0;\n\t"
+        "fma.rn.f32x2 %1, %16, %9, %1;\n\t"
+        "fma.rn.f32x2 %2, %16, %10, %2;\n\t"
+        "fma.rn.f32x2 %3, %16, %11, %3;\n\t"
+        "fma.rn.f32x2 %4, %16, %12, %4;\n\t"
+        "fma.rn.f32x2 %5, %16, %13, %5;\n\t"
+        "fma.rn.f32x2 %6, %16, %14, %6;\n\t"
+        "fma.rn.f32x2 %7, %16, %15, %7;\n\t"
+        ""
+        : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7])
+        : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(f2));
+}
+
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
     return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
 }

@@ -141,7 +141,7 @@ fp8bs_status fp8bs_grouped_gemm(const uint8_t* xq, const float* sx, int64_t lds,
  * device current); make that first call before any stream capture.  All
  * calls on a device share the array: calls whose kernels overlap on the GPU
  * race and must be serialised by the caller.  Allocates nothing. */
-#define FP8BS_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define FP8BS_NOALLOC_SCRATCH_BYTES (32u << 20)
 fp8bs_status fp8bs_gemm_noalloc(const uint8_t* xq, const float* sx, int64_t lds,
                                 const uint8_t* wq, const float* sw,
                                 int64_t M, int64_t N, int64_t K,
