@@ -351,14 +351,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ promotion + epilogue
         if (BN > 128) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
         constexpr int COLS = BN / 2;        // columns per warpgroup
-        // TMEM slice width: 16 columns when the warpgroup holds 128 columns
-        // (keeps the two staging buffers within the register budget), else 32
-        constexpr int SW = COLS >= 128 ? 16 : 32;
+        // A warpgroup holding up to 96 columns loads a whole chunk at once and
+        // releases the TMEM buffer before its FMAs (WHOLE); with 128 columns
+        // it walks 16-column slices, loading slice c+1 during slice c's FMAs.
+        constexpr bool WHOLE = COLS <= 96;
+        constexpr int SW = 16;
+        static_assert(COLS % 16 == 0, "promotion columns come in 16-column slices");
         constexpr int NCH = COLS / SW;      // TMEM slices per chunk
         constexpr int SP = SW / 2;          // packed pairs per slice
         // With BN = 256 or 128 a warpgroup's columns sit in one 128-column
-        // scale block; with BN = 192 its three slices may straddle two.
-        constexpr bool SLICE_SCALES = (128 % COLS) != 0;  // (implies SW = 32)
+        // scale block; with BN = 160 or 192 its slices may straddle two.
+        constexpr bool SLICE_SCALES = (128 % COLS) != 0;
         constexpr int NSC = SLICE_SCALES ? NCH : 1;  // distinct weight scales per chunk
         const int ew = warp - kEpiWarp0;
         const int wg = ew >> 2;
@@ -412,8 +415,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * BN + col0);
                 // promotion: acc += f * P_kb, slice by slice of 32 columns; the
                 // TMEM load of slice c+1 overlaps the FMAs of slice c
+                if constexpr (WHOLE) {
+                    uint64_t pr[COLS / 2];
+                    tmem_ld_cols_pairs(taddr, pr);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(b));  // the MMA may refill this buffer now
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c)
+                        fma_pairs(*reinterpret_cast<uint64_t(*)[SP]>(&acc[SP * c]),
+                                  *reinterpret_cast<uint64_t(*)[SP]>(&pr[SP * c]), f2[SLICE_SCALES ? c : 0]);
+                    continue;
+                }
                 uint64_t bufA[SP], bufB[SP];  // slices alternate between two buffers
-                if constexpr (SW == 16) tmem_ld_x16_pairs(taddr, bufA); else tmem_ld_x32_pairs(taddr, bufA);
+                tmem_ld_x16_pairs(taddr, bufA);
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     uint64_t(&a)[SP] = *reinterpret_cast<uint64_t(*)[SP]>(&acc[SP * c]);
@@ -421,10 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint64_t(&nxt)[SP] = (c & 1) ? bufA : bufB;
                     const uint64_t fc = f2[SLICE_SCALES ? c : 0];
                     if (c + 1 < NCH) {
-                        if constexpr (SW == 16)
-                            tmem_ld_x16_pairs_fma(taddr + SW * (c + 1), nxt, a, cur, fc);
-                        else
-                            tmem_ld_x32_pairs_fma(taddr + SW * (c + 1), nxt, a, cur, fc);
+                        tmem_ld_x16_pairs_fma(taddr + SW * (c + 1), nxt, a, cur, fc);
                     } else {
                         fma_pairs(a, cur, fc);
                     }
@@ -540,7 +552,9 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
 
 // Tile widths: 256 columns (N = 256 MMAs) in general; 192 when N is a
 // multiple of 192 but not of 256 (e.g. 576), which wastes no columns.
-// Stages: as many 128-K stages as fit in shared memory next to the tables.
+// Narrower tiles (128, 160) measured slower on every shape tried: the
+// per-chunk period hardly shrinks with the width.  Stages: as many 128-K
+// stages as fit in shared memory next to the tables.
 constexpr int kStages256 = 4;  // (16 + 32) KB per stage
 constexpr int kStages192 = 5;  // (16 + 24) KB per stage
 
@@ -597,9 +611,9 @@ cudaError_t ensure_kernel_ready(int device) {
         // The setmaxnreg split assumes exactly kRegsLaunch registers per
         // thread at launch; any other count could leave a warpgroup waiting
         // for registers that never free up.
+        cudaError_t e;
         cudaFuncAttributes attr;
-        cudaError_t e = cudaFuncGetAttributes(&attr, k);
-        if (e != cudaSuccess) return e;
+        if ((e = cudaFuncGetAttributes(&attr, k)) != cudaSuccess) return e;
         if (attr.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BN, STAGES>::ALLOC);
         if (e != cudaSuccess) return e;
@@ -618,6 +632,14 @@ cudaError_t launch_mode(const GemmArgs& a, Params& p, int grid, const DeviceInfo
     if ((e = ensure_kernel_ready<BN, STAGES, MODE>(dev.device)) != cudaSuccess) return e;
     fp8_gemm_kernel<BN, STAGES, MODE><<<grid, kThreads, Layout<BN, STAGES>::ALLOC, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_bn(int bn, const GemmArgs& a, Params& p, int grid, const DeviceInfo& dev, cudaStream_t stream) {
+    switch (bn) {
+        case 192: return launch_mode<192, kStages192, MODE>(a, p, grid, dev, stream);
+        default: return launch_mode<256, kStages256, MODE>(a, p, grid, dev, stream);
+    }
 }
 
 }  // namespace
@@ -652,16 +674,14 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
     cudaError_t e;
     if (pl.mode == kSplitK) {
         p.partial = static_cast<float*>(a.workspace);
-        e = pl.bn == 192 ? launch_mode<192, kStages192, kSplitK>(a, p, pl.grid, dev, stream)
-                         : launch_mode<256, kStages256, kSplitK>(a, p, pl.grid, dev, stream);
+        e = launch_bn<kSplitK>(pl.bn, a, p, pl.grid, dev, stream);
         if (e != cudaSuccess) return e;
         const int64_t work = a.M * ((a.N + 7) / 8);
         const int blocks = static_cast<int>(std::min<int64_t>((work + 255) / 256, dev.num_sms * 8));
         splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(p.partial, pl.splits, p.M, p.N, a.y, a.ldy);
         return cudaGetLastError();
     }
-    return pl.bn == 192 ? launch_mode<192, kStages192, kDense>(a, p, pl.grid, dev, stream)
-                        : launch_mode<256, kStages256, kDense>(a, p, pl.grid, dev, stream);
+    return launch_bn<kDense>(pl.bn, a, p, pl.grid, dev, stream);
 }
 
 }  // namespace fp8bs

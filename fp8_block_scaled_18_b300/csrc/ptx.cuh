@@ -366,6 +366,170 @@ __device__ __forceinline__ void fma_pairs(uint64_t (&acc)[8], const uint64_t (&c
         : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(f2));
 }
 
+// Load 64 consecutive fp32 TMEM columns of this warp's 32 lanes (one
+// wait for all the loads) as 32 packed pairs.
+__device__ __forceinline__ void tmem_ld_cols_pairs(uint32_t taddr, uint64_t (&p)[32]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<64>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t32,t33,t34,t35,t36,t37,t38,t39,t40,t41,t42,t43,t44,t45,t46,t47,t48,t49,t50,t51,t52,t53,t54,t55,t56,t57,t58,t59,t60,t61,t62,t63}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "mov.b64 %16, {t32, t33};\n\t"
+        "mov.b64 %17, {t34, t35};\n\t"
+        "mov.b64 %18, {t36, t37};\n\t"
+        "mov.b64 %19, {t38, t39};\n\t"
+        "mov.b64 %20, {t40, t41};\n\t"
+        "mov.b64 %21, {t42, t43};\n\t"
+        "mov.b64 %22, {t44, t45};\n\t"
+        "mov.b64 %23, {t46, t47};\n\t"
+        "mov.b64 %24, {t48, t49};\n\t"
+        "mov.b64 %25, {t50, t51};\n\t"
+        "mov.b64 %26, {t52, t53};\n\t"
+        "mov.b64 %27, {t54, t55};\n\t"
+        "mov.b64 %28, {t56, t57};\n\t"
+        "mov.b64 %29, {t58, t59};\n\t"
+        "mov.b64 %30, {t60, t61};\n\t"
+        "mov.b64 %31, {t62, t63};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31])
+        : "r"(taddr + 0u), "r"(taddr + 32u)
+        : "memory");
+}
+
+// Load 80 consecutive fp32 TMEM columns of this warp's 32 lanes (one
+// wait for all the loads) as 40 packed pairs.
+__device__ __forceinline__ void tmem_ld_cols_pairs(uint32_t taddr, uint64_t (&p)[40]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<80>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%40];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t32,t33,t34,t35,t36,t37,t38,t39,t40,t41,t42,t43,t44,t45,t46,t47,t48,t49,t50,t51,t52,t53,t54,t55,t56,t57,t58,t59,t60,t61,t62,t63}, [%41];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t64,t65,t66,t67,t68,t69,t70,t71,t72,t73,t74,t75,t76,t77,t78,t79}, [%42];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "mov.b64 %16, {t32, t33};\n\t"
+        "mov.b64 %17, {t34, t35};\n\t"
+        "mov.b64 %18, {t36, t37};\n\t"
+        "mov.b64 %19, {t38, t39};\n\t"
+        "mov.b64 %20, {t40, t41};\n\t"
+        "mov.b64 %21, {t42, t43};\n\t"
+        "mov.b64 %22, {t44, t45};\n\t"
+        "mov.b64 %23, {t46, t47};\n\t"
+        "mov.b64 %24, {t48, t49};\n\t"
+        "mov.b64 %25, {t50, t51};\n\t"
+        "mov.b64 %26, {t52, t53};\n\t"
+        "mov.b64 %27, {t54, t55};\n\t"
+        "mov.b64 %28, {t56, t57};\n\t"
+        "mov.b64 %29, {t58, t59};\n\t"
+        "mov.b64 %30, {t60, t61};\n\t"
+        "mov.b64 %31, {t62, t63};\n\t"
+        "mov.b64 %32, {t64, t65};\n\t"
+        "mov.b64 %33, {t66, t67};\n\t"
+        "mov.b64 %34, {t68, t69};\n\t"
+        "mov.b64 %35, {t70, t71};\n\t"
+        "mov.b64 %36, {t72, t73};\n\t"
+        "mov.b64 %37, {t74, t75};\n\t"
+        "mov.b64 %38, {t76, t77};\n\t"
+        "mov.b64 %39, {t78, t79};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31]), "=l"(p[32]), "=l"(p[33]), "=l"(p[34]), "=l"(p[35]), "=l"(p[36]), "=l"(p[37]), "=l"(p[38]), "=l"(p[39])
+        : "r"(taddr + 0u), "r"(taddr + 32u), "r"(taddr + 64u)
+        : "memory");
+}
+
+// Load 96 consecutive fp32 TMEM columns of this warp's 32 lanes (one
+// wait for all the loads) as 48 packed pairs.
+__device__ __forceinline__ void tmem_ld_cols_pairs(uint32_t taddr, uint64_t (&p)[48]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<96>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%48];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t32,t33,t34,t35,t36,t37,t38,t39,t40,t41,t42,t43,t44,t45,t46,t47,t48,t49,t50,t51,t52,t53,t54,t55,t56,t57,t58,t59,t60,t61,t62,t63}, [%49];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t64,t65,t66,t67,t68,t69,t70,t71,t72,t73,t74,t75,t76,t77,t78,t79,t80,t81,t82,t83,t84,t85,t86,t87,t88,t89,t90,t91,t92,t93,t94,t95}, [%50];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "mov.b64 %16, {t32, t33};\n\t"
+        "mov.b64 %17, {t34, t35};\n\t"
+        "mov.b64 %18, {t36, t37};\n\t"
+        "mov.b64 %19, {t38, t39};\n\t"
+        "mov.b64 %20, {t40, t41};\n\t"
+        "mov.b64 %21, {t42, t43};\n\t"
+        "mov.b64 %22, {t44, t45};\n\t"
+        "mov.b64 %23, {t46, t47};\n\t"
+        "mov.b64 %24, {t48, t49};\n\t"
+        "mov.b64 %25, {t50, t51};\n\t"
+        "mov.b64 %26, {t52, t53};\n\t"
+        "mov.b64 %27, {t54, t55};\n\t"
+        "mov.b64 %28, {t56, t57};\n\t"
+        "mov.b64 %29, {t58, t59};\n\t"
+        "mov.b64 %30, {t60, t61};\n\t"
+        "mov.b64 %31, {t62, t63};\n\t"
+        "mov.b64 %32, {t64, t65};\n\t"
+        "mov.b64 %33, {t66, t67};\n\t"
+        "mov.b64 %34, {t68, t69};\n\t"
+        "mov.b64 %35, {t70, t71};\n\t"
+        "mov.b64 %36, {t72, t73};\n\t"
+        "mov.b64 %37, {t74, t75};\n\t"
+        "mov.b64 %38, {t76, t77};\n\t"
+        "mov.b64 %39, {t78, t79};\n\t"
+        "mov.b64 %40, {t80, t81};\n\t"
+        "mov.b64 %41, {t82, t83};\n\t"
+        "mov.b64 %42, {t84, t85};\n\t"
+        "mov.b64 %43, {t86, t87};\n\t"
+        "mov.b64 %44, {t88, t89};\n\t"
+        "mov.b64 %45, {t90, t91};\n\t"
+        "mov.b64 %46, {t92, t93};\n\t"
+        "mov.b64 %47, {t94, t95};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31]), "=l"(p[32]), "=l"(p[33]), "=l"(p[34]), "=l"(p[35]), "=l"(p[36]), "=l"(p[37]), "=l"(p[38]), "=l"(p[39]), "=l"(p[40]), "=l"(p[41]), "=l"(p[42]), "=l"(p[43]), "=l"(p[44]), "=l"(p[45]), "=l"(p[46]), "=l"(p[47])
+        : "r"(taddr + 0u), "r"(taddr + 32u), "r"(taddr + 64u)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
     return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
 }

@@ -177,17 +177,18 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
 
 // ---------------------------------------------------------------- weight_quant
 //
-// 512 threads per block: each thread has four 16-byte loads in flight, which
-// keeps small weights (a few hundred blocks) from being latency-bound.
-constexpr int kWqThreads = 512;
-constexpr int kWqRowStep = kWqThreads / 16;          // rows between a thread's loads
-constexpr int kWqRowsPerThread = 128 / kWqRowStep;
+// The launch picks 512 threads per block (four 16-byte loads in flight per
+// thread) when there are few blocks -- a small weight would otherwise be
+// latency-bound -- and 256 (eight loads per thread) otherwise.
 //
 // One CTA per 128x128 block.  Thread t reads the 16-byte chunk (t % 16) of
 // rows (t / 16) + kWqRowStep j (each warp load covers two full
 // 256-byte row segments), block amax via warp shuffles and shared memory.
+template <int kWqThreads>
 __global__ void __launch_bounds__(kWqThreads) weight_quant_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                           uint8_t* __restrict__ wq, float* __restrict__ sw) {
+    constexpr int kWqRowStep = kWqThreads / 16;  // rows between a thread's loads
+    constexpr int kWqRowsPerThread = 128 / kWqRowStep;
     __shared__ float warp_max[kWqThreads / 32];
     const int kb = blockIdx.x, nb = blockIdx.y;
     const int64_t KB = K / 128;
@@ -223,15 +224,15 @@ __global__ void __launch_bounds__(kWqThreads) weight_quant_kernel(const uint16_t
 }
 
 // ---------------------------------------------------------------- weight_dequant
-constexpr int kDqThreads = 512;
-constexpr int kDqRowStep = kDqThreads / 8;
-constexpr int kDqRowsPerThread = 128 / kDqRowStep;
 //
 // One CTA per 128x128 block: thread t decodes the 16-byte chunk (t % 8) of
 // rows (t / 8) + kDqRowStep j: w = bf16_rne(fp32(dec(q)) * s).
+template <int kDqThreads>
 __global__ void __launch_bounds__(kDqThreads) weight_dequant_kernel(const uint8_t* __restrict__ wq,
                                                             const float* __restrict__ sw, int64_t N,
                                                             int64_t K, uint16_t* __restrict__ w) {
+    constexpr int kDqRowStep = kDqThreads / 8;
+    constexpr int kDqRowsPerThread = 128 / kDqRowStep;
     const int kb = blockIdx.x, nb = blockIdx.y;
     const int64_t KB = K / 128;
     const int t = threadIdx.x;
@@ -303,16 +304,22 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ld
 }
 
 cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
-                                const DeviceInfo&, cudaStream_t stream) {
+                                const DeviceInfo& dev, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
-    weight_quant_kernel<<<grid, kWqThreads, 0, stream>>>(w, N, K, wq, sw);
+    if (static_cast<int64_t>(grid.x) * grid.y < 2 * static_cast<int64_t>(dev.num_sms))
+        weight_quant_kernel<512><<<grid, 512, 0, stream>>>(w, N, K, wq, sw);
+    else
+        weight_quant_kernel<256><<<grid, 256, 0, stream>>>(w, N, K, wq, sw);
     return cudaGetLastError();
 }
 
 cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
-                                  const DeviceInfo&, cudaStream_t stream) {
+                                  const DeviceInfo& dev, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
-    weight_dequant_kernel<<<grid, kDqThreads, 0, stream>>>(wq, sw, N, K, w);
+    if (static_cast<int64_t>(grid.x) * grid.y < 2 * static_cast<int64_t>(dev.num_sms))
+        weight_dequant_kernel<512><<<grid, 512, 0, stream>>>(wq, sw, N, K, w);
+    else
+        weight_dequant_kernel<256><<<grid, 256, 0, stream>>>(wq, sw, N, K, w);
     return cudaGetLastError();
 }
 
