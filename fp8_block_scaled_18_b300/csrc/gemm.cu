@@ -12,29 +12,44 @@
 //   warp 0      TMA producer: A (128 x 128 B) and B (BN x 128 B) tiles of one
 //               K chunk per pipeline stage, 128-byte swizzled, mbarrier
 //               completion by byte count.
-//   warp 1      TMEM owner and MMA issuer: per chunk, four
-//               tcgen05.mma.kind::f8f6f4 (M=128, N=BN, K=32) into one of
-//               512/BN TMEM buffers of BN fp32 columns, then tcgen05.commit to
-//               free the smem stage and to publish the chunk.
+//   warps 1-2   MMA issuers taking alternate chunks (warp 1 also owns the
+//               TMEM allocation): per chunk, four tcgen05.mma.kind::f8f6f4
+//               (M=128, N=BN, K=32) into one of 512/BN TMEM buffers of BN
+//               fp32 columns, then tcgen05.commit to free the smem stage and
+//               to publish the chunk.  A thread issuing MMAs is held back
+//               until the tensor core takes them, so with one issuer the
+//               tensor core idled through that thread's two barrier waits
+//               every chunk; with two, one warp waits while the other
+//               issues.  Chunks use separate buffers and stages, and each
+//               commit tracks only its own thread's MMAs, so the two
+//               streams need no ordering between them.
+//   warp 3      scale loader: per block of four chunks, the tile's sx
+//               (128 rows x 4 chunks, one 16-byte TMA box column per row)
+//               and the at most three weight-scale rows the tile touches,
+//               into a ring of four slots (sfull/sempty mbarriers).  Having
+//               every promotion thread fetch its own row's sx from global
+//               memory, 4 scattered bytes per chunk, cost up to a third of
+//               the large GEMMs' time in load/store traffic.
 //   warps 4-11  promotion + epilogue: two warpgroups, each owning BN/2
-//               columns; thread = one row (TMEM lane).
-// With BN = 256 every promotion thread keeps 128 fp32 accumulators, so the
-// warpgroups rebalance registers after set-up (setmaxnreg): the TMA/MMA
-// warpgroup drops to kRegsSetup, the promotion warpgroups rise to kRegsPromo.
-// Per SM sub-partition (one set-up warp + two promotion warps) that is
-// kRegsSetup + 2 * kRegsPromo = 3 * kRegsLaunch registers per lane, exactly
-// what the launch reserved; the host refuses the kernel unless its compiled
-// register count is kRegsLaunch.  Per chunk: tcgen05.ld the raw
-//               chunk sum P_kb, acc += fp32(sx*sw) * P_kb in registers (one
-//               FFMA per element), release the TMEM buffer.  After the last
-//               chunk of a tile: round to bf16 and store (or store fp32
-//               partials for split-K).
+//               columns; thread = one row (TMEM lane).  Per chunk:
+//               tcgen05.ld the raw chunk sum P_kb, acc += fp32(sx*sw) * P_kb
+//               in registers (packed f32x2 FMAs), release the TMEM buffer.
+//               After the last chunk of a tile: round to bf16 and store (or
+//               store fp32 partials for split-K).
+// Every promotion thread keeps BN/2 fp32 accumulators (128 at BN = 256),
+// so the warpgroups rebalance registers after set-up (setmaxnreg): the
+// set-up warpgroup drops to kRegsSetup, the promotion warpgroups rise to
+// kRegsPromo.  Per SM sub-partition (one set-up warp + two promotion warps)
+// that is kRegsSetup + 2 * kRegsPromo = 3 * kRegsLaunch registers per lane,
+// exactly what the launch reserved; the host refuses the kernel unless its
+// compiled register count is kRegsLaunch.
 // The TMEM buffers let the tensor core run up to 512/BN - 1 chunks ahead of
 // the CUDA cores that promote them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <mutex>
 
 #include "internal.h"
@@ -47,12 +62,18 @@ constexpr int BM = 128;           // tile rows (tokens) = TMEM lanes
 constexpr int BK = 128;           // K chunk = one scale block = 4 MMAs of K=32
 constexpr int UMMA_K = 32;
 constexpr int kThreads = 384;
+constexpr int kMmaWarp0 = 1;      // MMA issuers: warps 1 and 2
+constexpr int kMmaWarps = 2;
 constexpr int kEpiWarp0 = 4;      // first promotion/epilogue warp
 constexpr int kRegsLaunch = 168;  // 65536 / 384, rounded down to a multiple of 8
 constexpr int kRegsSetup = 56;
 constexpr int kRegsPromo = 224;
 static_assert(kRegsSetup + 2 * kRegsPromo == 3 * kRegsLaunch, "register split must match the launch");
 constexpr int kEpiWarps = 8;
+constexpr int kScaleWarp = 3;     // scale loader
+constexpr int kScaleChunks = 4;   // K chunks per scale block (one 16-byte TMA column of sx)
+constexpr int kScaleSlots = 4;    // scale blocks in flight
+constexpr int kSwBlocks = 3;      // weight-scale blocks a tile of <= 256 columns can touch
 constexpr int kGroupM = 16;       // dense raster: 16 m-tiles share a sweep over n
 constexpr int kMaxGroups = 1024;
 
@@ -64,13 +85,21 @@ struct Layout {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int NBUF = 512 / BN;                       // TMEM chunk buffers
-    static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;   // full[S], empty[S], tfull[NBUF], tempty[NBUF], done
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1;
+    // full[S], empty[S], tfull[NBUF], tempty[NBUF], done[2], sfull[4], sempty[4]
+    static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+    // + one drain barrier per issuer + sfull/sempty per scale slot
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + kMmaWarps + 2 * kScaleSlots;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_TABLE = (OFF_ABORT + 4 + 15) & ~15;  // grouped: tile prefix [G+1]
     static constexpr int TABLE_BYTES = (kMaxGroups + 1) * 4;
-    static constexpr int BYTES = OFF_TABLE + TABLE_BYTES;
+    // scale slots: sx of the tile's 128 rows x kScaleChunks chunks (the TMA
+    // box, row-major), then the weight scales of kSwBlocks blocks x chunks
+    static constexpr int SX_SLOT = BM * kScaleChunks * 4;
+    static constexpr int SW_SLOT = kSwBlocks * kScaleChunks * 4;
+    static constexpr int OFF_SX = (OFF_TABLE + TABLE_BYTES + 127) & ~127;
+    static constexpr int OFF_SWS = OFF_SX + kScaleSlots * SX_SLOT;
+    static constexpr int BYTES = OFF_SWS + kScaleSlots * SW_SLOT;
     static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;                  // allocation: a power of two
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
@@ -235,8 +264,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <int BN, int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ Params p) {
+                    const __grid_constant__ CUtensorMap tmS, const __grid_constant__ Params p) {
     using L = Layout<BN, STAGES>;
+    static_assert(BN == 160 || BN == 256, "tile widths the host dispatches");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
@@ -251,7 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NBUF = L::NBUF;
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + NBUF + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 2 * NBUF);
+    auto done_bar = [&](int w) { return bar0 + 8u * (2 * STAGES + 2 * NBUF + w); };
+    auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * NBUF + kMmaWarps + s); };
+    auto sempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * NBUF + kMmaWarps + kScaleSlots + s); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
     int* prefix = reinterpret_cast<int*>(smem + L::OFF_TABLE);
 
@@ -264,7 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), kEpiWarps);
         }
-        mbar_init(done_bar, 1);
+        for (int w = 0; w < kMmaWarps; ++w) mbar_init(done_bar(w), 1);
+        for (int s = 0; s < kScaleSlots; ++s) {
+            mbar_init(sfull_bar(s), 1 + 32);  // the TMA's byte count + one arrival per loader lane
+            mbar_init(sempty_bar(s), kEpiWarps);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -281,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
     if (warp < kEpiWarp0) {
-      if (BN > 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSetup));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSetup));
       if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -309,9 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Every issued load must land before the CTA's shared memory goes away.
         const uint32_t first = it > STAGES ? it - STAGES : 0;
         for (uint32_t j = first; j < it; ++j) drain_wait(full_bar(j % STAGES), (j / STAGES) & 1u, ctl);
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp < kMmaWarp0 + kMmaWarps) {
+        // ------------------------------------------------------------ MMA issuers
         constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+        const uint32_t mw = static_cast<uint32_t>(warp - kMmaWarp0);  // takes chunks with it % 2 == mw
         uint32_t it = 0;
         bool ok = true, issued = false;
         WorkCursor<BN, MODE> wc;
@@ -319,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Tile tl;
         while (ok && wc.next(p, prefix, num_tiles, tl)) {
             for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
+                if ((it % kMmaWarps) != mw) continue;
                 const int s = it % STAGES;
                 const uint32_t sph = (it / STAGES) & 1u;
                 const int b = it % NBUF;
@@ -340,16 +378,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
         }
-        // All MMAs must finish before TMEM is released.
+        // All of this warp's MMAs must finish before TMEM is released.
         if (issued) {
-            if (lane == 0) umma_commit(done_bar);
+            if (lane == 0) umma_commit(done_bar(mw));
             __syncwarp();
-            drain_wait(done_bar, 0, ctl);
+            drain_wait(done_bar(mw), 0, ctl);
         }
+      } else if (warp == kScaleWarp) {
+        // ------------------------------------------------------------ scale loader
+        // Per block of kScaleChunks chunks: sx of the tile's rows by TMA (one
+        // 16-byte column per row, so the promotion threads never gather
+        // scattered 4-byte values), and the tile's weight scales by plain loads.
+        if (lane == 0) tma_prefetch_desc(&tmS);
+        const int nblk = (p.N + 127) / 128;  // weight-scale blocks per operand
+        float* sw_slots = reinterpret_cast<float*>(smem + L::OFF_SWS);
+        uint32_t sb = 0;
+        bool ok = true;
+        WorkCursor<BN, MODE> wc;
+        wc.begin(p);
+        Tile tl;
+        while (ok && wc.next(p, prefix, num_tiles, tl)) {
+            const int fb = tl.n0 / 128;      // the tile's first weight-scale block
+            // lane (bi, c) of the first kSwBlocks * kScaleChunks lanes loads the
+            // weight scale of block fb + bi, chunk c of a scale block; blocks
+            // past N and chunks past K are never used and read as 0
+            const int bi = lane / kScaleChunks;
+            const bool sw_lane = lane < kSwBlocks * kScaleChunks && fb + bi < nblk;
+            const float* swr = p.sw + static_cast<int64_t>(tl.sw_base + (sw_lane ? fb + bi : 0)) * p.KB;
+            auto load_sw = [&](int q) {
+                const int kb = q * kScaleChunks + lane % kScaleChunks;
+                return sw_lane && kb < p.KB ? __ldg(swr + kb) : 0.0f;
+            };
+            const int q1 = (tl.kb1 - 1) / kScaleChunks;
+            float v = load_sw(tl.kb0 / kScaleChunks);
+            for (int q = tl.kb0 / kScaleChunks; q <= q1; ++q, ++sb) {
+                // the next block's weight scales load while this block waits for its slot
+                const float v_next = q < q1 ? load_sw(q + 1) : 0.0f;
+                const int s = sb % kScaleSlots;
+                const uint32_t ph = (sb / kScaleSlots) & 1u;
+                if (!warp_wait(sempty_bar(s), ph ^ 1u, ctl)) { ok = false; break; }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(sfull_bar(s), L::SX_SLOT);
+                    tma_load_2d(sbase + L::OFF_SX + s * L::SX_SLOT, &tmS, sfull_bar(s), q * kScaleChunks, tl.m0);
+                }
+                if (lane < kSwBlocks * kScaleChunks) sw_slots[s * (kSwBlocks * kScaleChunks) + lane] = v;
+                mbar_arrive(sfull_bar(s));   // releases this lane's store
+                v = v_next;
+            }
+        }
+        // Every issued sx load must land before the CTA's shared memory goes away.
+        const uint32_t first = sb > kScaleSlots ? sb - kScaleSlots : 0;
+        for (uint32_t j = first; j < sb; ++j)
+            drain_wait(sfull_bar(j % kScaleSlots), (j / kScaleSlots) & 1u, ctl);
       }
     } else {
         // ------------------------------------------------------------ promotion + epilogue
-        if (BN > 128) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
         constexpr int COLS = BN / 2;        // columns per warpgroup
         // A warpgroup holding up to 96 columns loads a whole chunk at once and
         // releases the TMEM buffer before its FMAs (WHOLE); with 128 columns
@@ -359,16 +443,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         static_assert(COLS % 16 == 0, "promotion columns come in 16-column slices");
         constexpr int NCH = COLS / SW;      // TMEM slices per chunk
         constexpr int SP = SW / 2;          // packed pairs per slice
-        // With BN = 256 or 128 a warpgroup's columns sit in one 128-column
-        // scale block; with BN = 160 or 192 its slices may straddle two.
-        constexpr bool SLICE_SCALES = (128 % COLS) != 0;
-        constexpr int NSC = SLICE_SCALES ? NCH : 1;  // distinct weight scales per chunk
+        // A warpgroup's columns (at most 128) touch at most two 128-column
+        // weight-scale blocks; each 16-column slice lies inside one of them.
+        static_assert(COLS <= 128 && 128 % SW == 0, "slice-to-scale-block mapping");
+        // Tiles of 256 columns start on a block boundary, so each warpgroup's
+        // 128 columns share one weight scale per chunk.
+        constexpr bool ONE_BLOCK = COLS == 128 && BN % 128 == 0;
+        constexpr int NF = ONE_BLOCK ? 1 : NCH;  // distinct scale factors per chunk
         const int ew = warp - kEpiWarp0;
         const int wg = ew >> 2;
         const int quarter = warp & 3;       // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
         const int col0 = wg * COLS;
         const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+        // Scales come from the loader's slots (sfull/sempty per block of
+        // kScaleChunks chunks).
+        const float* sx_slots = reinterpret_cast<const float*>(smem + L::OFF_SX);
+        const float* sw_slots = reinterpret_cast<const float*>(smem + L::OFF_SWS);
+        uint32_t ss = 0;                    // scale blocks consumed
         uint32_t it = 0;
         bool ok = true;
         WorkCursor<BN, MODE> wc;
@@ -377,39 +469,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (ok && wc.next(p, prefix, num_tiles, tl)) {
             const int m = tl.m0 + row;
             const bool row_ok = m < tl.m_end;
-            const float* sxr = p.sx + static_cast<int64_t>(row_ok ? m : 0) * p.lds;
-            // weight-scale row of each 32-column slice (a slice never straddles a
-            // 128-column block); slices past N read row 0 and store nothing
-            const float* swr[NSC];
+            // The warpgroup's columns [n_first, n_last] lie in weight-scale
+            // blocks i0 and i1 of the tile's slot rows (equal when they share
+            // one); columns past N read row 0 and store nothing.
+            const int n_first = tl.n0 + col0;
+            const int n_last = min(n_first + COLS, p.N) - 1;
+            const int fb = tl.n0 / 128;
+            const int i0 = n_first < p.N ? n_first / 128 - fb : 0;
+            const int i1 = n_first < p.N ? n_last / 128 - fb : 0;
+            uint32_t upper = 0;             // bit c: slice c lies in block i1
 #pragma unroll
-            for (int c = 0; c < NSC; ++c) {
-                const int n = tl.n0 + col0 + SW * c;
-                swr[c] = p.sw + static_cast<int64_t>(n < p.N ? tl.sw_base + n / 128 : 0) * p.KB;
-            }
+            for (int c = 0; c < NCH; ++c)
+                if (n_first < p.N && (n_first + SW * c) / 128 - fb != i0) upper |= 1u << c;
+            const int nk = tl.kb1 - tl.kb0;
             // running sums as packed fp32 pairs: acc[j] = (column 2j, column 2j+1)
             uint64_t acc[COLS / 2];
 #pragma unroll
             for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
 
-            float sx_next = row_ok ? __ldg(sxr + tl.kb0) : 0.0f;
-            float sw_next[NSC];
-#pragma unroll
-            for (int c = 0; c < NSC; ++c) sw_next[c] = __ldg(swr[c] + tl.kb0);
-
-            for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
+            for (int j = 0; j < nk; ++j, ++it) {
                 const int b = it % NBUF;
                 const uint32_t bph = (it / NBUF) & 1u;
-                uint64_t f2[NSC];  // fp32(sx * sw) of this chunk per distinct scale, as a packed pair
-#pragma unroll
-                for (int c = 0; c < NSC; ++c) {
-                    const float f = __fmul_rn(sx_next, sw_next[c]);
-                    f2[c] = pack_f32x2(f, f);
+                const int kb = tl.kb0 + j;
+                const int c4 = kb % kScaleChunks;
+                const int sl = ss % kScaleSlots;
+                if ((j == 0 || c4 == 0) && !warp_wait(sfull_bar(sl), (ss / kScaleSlots) & 1u, ctl)) {
+                    ok = false;
+                    break;
                 }
-                if (kb + 1 < tl.kb1) {
-                    sx_next = row_ok ? __ldg(sxr + kb + 1) : 0.0f;
-#pragma unroll
-                    for (int c = 0; c < NSC; ++c) sw_next[c] = __ldg(swr[c] + kb + 1);
+                const float* swv = sw_slots + sl * (kSwBlocks * kScaleChunks) + c4;
+                const float sxv = sx_slots[sl * (BM * kScaleChunks) + row * kScaleChunks + c4];
+                const float f_lo = __fmul_rn(sxv, swv[i0 * kScaleChunks]);
+                const float f_hi = __fmul_rn(sxv, swv[i1 * kScaleChunks]);
+                if (c4 == kScaleChunks - 1 || j == nk - 1) {  // the block's last chunk here: free the slot
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sempty_bar(sl));
+                    ++ss;
                 }
+                const uint64_t f2lo = pack_f32x2(f_lo, f_lo), f2hi = pack_f32x2(f_hi, f_hi);
+                uint64_t f2[NF];  // fp32(sx * sw) of each slice, as a packed pair
+#pragma unroll
+                for (int c = 0; c < NF; ++c) f2[c] = ((upper >> c) & 1u) ? f2hi : f2lo;
                 if (!warp_wait(tfull_bar(b), bph, ctl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * BN + col0);
@@ -424,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < NCH; ++c)
                         fma_pairs(*reinterpret_cast<uint64_t(*)[SP]>(&acc[SP * c]),
-                                  *reinterpret_cast<uint64_t(*)[SP]>(&pr[SP * c]), f2[SLICE_SCALES ? c : 0]);
+                                  *reinterpret_cast<uint64_t(*)[SP]>(&pr[SP * c]), f2[ONE_BLOCK ? 0 : c]);
                     continue;
                 }
                 uint64_t bufA[SP], bufB[SP];  // slices alternate between two buffers
@@ -434,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint64_t(&a)[SP] = *reinterpret_cast<uint64_t(*)[SP]>(&acc[SP * c]);
                     uint64_t(&cur)[SP] = (c & 1) ? bufB : bufA;
                     uint64_t(&nxt)[SP] = (c & 1) ? bufA : bufB;
-                    const uint64_t fc = f2[SLICE_SCALES ? c : 0];
+                    const uint64_t fc = f2[ONE_BLOCK ? 0 : c];
                     if (c + 1 < NCH) {
                         tmem_ld_x16_pairs_fma(taddr + SW * (c + 1), nxt, a, cur, fc);
                     } else {
@@ -550,15 +650,33 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return make_tmap_2d(map, base, 1, inner, rows, stride_bytes, BK, box_rows, true);
 }
 
-// Tile widths: 256 columns (N = 256 MMAs) in general; 192 when N is a
-// multiple of 192 but not of 256 (e.g. 576), which wastes no columns.
-// Narrower tiles (128, 160) measured slower on every shape tried: the
-// per-chunk period hardly shrinks with the width.  Stages: as many 128-K
-// stages as fit in shared memory next to the tables.
+// Tile widths 256 or 160 columns.  A CTA's time per 128-K chunk is set by
+// the round trip of its TMEM buffers (MMA, promotion, release) more than by
+// the MMA width: 256-column tiles fit two buffers in the 512 TMEM columns,
+// 160-column tiles fit three and measured about 0.86 of the 256-column
+// period.  The width with the fewest waves of tiles times that period wins;
+// ties go to the wider tile.  (192-column tiles measured the 256-column
+// period, so never win; 128-column tiles measured slower everywhere.)
+// Stages: as many 128-K stages as fit in shared memory next to the tables
+// and the scale slots.
 constexpr int kStages256 = 4;  // (16 + 32) KB per stage
-constexpr int kStages192 = 5;  // (16 + 24) KB per stage
+constexpr int kStages160 = 5;  // (16 + 20) KB per stage
 
-int pick_bn(int64_t N) { return (N % 256 != 0 && N % 192 == 0) ? 192 : 256; }
+int pick_bn(int64_t M, int64_t N, int num_sms) {
+    constexpr int kWidths[2] = {256, 160};
+    constexpr int kPeriod[2] = {100, 86};  // relative chunk period
+    int best = 256;
+    int64_t best_cost = INT64_MAX;
+    for (int i = 0; i < 2; ++i) {
+        const int64_t tiles = ((M + BM - 1) / BM) * ((N + kWidths[i] - 1) / kWidths[i]);
+        const int64_t cost = ((tiles + num_sms - 1) / num_sms) * kPeriod[i];
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = kWidths[i];
+        }
+    }
+    return best;
+}
 
 struct Plan {
     int bn;
@@ -572,10 +690,11 @@ struct Plan {
 // Split-K when the tiles occupy less than half of the SMs (small M): each
 // tile's 128-K chunks are cut into up to num_sms / tiles ranges of at least
 // two chunks, the partial sums go to the workspace, and a second kernel adds
-// them in split order.  Otherwise one CTA per tile (persistent).
+// them in split order.  Such shapes fit one wave at either width, so they
+// always take the 160-column tiles.  Otherwise one CTA per tile (persistent).
 Plan dense_plan(int64_t M, int64_t N, int64_t K, int num_sms, size_t ws_cap) {
     Plan pl{};
-    pl.bn = pick_bn(N);
+    pl.bn = pick_bn(M, N, num_sms);
     const int64_t KB = K / 128;
     pl.tiles = ((M + BM - 1) / BM) * ((N + pl.bn - 1) / pl.bn);
     pl.mode = kDense;
@@ -584,6 +703,7 @@ Plan dense_plan(int64_t M, int64_t N, int64_t K, int num_sms, size_t ws_cap) {
     pl.grid = static_cast<int>(std::min<int64_t>(pl.tiles, num_sms));
     pl.ws = 0;
     if (pl.tiles * 2 > num_sms || KB < 4) return pl;
+    if (pl.bn != 160) return pl;  // not reached with the widths above; split-K is built for 160 only
     for (int64_t splits = std::min<int64_t>(num_sms / pl.tiles, KB / 2); splits > 1; --splits) {
         const int64_t kps = (KB + splits - 1) / splits;
         const int64_t s = (KB + kps - 1) / kps;
@@ -625,21 +745,22 @@ cudaError_t ensure_kernel_ready(int device) {
 template <int BN, int STAGES, int MODE>
 cudaError_t launch_mode(const GemmArgs& a, Params& p, int grid, const DeviceInfo& dev, cudaStream_t stream) {
     const int64_t b_rows = MODE == kGrouped ? static_cast<int64_t>(a.G) * a.N : a.N;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmS;
     cudaError_t e;
     if ((e = make_map(&tmA, a.xq, a.K, a.M, a.K, BM)) != cudaSuccess) return e;
     if ((e = make_map(&tmB, a.wq, a.K, b_rows, a.K, BN)) != cudaSuccess) return e;
+    // sx [M, lds] fp32: boxes of kScaleChunks chunks x BM rows
+    if ((e = make_tmap_2d(&tmS, a.sx, 4, a.lds, a.M, a.lds * 4, kScaleChunks, BM, false)) != cudaSuccess) return e;
     if ((e = ensure_kernel_ready<BN, STAGES, MODE>(dev.device)) != cudaSuccess) return e;
-    fp8_gemm_kernel<BN, STAGES, MODE><<<grid, kThreads, Layout<BN, STAGES>::ALLOC, stream>>>(tmA, tmB, p);
+    fp8_gemm_kernel<BN, STAGES, MODE><<<grid, kThreads, Layout<BN, STAGES>::ALLOC, stream>>>(tmA, tmB, tmS, p);
     return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t launch_bn(int bn, const GemmArgs& a, Params& p, int grid, const DeviceInfo& dev, cudaStream_t stream) {
-    switch (bn) {
-        case 192: return launch_mode<192, kStages192, MODE>(a, p, grid, dev, stream);
-        default: return launch_mode<256, kStages256, MODE>(a, p, grid, dev, stream);
-    }
+    if (bn == 160) return launch_mode<160, kStages160, MODE>(a, p, grid, dev, stream);
+    if constexpr (MODE == kSplitK) return cudaErrorNotSupported;  // split-K plans use 160 only
+    else return launch_mode<256, kStages256, MODE>(a, p, grid, dev, stream);
 }
 
 }  // namespace

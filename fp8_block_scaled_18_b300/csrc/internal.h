@@ -24,7 +24,7 @@ cudaError_t device_info(DeviceInfo* out);
 uint64_t wait_timeout_ns();
 
 // Encode a 2-D TMA descriptor over a row-major tensor [rows, inner] of
-// elem_bytes-sized elements (1 or 2) with the given row stride in bytes;
+// elem_bytes-sized elements (1, 2 or 4; 4 = fp32) with the given row stride in bytes;
 // boxes of box_rows x box_inner elements; swizzle128 selects the 128-byte
 // swizzle (the MMA operand layout), else no swizzle.  Reads outside the
 // tensor fill with zeros.  (tmap.cu)

@@ -99,6 +99,22 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
     return __all_sync(0xffffffffu, ok);
 }
 
+// ---------------------------------------------------------------- cp.async
+
+// 4-byte asynchronous copy global -> shared (L1-allocating).  The copies a
+// thread issues are grouped by cp_async_commit; cp_async_wait<N> returns once
+// at most N of the thread's most recent groups are still pending, after which
+// the thread sees the data (other threads after a __syncwarp/__syncthreads).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

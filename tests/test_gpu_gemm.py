@@ -55,6 +55,26 @@ def test_gemm_ragged_shapes(F, orc, M, N, K):
     _gemm_only(F, orc, x, w)
 
 
+@pytest.mark.parametrize("M,N,K", [
+    # 148 SMs: 160-column tiles 32 x 5 = 160 (two waves), 256-column 32 x 3 = 96
+    # (one wave) -> the 256-column kernel, ragged in M, N and with 3 K chunks
+    (4000, 700, 384),
+    # 160-column 32 x 8 = 256 tiles (two waves) against 256-column 32 x 5 = 160
+    # (two waves) -> the 160-column kernel, persistent CTAs taking two tiles
+    (4000, 1200, 256),
+])
+def test_gemm_both_tile_widths(F, orc, M, N, K):
+    """Shapes picked so that each tile width runs over several CTAs with
+    ragged edges; every row whose index is 0 or 127 modulo 128, plus a
+    random sample, is compared."""
+    rng = np.random.default_rng(M + N + K)
+    x = synth.activations(rng, M, K, n_outlier=4, outlier_scale=25.0)
+    w = synth.normal_bf16(rng, (N, K), 0.02)
+    edge = np.array(sorted({r for t in range(0, M, 128) for r in (t, min(t + 127, M - 1))}))
+    rows = np.union1d(edge, sample_rows(M, 64, seed=K))
+    _gemm_only(F, orc, x, w, rows=rows)
+
+
 @pytest.mark.parametrize("M", [1, 16, 64])
 def test_gemm_decode_split_k_matches_unsplit(F, orc, M):
     """Small-M uses a split-K plan when a workspace is given; both plans are
