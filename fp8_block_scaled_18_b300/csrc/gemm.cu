@@ -304,6 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    // Everything above touches only shared memory; from here on the kernel
+    // reads its inputs and claims TMEM, which the previous kernel in the
+    // stream may still be using.
+    grid_dependency_wait();
+    allow_dependents();
     if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
     constexpr bool GROUPED = MODE == kGrouped;
     if (GROUPED && warp == kEpiWarp0) build_tile_table<BN>(p, prefix, lane);
@@ -600,6 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Deterministic split-K reduction: y = bf16(sum over splits in order 0..S-1).
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int splits, int M,
                                                            int N, uint16_t* __restrict__ y, int64_t ldy) {
+    grid_dependency_wait();  // the partial sums come from the GEMM just before
+    allow_dependents();
     const int64_t nch = (N + 7) / 8;
     const int64_t total = static_cast<int64_t>(M) * nch;
     const bool vec = (N & 3) == 0;
@@ -752,8 +759,8 @@ cudaError_t launch_mode(const GemmArgs& a, Params& p, int grid, const DeviceInfo
     // sx [M, lds] fp32: boxes of kScaleChunks chunks x BM rows
     if ((e = make_tmap_2d(&tmS, a.sx, 4, a.lds, a.M, a.lds * 4, kScaleChunks, BM, false)) != cudaSuccess) return e;
     if ((e = ensure_kernel_ready<BN, STAGES, MODE>(dev.device)) != cudaSuccess) return e;
-    fp8_gemm_kernel<BN, STAGES, MODE><<<grid, kThreads, Layout<BN, STAGES>::ALLOC, stream>>>(tmA, tmB, tmS, p);
-    return cudaGetLastError();
+    return launch_pdl(fp8_gemm_kernel<BN, STAGES, MODE>, dim3(grid), dim3(kThreads), Layout<BN, STAGES>::ALLOC,
+                      stream, tmA, tmB, tmS, p);
 }
 
 template <int MODE>
@@ -799,8 +806,8 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
         if (e != cudaSuccess) return e;
         const int64_t work = a.M * ((a.N + 7) / 8);
         const int blocks = static_cast<int>(std::min<int64_t>((work + 255) / 256, dev.num_sms * 8));
-        splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(p.partial, pl.splits, p.M, p.N, a.y, a.ldy);
-        return cudaGetLastError();
+        return launch_pdl(splitk_reduce_kernel, dim3(blocks), dim3(256), 0, stream,
+                          static_cast<const float*>(p.partial), pl.splits, p.M, p.N, a.y, a.ldy);
     }
     return launch_bn<kDense>(pl.bn, a, p, pl.grid, dev, stream);
 }

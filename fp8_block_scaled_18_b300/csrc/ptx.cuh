@@ -99,6 +99,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
     return __all_sync(0xffffffffu, ok);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// A kernel launched with programmatic stream serialisation may start while
+// the previous kernel in its stream is still running.  grid_dependency_wait()
+// returns once that kernel has completed and its memory is visible, so it
+// must come before the kernel's first global-memory access (read or write)
+// and before it claims any resource the previous kernel might still need
+// (TMEM).  allow_dependents() lets the next such kernel start its prologue.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- cp.async
 
 // 4-byte asynchronous copy global -> shared (L1-allocating).  The copies a

@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
                                                        int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
                                                        float* __restrict__ sx, int64_t lds,
                                                        int64_t total_groups) {
+    grid_dependency_wait();  // the previous kernel may still read xq / sx
+    allow_dependents();
     const int lane = threadIdx.x & 31;
     const int sub = lane & (kAqTeam - 1);
     const int team = lane / kAqTeam;
@@ -188,6 +190,8 @@ template <int kWqThreads>
 __global__ void __launch_bounds__(kWqThreads) weight_quant_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                           uint8_t* __restrict__ wq, float* __restrict__ sw) {
     constexpr int kWqRowStep = kWqThreads / 16;  // rows between a thread's loads
+    grid_dependency_wait();
+    allow_dependents();
     constexpr int kWqRowsPerThread = 128 / kWqRowStep;
     __shared__ float warp_max[kWqThreads / 32];
     const int kb = blockIdx.x, nb = blockIdx.y;
@@ -232,6 +236,8 @@ __global__ void __launch_bounds__(kDqThreads) weight_dequant_kernel(const uint8_
                                                             const float* __restrict__ sw, int64_t N,
                                                             int64_t K, uint16_t* __restrict__ w) {
     constexpr int kDqRowStep = kDqThreads / 8;
+    grid_dependency_wait();  // wq / sw may come from the kernel just before
+    allow_dependents();
     constexpr int kDqRowsPerThread = 128 / kDqRowStep;
     const int kb = blockIdx.x, nb = blockIdx.y;
     const int64_t KB = K / 128;
@@ -299,28 +305,23 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ld
     const int64_t blocks_needed = (warps_needed + 7) / 8;
     const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 8;  // 8 x 256 threads per SM
     const int blocks = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
-    act_quant_kernel<<<blocks, 256, 0, stream>>>(x, KB, ldx, xq, ldq, sx, lds, groups);
-    return cudaGetLastError();
+    return launch_pdl(act_quant_kernel, dim3(blocks), dim3(256), 0, stream, x, KB, ldx, xq, ldq, sx, lds, groups);
 }
 
 cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
                                 const DeviceInfo& dev, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
     if (static_cast<int64_t>(grid.x) * grid.y < 2 * static_cast<int64_t>(dev.num_sms))
-        weight_quant_kernel<512><<<grid, 512, 0, stream>>>(w, N, K, wq, sw);
-    else
-        weight_quant_kernel<256><<<grid, 256, 0, stream>>>(w, N, K, wq, sw);
-    return cudaGetLastError();
+        return launch_pdl(weight_quant_kernel<512>, grid, dim3(512), 0, stream, w, N, K, wq, sw);
+    return launch_pdl(weight_quant_kernel<256>, grid, dim3(256), 0, stream, w, N, K, wq, sw);
 }
 
 cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
                                   const DeviceInfo& dev, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
     if (static_cast<int64_t>(grid.x) * grid.y < 2 * static_cast<int64_t>(dev.num_sms))
-        weight_dequant_kernel<512><<<grid, 512, 0, stream>>>(wq, sw, N, K, w);
-    else
-        weight_dequant_kernel<256><<<grid, 256, 0, stream>>>(wq, sw, N, K, w);
-    return cudaGetLastError();
+        return launch_pdl(weight_dequant_kernel<512>, grid, dim3(512), 0, stream, wq, sw, N, K, w);
+    return launch_pdl(weight_dequant_kernel<256>, grid, dim3(256), 0, stream, wq, sw, N, K, w);
 }
 
 cudaError_t launch_e4m3_encode(const float* v, int64_t n, uint8_t* q, const DeviceInfo& dev,
