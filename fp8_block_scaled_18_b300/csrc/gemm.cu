@@ -287,6 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
     int* prefix = reinterpret_cast<int*>(smem + L::OFF_TABLE);
 
+    if (threadIdx.x == 32) {  // the descriptors are kernel parameters: fetch them while the set-up runs
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmS);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -325,10 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSetup));
       if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(&tmB);
-        }
         uint32_t it = 0;
         bool ok = true;
         WorkCursor<BN, MODE> wc;
@@ -394,7 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Per block of kScaleChunks chunks: sx of the tile's rows by TMA (one
         // 16-byte column per row, so the promotion threads never gather
         // scattered 4-byte values), and the tile's weight scales by plain loads.
-        if (lane == 0) tma_prefetch_desc(&tmS);
         const int nblk = (p.N + 127) / 128;  // weight-scale blocks per operand
         float* sw_slots = reinterpret_cast<float*>(smem + L::OFF_SWS);
         uint32_t sb = 0;
