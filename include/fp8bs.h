@@ -27,6 +27,11 @@
  *     device memory in any call (it holds a small static status word per
  *     device, and the fixed scratch array of fp8bs_gemm_noalloc).
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *     The kernels are launched with programmatic stream serialisation: one
+ *     may start its set-up while the previous kernel on the stream finishes,
+ *     but it waits for that kernel to complete before it reads or writes any
+ *     global memory, so stream order is kept exactly as for plain launches
+ *     (also inside CUDA graphs captured from the stream).
  *     Argument errors are returned synchronously and launch nothing.  Errors
  *     inside a kernel (a bounded pipeline wait that expired) are recorded in
  *     the device status word and reported by fp8bs_sync_status().
