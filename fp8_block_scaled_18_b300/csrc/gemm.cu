@@ -8,7 +8,8 @@
 // four K=32 MMAs, after the Float8 paragraph of the 88811315.cn post and the
 // "FP8 量化" section of the qdgithub overview.)
 //
-// Design (one persistent CTA per SM, 384 threads = 3 warpgroups, warp-specialised):
+// Design (one persistent CTA per SM, warp-specialised; 384 threads for 160-
+// and 256-column tiles, 512 for 192-column tiles):
 //   warp 0      TMA producer: A (128 x 128 B) and B (BN x 128 B) tiles of one
 //               K chunk per pipeline stage, 128-byte swizzled, mbarrier
 //               completion by byte count.
@@ -30,19 +31,20 @@
 //               every promotion thread fetch its own row's sx from global
 //               memory, 4 scattered bytes per chunk, cost up to a third of
 //               the large GEMMs' time in load/store traffic.
-//   warps 4-11  promotion + epilogue: two warpgroups, each owning BN/2
-//               columns; thread = one row (TMEM lane).  Per chunk:
+//   warps 4-    promotion + epilogue: two warpgroups (three for 192-column
+//               tiles), each owning BN/NWG columns; thread = one row (TMEM
+//               lane).  Per chunk:
 //               tcgen05.ld the raw chunk sum P_kb, acc += fp32(sx*sw) * P_kb
 //               in registers (packed f32x2 FMAs), release the TMEM buffer.
 //               After the last chunk of a tile: round to bf16 and store (or
 //               store fp32 partials for split-K).
-// Every promotion thread keeps BN/2 fp32 accumulators (128 at BN = 256),
+// Every promotion thread keeps BN/NWG fp32 accumulators (128 at BN = 256),
 // so the warpgroups rebalance registers after set-up (setmaxnreg): the
-// set-up warpgroup drops to kRegsSetup, the promotion warpgroups rise to
-// kRegsPromo.  Per SM sub-partition (one set-up warp + two promotion warps)
-// that is kRegsSetup + 2 * kRegsPromo = 3 * kRegsLaunch registers per lane,
-// exactly what the launch reserved; the host refuses the kernel unless its
-// compiled register count is kRegsLaunch.
+// set-up warpgroup drops to Roles::kRegsSetup, the promotion warpgroups rise
+// to Roles::kRegsPromo.  Per SM sub-partition (one set-up warp + NWG
+// promotion warps) that stays within the (1 + NWG) * Roles::kRegsLaunch
+// registers per lane the launch reserved; the host refuses the kernel unless
+// its compiled register count is Roles::kRegsLaunch.
 // The TMEM buffers let the tensor core run up to 512/BN - 1 chunks ahead of
 // the CUDA cores that promote them.
 #include <cuda.h>
@@ -61,16 +63,28 @@ namespace {
 constexpr int BM = 128;           // tile rows (tokens) = TMEM lanes
 constexpr int BK = 128;           // K chunk = one scale block = 4 MMAs of K=32
 constexpr int UMMA_K = 32;
-constexpr int kThreads = 384;
 constexpr int kMmaWarp0 = 1;      // MMA issuers: warps 1 and 2
 constexpr int kMmaWarps = 2;
 constexpr int kEpiWarp0 = 4;      // first promotion/epilogue warp
-constexpr int kRegsLaunch = 168;  // 65536 / 384, rounded down to a multiple of 8
-constexpr int kRegsSetup = 56;
-constexpr int kRegsPromo = 224;
-static_assert(kRegsSetup + 2 * kRegsPromo == 3 * kRegsLaunch, "register split must match the launch");
-constexpr int kEpiWarps = 8;
 constexpr int kScaleWarp = 3;     // scale loader
+
+// Promotion warpgroups per tile width: two for 160- and 256-column tiles,
+// three for 192, whose warpgroups then hold 64 columns each and load a
+// chunk's share from TMEM in one go.  The set-up warpgroup (warps 0-3) gives
+// registers to the promotion warpgroups with setmaxnreg; per SM
+// sub-partition one set-up warp and NWG promotion warps must fit in the
+// (1 + NWG) * kRegsLaunch registers per lane the launch reserved.
+__host__ __device__ constexpr int nwg_for(int bn) { return bn == 192 ? 3 : 2; }
+template <int NWG>
+struct Roles {
+    static constexpr int kThreads = 128 * (1 + NWG);
+    static constexpr int kEpiWarps = 4 * NWG;
+    static constexpr int kRegsLaunch = NWG == 2 ? 168 : 128;  // 65536 / threads, a multiple of 8
+    static constexpr int kRegsSetup = NWG == 2 ? 56 : 40;
+    static constexpr int kRegsPromo = NWG == 2 ? 224 : 152;
+    static_assert(kRegsLaunch * kThreads <= 65536, "one CTA per SM");
+    static_assert(kRegsSetup + NWG * kRegsPromo <= (1 + NWG) * kRegsLaunch, "register split must fit the launch");
+};
 constexpr int kScaleChunks = 4;   // K chunks per scale block (one 16-byte TMA column of sx)
 constexpr int kScaleSlots = 4;    // scale blocks in flight
 constexpr int kSwBlocks = 3;      // weight-scale blocks a tile of <= 256 columns can touch
@@ -84,7 +98,9 @@ struct Layout {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
-    static constexpr int NBUF = 512 / BN;                       // TMEM chunk buffers
+    // TMEM chunk buffers, each starting on a 32-column boundary
+    static constexpr int BUF_COLS = (BN + 31) / 32 * 32;
+    static constexpr int NBUF = 512 / BUF_COLS;
     // full[S], empty[S], tfull[NBUF], tempty[NBUF], done[2], sfull[4], sempty[4]
     static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
     // + one drain barrier per issuer + sfull/sempty per scale slot
@@ -103,7 +119,7 @@ struct Layout {
     static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;                  // allocation: a power of two
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
-    static_assert(NBUF >= 2 && NBUF * BN <= 512, "two or more chunk buffers must fit in TMEM");
+    static_assert(NBUF >= 2 && NBUF * BUF_COLS <= 512, "two or more chunk buffers must fit in TMEM");
 };
 
 struct Params {
@@ -262,11 +278,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 
 template <int BN, int STAGES, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmS, const __grid_constant__ Params p) {
     using L = Layout<BN, STAGES>;
-    static_assert(BN == 160 || BN == 256, "tile widths the host dispatches");
+    using R = Roles<nwg_for(BN)>;
+    constexpr int kEpiWarps = R::kEpiWarps;
+    static_assert(BN == 160 || BN == 192 || BN == 256, "tile widths the host dispatches");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
@@ -327,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
     if (warp < kEpiWarp0) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSetup));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R::kRegsSetup));
       if (warp == 0) {
         // ------------------------------------------------------------ producer
         uint32_t it = 0;
@@ -373,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const uint64_t adesc = sdesc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
                     const uint64_t bdesc = sdesc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
-                    const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                    const uint32_t d = tmem + static_cast<uint32_t>(b * L::BUF_COLS);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)  // +32 bytes along K = +2 in the address field
                         umma_e4m3(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
@@ -438,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
         // ------------------------------------------------------------ promotion + epilogue
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsPromo));
-        constexpr int COLS = BN / 2;        // columns per warpgroup
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R::kRegsPromo));
+        constexpr int COLS = BN / nwg_for(BN);  // columns per warpgroup
         // A warpgroup holding up to 96 columns loads a whole chunk at once and
         // releases the TMEM buffer before its FMAs (WHOLE); with 128 columns
         // it walks 16-column slices, loading slice c+1 during slice c's FMAs.
@@ -517,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < NF; ++c) f2[c] = ((upper >> c) & 1u) ? f2hi : f2lo;
                 if (!warp_wait(tfull_bar(b), bph, ctl)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * BN + col0);
+                const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * L::BUF_COLS + col0);
                 // promotion: acc += f * P_kb, slice by slice of 32 columns; the
                 // TMEM load of slice c+1 overlaps the FMAs of slice c
                 if constexpr (WHOLE) {
@@ -657,24 +675,25 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return make_tmap_2d(map, base, 1, inner, rows, stride_bytes, BK, box_rows, true);
 }
 
-// Tile widths 256 or 160 columns.  A CTA's time per 128-K chunk is set by
-// the round trip of its TMEM buffers (MMA, promotion, release) more than by
-// the MMA width: 256-column tiles fit two buffers in the 512 TMEM columns,
-// 160-column tiles fit three and measured about 0.86 of the 256-column
-// period.  The width with the fewest waves of tiles times that period wins;
-// ties go to the wider tile.  (192-column tiles measured the 256-column
-// period, so never win; 128-column tiles measured slower everywhere.)
-// Stages: as many 128-K stages as fit in shared memory next to the tables
-// and the scale slots.
+// Tile widths 256, 192 or 160 columns.  A CTA's time per 128-K chunk is set
+// by the round trip of its TMEM buffers (MMA, promotion, release) more than
+// by the MMA width.  Measured on B300, relative to 256-column tiles (two TMEM
+// buffers, two promotion warpgroups of 128 columns): 192-column tiles with
+// three promotion warpgroups 0.91, 160-column tiles (three buffers) 0.77.
+// The width with the fewest waves of tiles times that period wins; ties go to
+// the wider tile.  (144-column tiles, 0.81, never need fewer waves than 160;
+// 128-column tiles measured slower everywhere.)  Stages: as many 128-K
+// stages as fit in shared memory next to the tables and the scale slots.
 constexpr int kStages256 = 4;  // (16 + 32) KB per stage
 constexpr int kStages160 = 5;  // (16 + 20) KB per stage
+constexpr int kStages192 = 5;  // (16 + 24) KB per stage
 
 int pick_bn(int64_t M, int64_t N, int num_sms) {
-    constexpr int kWidths[2] = {256, 160};
-    constexpr int kPeriod[2] = {100, 86};  // relative chunk period
+    constexpr int kWidths[3] = {256, 192, 160};
+    constexpr int kPeriod[3] = {100, 91, 77};  // relative chunk period
     int best = 256;
     int64_t best_cost = INT64_MAX;
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
         const int64_t tiles = ((M + BM - 1) / BM) * ((N + kWidths[i] - 1) / kWidths[i]);
         const int64_t cost = ((tiles + num_sms - 1) / num_sms) * kPeriod[i];
         if (cost < best_cost) {
@@ -735,13 +754,13 @@ cudaError_t ensure_kernel_ready(int device) {
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!done[device]) {
         auto* k = fp8_gemm_kernel<BN, STAGES, MODE>;
-        // The setmaxnreg split assumes exactly kRegsLaunch registers per
+        // The setmaxnreg split assumes exactly Roles::kRegsLaunch registers per
         // thread at launch; any other count could leave a warpgroup waiting
         // for registers that never free up.
         cudaError_t e;
         cudaFuncAttributes attr;
         if ((e = cudaFuncGetAttributes(&attr, k)) != cudaSuccess) return e;
-        if (attr.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
+        if (attr.numRegs != Roles<nwg_for(BN)>::kRegsLaunch) return cudaErrorInvalidKernelImage;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BN, STAGES>::ALLOC);
         if (e != cudaSuccess) return e;
         done[device] = true;
@@ -759,15 +778,20 @@ cudaError_t launch_mode(const GemmArgs& a, Params& p, int grid, const DeviceInfo
     // sx [M, lds] fp32: boxes of kScaleChunks chunks x BM rows
     if ((e = make_tmap_2d(&tmS, a.sx, 4, a.lds, a.M, a.lds * 4, kScaleChunks, BM, false)) != cudaSuccess) return e;
     if ((e = ensure_kernel_ready<BN, STAGES, MODE>(dev.device)) != cudaSuccess) return e;
-    return launch_pdl(fp8_gemm_kernel<BN, STAGES, MODE>, dim3(grid), dim3(kThreads), Layout<BN, STAGES>::ALLOC,
+    return launch_pdl(fp8_gemm_kernel<BN, STAGES, MODE>, dim3(grid), dim3(Roles<nwg_for(BN)>::kThreads),
+                      Layout<BN, STAGES>::ALLOC,
                       stream, tmA, tmB, tmS, p);
 }
 
 template <int MODE>
 cudaError_t launch_bn(int bn, const GemmArgs& a, Params& p, int grid, const DeviceInfo& dev, cudaStream_t stream) {
     if (bn == 160) return launch_mode<160, kStages160, MODE>(a, p, grid, dev, stream);
-    if constexpr (MODE == kSplitK) return cudaErrorNotSupported;  // split-K plans use 160 only
-    else return launch_mode<256, kStages256, MODE>(a, p, grid, dev, stream);
+    if constexpr (MODE == kSplitK) {
+        return cudaErrorNotSupported;  // split-K plans use 160 only
+    } else {
+        if (bn == 192) return launch_mode<192, kStages192, MODE>(a, p, grid, dev, stream);
+        return launch_mode<256, kStages256, MODE>(a, p, grid, dev, stream);
+    }
 }
 
 }  // namespace

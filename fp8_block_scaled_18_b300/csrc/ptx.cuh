@@ -394,6 +394,44 @@ __device__ __forceinline__ void fma_pairs(uint64_t (&acc)[8], const uint64_t (&c
         : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(f2));
 }
 
+// Load 48 consecutive fp32 TMEM columns of this warp's 32 lanes (one
+// wait for all the loads) as 24 packed pairs.
+__device__ __forceinline__ void tmem_ld_cols_pairs(uint32_t taddr, uint64_t (&p)[24]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<48>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%24];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t32,t33,t34,t35,t36,t37,t38,t39,t40,t41,t42,t43,t44,t45,t46,t47}, [%25];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "mov.b64 %16, {t32, t33};\n\t"
+        "mov.b64 %17, {t34, t35};\n\t"
+        "mov.b64 %18, {t36, t37};\n\t"
+        "mov.b64 %19, {t38, t39};\n\t"
+        "mov.b64 %20, {t40, t41};\n\t"
+        "mov.b64 %21, {t42, t43};\n\t"
+        "mov.b64 %22, {t44, t45};\n\t"
+        "mov.b64 %23, {t46, t47};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23])
+        : "r"(taddr + 0u), "r"(taddr + 32u)
+        : "memory");
+}
+
 // Load 64 consecutive fp32 TMEM columns of this warp's 32 lanes (one
 // wait for all the loads) as 32 packed pairs.
 __device__ __forceinline__ void tmem_ld_cols_pairs(uint32_t taddr, uint64_t (&p)[32]) {

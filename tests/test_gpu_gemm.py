@@ -56,14 +56,18 @@ def test_gemm_ragged_shapes(F, orc, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [
-    # 148 SMs: 160-column tiles 32 x 5 = 160 (two waves), 256-column 32 x 3 = 96
-    # (one wave) -> the 256-column kernel, ragged in M, N and with 3 K chunks
+    # 148 SMs, relative chunk periods 256 -> 1.00, 192 -> 0.91, 160 -> 0.77:
+    # 256 columns 32 x 4 = 128 tiles (one wave) against 192: 32 x 6 = 192 and
+    # 160: 32 x 7 = 224 (two waves each) -> the 256-column kernel
+    (4000, 1000, 384),
+    # 256: 32 x 3 = 96 and 192: 32 x 4 = 128 tiles (one wave), 160: 160 tiles
+    # (two) -> the 192-column kernel (three promotion warpgroups)
     (4000, 700, 384),
-    # 160-column 32 x 8 = 256 tiles (two waves) against 256-column 32 x 5 = 160
-    # (two waves) -> the 160-column kernel, persistent CTAs taking two tiles
+    # 256: 160, 192: 224, 160: 256 tiles, two waves each -> the 160-column
+    # kernel, persistent CTAs taking two tiles
     (4000, 1200, 256),
 ])
-def test_gemm_both_tile_widths(F, orc, M, N, K):
+def test_gemm_tile_widths(F, orc, M, N, K):
     """Shapes picked so that each tile width runs over several CTAs with
     ragged edges; every row whose index is 0 or 127 modulo 128, plus a
     random sample, is compared."""
@@ -124,6 +128,44 @@ def _pipeline(F, orc, case, nrows=24, seed=0):
 
 def test_pipeline_kv_down_full(F, orc):
     _pipeline(F, orc, synth.kv_down())
+
+
+def test_stream_order_with_shared_buffers(F, orc):
+    """Kernels start early under programmatic dependent launch; each must wait
+    for its predecessor before touching memory.  Two inputs alternate through
+    one Xq/Sx and one Wq/Sw buffer on one stream with no host sync between
+    calls, so every weight_quant and act_quant overwrites what the GEMM just
+    before it reads (write after read), and every GEMM reads what was just
+    written (read after write).  Each output must match its own inputs."""
+    c1 = synth.kv_down()
+    M, N, K = c1.shape
+    rng = np.random.default_rng(77)
+    x2 = synth.activations(rng, M, K, n_outlier=16, outlier_scale=10.0)
+    w2 = synth.normal_bf16(rng, (N, K), 0.05)
+    cases = [(c1.x, c1.w), (x2, w2)]
+    xs = [dev_bf16(x) for x, _ in cases]
+    ws = [dev_bf16(w) for _, w in cases]
+    lds = (K // 128 + 3) // 4 * 4
+    xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    sx = torch.empty((M, lds), dtype=torch.float32, device="cuda")
+    wq = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device="cuda")
+    ys = []
+    for rep in range(3):
+        for i in range(2):
+            F.fp8bs_weight_quant(ws[i], wq=wq, sw=sw)
+            F.fp8bs_act_quant(xs[i], xq=xq, sx=sx)
+            ys.append((i, F.fp8bs_gemm(xq, sx, wq, sw)))
+    assert F.fp8bs_sync_status() == 0
+    rows = sample_rows(M, 16, seed=5)
+    for i, (x, w) in enumerate(cases):
+        xq_o, sx_o = orc.act_quant(x[rows])
+        wq_o, sw_o = orc.weight_quant(w)
+        y_ref, L = orc.gemm(xq_o, sx_o, wq_o, sw_o)
+        outs = [host(y) for j, y in ys if j == i]
+        assert_gemm_close(outs[0][rows], y_ref, L, f"input {i}")
+        for o in outs[1:]:
+            assert np.array_equal(o, outs[0]), f"input {i}: a repetition differs"
 
 
 @pytest.mark.parametrize("M", list(synth.Q_SWEEP_M))
