@@ -115,7 +115,7 @@ def sum_over_ranks(x: float, world: int, device: str = "cpu") -> float:
 
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
-    for name in ("quant.cu", "gemm.cu", "ptx.cuh"):
+    for name in ("quant.cu", "gemm.cu", "ptx.cuh", "codec.cuh"):
         with open(os.path.join(ROOT, "fp8_block_scaled_18_b300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -192,9 +192,11 @@ class ClockSampler:
 # ---------------------------------------------------------------- workloads
 
 class DenseWork:
-    """weight_quant(W) -> act_quant(X) -> fp8_gemm -> weight_dequant(Wq)."""
+    """weight_quant(W) -> act_quant(X) -> fp8_gemm -> weight_dequant(Wq).
+    fused: the GEMM is fp8bs_gemm_fused with a bias and the output re-quantised
+    to FP8 (1x128 groups, ready for the next FP8 GEMM) instead of bf16."""
 
-    def __init__(self, case, device):
+    def __init__(self, case, device, fused=False):
         import torch
         from fp8_block_scaled_18_b300 import fp8bs as F
         self.F = F
@@ -207,6 +209,10 @@ class DenseWork:
         self.R = max(1, min(8, math.ceil(2 * L2_BYTES / per_set) + 1)) if per_set < 2 * L2_BYTES else 1
         lds = max(4, (K // 128 + 3) // 4 * 4)
         ws_bytes = F.fp8bs_gemm_workspace_size(M, N, K)
+        self.fused = fused
+        if fused:
+            self.bias = torch.from_numpy(
+                np.random.default_rng(5).standard_normal(N).astype(np.float32)).to(torch.bfloat16).to(device)
         self.sets = []
         for _ in range(self.R):
             s = dict(x=self.x_host.to(device), w=self.w_host.to(device),
@@ -217,6 +223,11 @@ class DenseWork:
                      y=torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=device)[:, :N],
                      wd=torch.empty((N, K), dtype=torch.bfloat16, device=device),
                      ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None)
+            if fused:
+                s["yq"] = torch.empty((M, N), dtype=torch.uint8, device=device)
+                s["sy"] = torch.empty((M, max(4, (N // 128 + 3) // 4 * 4)), dtype=torch.float32, device=device)
+                s["yq2"] = torch.empty((M, N), dtype=torch.uint8, device=device)
+                s["sy2"] = torch.empty((M, max(4, (N // 128 + 3) // 4 * 4)), dtype=torch.float32, device=device)
             self.sets.append(s)
         self.set_bytes = per_set
         self.gemm_launches = 2 if ws_bytes else 1
@@ -234,6 +245,17 @@ class DenseWork:
                                3.0 * N * K + 4.0 * nb * kb, "hbm"),
         }
         self.order = ["weight_quant", "act_quant", "fp8_gemm", "weight_dequant"]
+        if fused:
+            # the fused GEMM, and what it replaces: the plain GEMM plus act_quant over its output
+            self.kernels["fp8_gemm_fused"] = (
+                lambda s: F.fp8bs_gemm_fused(s["xq"], s["sx"], s["wq"], s["sw"], bias=self.bias, want_y=False,
+                                             want_fp8=True, yq=s["yq"], sy=s["sy"]), 1, self.flops, "tensor")
+            self.kernels["act_quant_of_y"] = (lambda s: F.fp8bs_act_quant(s["y"], xq=s["yq2"], sx=s["sy2"]), 1,
+                                              3.0 * M * N + 4.0 * M * (N // 128), "hbm")
+            self.order = ["weight_quant", "act_quant", "fp8_gemm_fused", "weight_dequant", "fp8_gemm",
+                          "act_quant_of_y"]
+        self.step_kernels = ["weight_quant", "act_quant", "fp8_gemm_fused" if fused else "fp8_gemm",
+                             "weight_dequant"]
         # weight_quant and weight_dequant run on a second stream: they need
         # nothing from act_quant, and the GEMM only needs weight_quant's output
         self.side = torch.cuda.Stream(device=device)
@@ -250,31 +272,46 @@ class DenseWork:
         F.fp8bs_weight_dequant(s["wq"], s["sw"], w=s["wd"], stream=self.side)
         F.fp8bs_act_quant(s["x"], xq=s["xq"], sx=s["sx"], stream=main)
         main.wait_event(self.wq_done)
-        F.fp8bs_gemm(s["xq"], s["sx"], s["wq"], s["sw"], y=s["y"], workspace=s["ws"], stream=main)
+        if self.fused:
+            F.fp8bs_gemm_fused(s["xq"], s["sx"], s["wq"], s["sw"], bias=self.bias, want_y=False, want_fp8=True,
+                               yq=s["yq"], sy=s["sy"], stream=main)
+        else:
+            F.fp8bs_gemm(s["xq"], s["sx"], s["wq"], s["sw"], y=s["y"], workspace=s["ws"], stream=main)
         main.wait_stream(self.side)
 
     def launches_per_step(self):
-        return sum(self.kernels[k][1] for k in self.order)
+        return sum(self.kernels[k][1] for k in self.step_kernels)
 
-    # e2e: host (pinned) bf16 X and W in, bf16 Y out, through the public calls
+    # e2e: host (pinned) bf16 X and W in, the output (bf16 Y, or FP8 Yq and
+    # its scales for the fused workload) out, through the public calls
     def e2e_setup(self):
         self.xp = self.x_host.pin_memory()
         self.wp = self.w_host.pin_memory()
         import torch
-        self.yp = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
         self.h2d = self.xp.numel() * 2 + self.wp.numel() * 2
-        self.d2h = self.yp.numel() * 2
+        if self.fused:
+            self.yp = torch.empty((self.M, self.N), dtype=torch.uint8).pin_memory()
+            self.syp = torch.empty(self.sets[0]["sy"].shape, dtype=torch.float32).pin_memory()
+            self.d2h = self.yp.numel() + self.syp.numel() * 4
+        else:
+            self.yp = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
+            self.d2h = self.yp.numel() * 2
 
     def e2e_step(self, i):
         s = self.sets[i % self.R]
         s["w"].copy_(self.wp, non_blocking=True)
         s["x"].copy_(self.xp, non_blocking=True)
         self.step(i)
-        self.yp.copy_(s["y"], non_blocking=True)
+        if self.fused:
+            self.yp.copy_(s["yq"], non_blocking=True)
+            self.syp.copy_(s["sy"], non_blocking=True)
+        else:
+            self.yp.copy_(s["y"], non_blocking=True)
 
     def config(self):
-        return {"workload": self.case.name, "M": self.M, "N": self.N, "K": self.K,
-                "step": "weight_quant+act_quant+fp8_gemm+weight_dequant",
+        return {"workload": self.case.name + ("_fused" if self.fused else ""), "M": self.M, "N": self.N, "K": self.K,
+                "step": "weight_quant+act_quant+" + ("fp8_gemm_fused(bias, fp8 out)" if self.fused
+                                                      else "fp8_gemm") + "+weight_dequant",
                 "streams": "weight_quant then weight_dequant on a second stream (joined before the GEMM "
                            "and at the end of each step); act_quant then fp8_gemm on the main stream",
                 "l2": f"inputs rotate over {self.R} buffer sets of {self.set_bytes / 1e6:.0f} MB (> 126 MB L2)"
@@ -358,6 +395,8 @@ def make_work(name: str, device):
         return DenseWork(synth.tiny(), device)
     if name == "large_square":
         return DenseWork(synth.large_square(), device)
+    if name.startswith("q_down_m") and name.endswith("_fused"):
+        return DenseWork(synth.q_down(int(name[len("q_down_m"):-len("_fused")])), device, fused=True)
     if name.startswith("q_down_m"):
         return DenseWork(synth.q_down(int(name[len("q_down_m"):])), device)
     raise SystemExit(f"unknown workload {name}")
@@ -449,6 +488,10 @@ def run_ours(args, rank, local, world):
     hbm_peak = float(peaks["hbm_gbs"])
     fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
     kernels = {}
+    # shares and the roofline kernel over the step's own kernels; other
+    # kernels (comparisons) are timed alone and reported without a share
+    step_kernels = getattr(work, "step_kernels", work.order)
+    step_ms_sum = sum(kernel_ms[k] for k in step_kernels)
     for k in work.order:
         _, launches, units, bound = work.kernels[k]
         per_call_s = kernel_ms[k] / K * 1e-3
@@ -458,10 +501,11 @@ def run_ours(args, rank, local, world):
             ach, peak, unit = units / per_call_s / 1e9, hbm_peak, "GB/s"
         kernels[k] = {"us_per_call": round(per_call_s * 1e6, 3), "launches_per_call": launches,
                       "achieved": round(ach, 2), "unit": unit, "bound": bound,
-                      "frac": round(ach / peak, 4), "share": round(kernel_ms[k] / sum(kernel_ms.values()), 4)}
+                      "frac": round(ach / peak, 4),
+                      "share": round(kernel_ms[k] / step_ms_sum, 4) if k in step_kernels else None}
     if "fp8_gemm" in kernels:
         kernels["fp8_gemm"]["tflops"] = kernels["fp8_gemm"]["achieved"]
-    dom = max(work.order, key=lambda k: kernel_ms[k])
+    dom = max(step_kernels, key=lambda k: kernel_ms[k])
     _, launches, units, bound = work.kernels[dom]
     dom_s = kernel_ms[dom] / K * 1e-3
     if bound == "tensor":

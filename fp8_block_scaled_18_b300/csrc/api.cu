@@ -101,6 +101,40 @@ fp8bs_status fp8bs_gemm(const uint8_t* xq, const float* sx, int64_t lds, const u
     return from_cuda(launch_gemm(a, d, cs(stream)));
 }
 
+fp8bs_status fp8bs_gemm_fused(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* wq, const float* sw,
+                              const uint16_t* bias, int64_t M, int64_t N, int64_t K, uint16_t* y, int64_t ldy,
+                              uint8_t* yq, int64_t ldyq, float* sy, int64_t ldsy, fp8bs_stream_t stream) {
+    if (M < 0 || N < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (M == 0 || N == 0) return FP8BS_OK;
+    if (!y && !yq) return FP8BS_ERR_INVALID_ARG;  // nothing to write
+    if (!xq || !sx || !wq || !sw) return FP8BS_ERR_INVALID_ARG;
+    if (M > kMaxRows || N > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
+    if (lds < K / 128) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(wq) || !aligned16(sx) || lds % 4 || (reinterpret_cast<uintptr_t>(sw) & 3u))
+        return FP8BS_ERR_MISALIGNED;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8BS_ERR_MISALIGNED;
+    if (y) {
+        if (ldy < N) return FP8BS_ERR_INVALID_ARG;
+        if (!aligned16(y) || ldy % 8) return FP8BS_ERR_MISALIGNED;
+    }
+    if (yq) {
+        if (N % 128) return FP8BS_ERR_UNSUPPORTED;  // whole 128-column output groups only
+        if (!sy) return FP8BS_ERR_INVALID_ARG;
+        if (ldyq < N || ldsy < N / 128) return FP8BS_ERR_INVALID_ARG;
+        if (!aligned16(yq) || ldyq % 16 || !aligned16(sy) || ldsy % 4) return FP8BS_ERR_MISALIGNED;
+    }
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    GemmArgs a{xq, sx, lds, wq, sw, M, N, K, y, ldy, nullptr, 0, nullptr, 0};
+    a.bias = bias;
+    a.yq = yq;
+    a.ldyq = ldyq;
+    a.sy = sy;
+    a.ldsy = ldsy;
+    return from_cuda(launch_gemm(a, d, cs(stream)));
+}
+
 size_t fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || K % 128) return 0;
     DeviceInfo d;

@@ -54,6 +54,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "codec.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -115,7 +116,12 @@ struct Layout {
     static constexpr int SW_SLOT = kSwBlocks * kScaleChunks * 4;
     static constexpr int OFF_SX = (OFF_TABLE + TABLE_BYTES + 127) & ~127;
     static constexpr int OFF_SWS = OFF_SX + kScaleSlots * SX_SLOT;
-    static constexpr int BYTES = OFF_SWS + kScaleSlots * SW_SLOT;
+    // fused bias: per scale slot, the bf16 bias of the tile's BN columns
+    // (written with the first scale block of each tile)
+    static constexpr int OFF_BIAS = (OFF_SWS + kScaleSlots * SW_SLOT + 15) & ~15;
+    static constexpr int BIAS_SLOT = BN * 2;
+    static constexpr int BIAS_BYTES = kScaleSlots * BIAS_SLOT;
+    static constexpr int BYTES = OFF_BIAS + BIAS_BYTES;
     static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;                  // allocation: a power of two
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
@@ -126,8 +132,16 @@ struct Params {
     const float* sx;
     int64_t lds;
     const float* sw;
-    uint16_t* y;
+    uint16_t* y;             // bf16 output, or nullptr when only yq is written
     int64_t ldy;
+    // fused epilogue (dense, 256-column tiles for yq): y += bias before the
+    // bf16 rounding; yq / sy = the bf16 output quantised per row per 128
+    // columns, as act_quant would quantise it
+    const uint16_t* bias;    // bf16 [N] or nullptr
+    uint8_t* yq;             // e4m3 [M, ldyq] or nullptr
+    int64_t ldyq;
+    float* sy;               // fp32 [M, ldsy]
+    int64_t ldsy;
     const int32_t* offsets;  // grouped: device [G+1], else nullptr
     int G;
     int M, N, KB;
@@ -434,6 +448,16 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
             };
             const int q1 = (tl.kb1 - 1) / kScaleChunks;
             float v = load_sw(tl.kb0 / kScaleChunks);
+            // fused bias: lane l takes the tile's columns l, l + 32, ...;
+            // loaded now (alongside the first weight scales), stored with the
+            // tile's first scale block; columns past N read as 0
+            constexpr int kBiasPerLane = BN / 32;
+            uint16_t bias_v[kBiasPerLane];
+#pragma unroll
+            for (int i = 0; i < kBiasPerLane; ++i) {
+                const int n = tl.n0 + lane + 32 * i;
+                bias_v[i] = (p.bias != nullptr && n < p.N) ? p.bias[n] : uint16_t{0};
+            }
             for (int q = tl.kb0 / kScaleChunks; q <= q1; ++q, ++sb) {
                 // the next block's weight scales load while this block waits for its slot
                 const float v_next = q < q1 ? load_sw(q + 1) : 0.0f;
@@ -445,7 +469,12 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                     tma_load_2d(sbase + L::OFF_SX + s * L::SX_SLOT, &tmS, sfull_bar(s), q * kScaleChunks, tl.m0);
                 }
                 if (lane < kSwBlocks * kScaleChunks) sw_slots[s * (kSwBlocks * kScaleChunks) + lane] = v;
-                mbar_arrive(sfull_bar(s));   // releases this lane's store
+                if (p.bias != nullptr && q == tl.kb0 / kScaleChunks) {
+                    uint16_t* bias_slot = reinterpret_cast<uint16_t*>(smem + L::OFF_BIAS + s * L::BIAS_SLOT);
+#pragma unroll
+                    for (int i = 0; i < kBiasPerLane; ++i) bias_slot[lane + 32 * i] = bias_v[i];
+                }
+                mbar_arrive(sfull_bar(s));   // releases this lane's stores
                 v = v_next;
             }
         }
@@ -505,6 +534,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
             for (int c = 0; c < NCH; ++c)
                 if (n_first < p.N && (n_first + SW * c) / 128 - fb != i0) upper |= 1u << c;
             const int nk = tl.kb1 - tl.kb0;
+
             // running sums as packed fp32 pairs: acc[j] = (column 2j, column 2j+1)
             uint64_t acc[COLS / 2];
 #pragma unroll
@@ -519,6 +549,20 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                 if ((j == 0 || c4 == 0) && !warp_wait(sfull_bar(sl), (ss / kScaleSlots) & 1u, ctl)) {
                     ok = false;
                     break;
+                }
+                if (j == 0 && p.bias != nullptr) {
+                    // fused bias: the sums start from the bias (any fp32 summation
+                    // order is within the result's bound)
+                    const uint16_t* bias_s =
+                        reinterpret_cast<const uint16_t*>(smem + L::OFF_BIAS + sl * L::BIAS_SLOT) + col0;
+#pragma unroll
+                    for (int v = 0; v < COLS / 8; ++v) {
+                        const uint4 b8 = *reinterpret_cast<const uint4*>(bias_s + 8 * v);
+                        const uint32_t bw[4] = {b8.x, b8.y, b8.z, b8.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            acc[4 * v + t] = pack_f32x2(__uint_as_float(bw[t] << 16), __uint_as_float(bw[t] & 0xFFFF0000u));
+                    }
                 }
                 const float* swv = sw_slots + sl * (kSwBlocks * kScaleChunks) + c4;
                 const float sxv = sx_slots[sl * (BM * kScaleChunks) + row * kScaleChunks + c4];
@@ -587,25 +631,46 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                     }
                 }
             } else {
-                uint16_t* yr = p.y + static_cast<int64_t>(m) * p.ldy;
+                uint32_t yb[COLS / 2];  // bf16 pairs (column 2v in the low half)
 #pragma unroll
-                for (int v = 0; v < COLS / 8; ++v) {
-                    const int n = nbase + 8 * v;
-                    if (n + 8 <= p.N) {
-                        uint4 o;
-                        o.x = pack_bf16x2(lo_f32(acc[4 * v + 0]), hi_f32(acc[4 * v + 0]));
-                        o.y = pack_bf16x2(lo_f32(acc[4 * v + 1]), hi_f32(acc[4 * v + 1]));
-                        o.z = pack_bf16x2(lo_f32(acc[4 * v + 2]), hi_f32(acc[4 * v + 2]));
-                        o.w = pack_bf16x2(lo_f32(acc[4 * v + 3]), hi_f32(acc[4 * v + 3]));
-                        *reinterpret_cast<uint4*>(yr + n) = o;
-                    } else if (n < p.N) {
+                for (int v = 0; v < COLS / 2; ++v) yb[v] = pack_bf16x2(lo_f32(acc[v]), hi_f32(acc[v]));
+                if (p.y != nullptr) {
+                    uint16_t* yr = p.y + static_cast<int64_t>(m) * p.ldy;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (n + j < p.N) {
-                                const uint64_t pr = acc[4 * v + j / 2];
-                                const __nv_bfloat16 h = __float2bfloat16_rn((j & 1) ? hi_f32(pr) : lo_f32(pr));
-                                yr[n + j] = *reinterpret_cast<const uint16_t*>(&h);
-                            }
+                    for (int v = 0; v < COLS / 8; ++v) {
+                        const int n = nbase + 8 * v;
+                        if (n + 8 <= p.N) {
+                            *reinterpret_cast<uint4*>(yr + n) =
+                                make_uint4(yb[4 * v], yb[4 * v + 1], yb[4 * v + 2], yb[4 * v + 3]);
+                        } else if (n < p.N) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (n + j < p.N) yr[n + j] = static_cast<uint16_t>(yb[4 * v + j / 2] >> (16 * (j & 1)));
+                        }
+                    }
+                }
+                if constexpr (COLS == 128 && BN % 128 == 0) {
+                    // The warpgroup's 128 columns are exactly one output group
+                    // (the host asks for yq only with N % 128 == 0).
+                    if (p.yq != nullptr && nbase < p.N) {
+                        uint32_t amax2 = 0;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            amax2 = absmax_bits8(make_uint4(yb[4 * i], yb[4 * i + 1], yb[4 * i + 2], yb[4 * i + 3]),
+                                                 amax2);
+                        const float amax = bits_to_amax(amax2);
+                        const GroupScale gs = group_scale(amax);
+                        const bool zero = amax == 0.0f;
+                        uint8_t* qr = p.yq + static_cast<int64_t>(m) * p.ldyq + nbase;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint2 c0 = encode8(
+                                make_uint4(yb[8 * i], yb[8 * i + 1], yb[8 * i + 2], yb[8 * i + 3]), gs, zero);
+                            const uint2 c1 = encode8(
+                                make_uint4(yb[8 * i + 4], yb[8 * i + 5], yb[8 * i + 6], yb[8 * i + 7]), gs, zero);
+                            *reinterpret_cast<uint4*>(qr + 16 * i) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+                        }
+                        p.sy[static_cast<int64_t>(m) * p.ldsy + nbase / 128] = gs.s;
                     }
                 }
             }
@@ -817,7 +882,20 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
         p.G = a.G;
         return launch_mode<256, kStages256, kGrouped>(a, p, dev.num_sms, dev, stream);
     }
-    const Plan pl = dense_plan(a.M, a.N, a.K, dev.num_sms, a.workspace ? a.ws_bytes : 0);
+    const bool fused = a.bias != nullptr || a.yq != nullptr;
+    Plan pl = dense_plan(a.M, a.N, a.K, dev.num_sms, a.workspace && !fused ? a.ws_bytes : 0);
+    if (a.yq != nullptr && pl.bn != 256) {
+        // Output quantisation needs each promotion warpgroup to hold one whole
+        // 128-column group: 256-column tiles, whatever the cost model prefers.
+        pl.bn = 256;
+        pl.tiles = ((a.M + BM - 1) / BM) * ((a.N + 255) / 256);
+        pl.grid = static_cast<int>(std::min<int64_t>(pl.tiles, dev.num_sms));
+    }
+    p.bias = a.bias;
+    p.yq = a.yq;
+    p.ldyq = a.ldyq;
+    p.sy = a.sy;
+    p.ldsy = a.ldsy;
     p.MT = static_cast<int>((a.M + BM - 1) / BM);
     p.NT = static_cast<int>((a.N + pl.bn - 1) / pl.bn);
     p.splits = pl.splits;

@@ -76,6 +76,13 @@ struct GemmArgs {
     // dense split-K scratch
     void* workspace;
     size_t ws_bytes;
+    // fused epilogue (dense only; no split-K): bias bf16 [N] or nullptr; yq
+    // e4m3 [M, ldyq] + sy fp32 [M, ldsy] or nullptr (then N % 128 == 0)
+    const uint16_t* bias = nullptr;
+    uint8_t* yq = nullptr;
+    int64_t ldyq = 0;
+    float* sy = nullptr;
+    int64_t ldsy = 0;
 };
 
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);

@@ -32,6 +32,7 @@ _SIGS = {
     "fp8bs_weight_quant": (_ST, [_P, _I64, _I64, _P, _P, _P]),
     "fp8bs_weight_dequant": (_ST, [_P, _P, _I64, _I64, _P, _P]),
     "fp8bs_gemm": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P]),
+    "fp8bs_gemm_fused": (_ST, [_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
     "fp8bs_gemm_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fp8bs_gemm_noalloc": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm": (_ST, [_P, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
@@ -176,6 +177,36 @@ def fp8bs_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.T
                           _bf16_ptr(y, "y"), _rows_stride(y, "y"), ws_ptr, ws_bytes, _stream(stream)),
            "fp8bs_gemm")
     return y
+
+
+def fp8bs_gemm_fused(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
+                     bias: Optional[torch.Tensor] = None, want_y: bool = True, want_fp8: bool = False,
+                     y: Optional[torch.Tensor] = None, yq: Optional[torch.Tensor] = None,
+                     sy: Optional[torch.Tensor] = None, stream=None):
+    """fp8_gemm with the fused epilogue: returns (y, yq, sy), y [M, N] bf16 =
+    gemm + bias (None unless want_y), and (yq [M, N] uint8 e4m3, sy [M, N/128]
+    fp32) = y quantised per row per 128 columns (None unless want_fp8)."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    if bias is not None and (bias.dim() != 1 or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous 1-D tensor of N elements")
+    if want_y and y is None:
+        y = _out_rows(M, N, xq.device)
+    if want_fp8:
+        if yq is None:
+            yq = torch.empty((M, (N + 15) // 16 * 16), dtype=torch.uint8, device=xq.device)[:, :N]
+        if sy is None:
+            sy = torch.empty((M, max(4, (N // 128 + 3) // 4 * 4)), dtype=torch.float32, device=xq.device)
+    _check(lib.fp8bs_gemm_fused(_dev(xq, torch.uint8, "xq"), _dev(sx, torch.float32, "sx"), _rows_stride(sx, "sx"),
+                                _dev(wq, torch.uint8, "wq"), _dev(sw, torch.float32, "sw"),
+                                None if bias is None else _bf16_ptr(bias, "bias"), M, N, K,
+                                None if y is None else _bf16_ptr(y, "y"), 0 if y is None else _rows_stride(y, "y"),
+                                None if yq is None else _dev(yq, torch.uint8, "yq"),
+                                0 if yq is None else _rows_stride(yq, "yq"),
+                                None if sy is None else _dev(sy, torch.float32, "sy"),
+                                0 if sy is None else _rows_stride(sy, "sy"), _stream(stream)),
+           "fp8bs_gemm_fused")
+    return y, yq, (None if sy is None else sy[:, :N // 128])
 
 
 def fp8bs_gemm_noalloc(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,

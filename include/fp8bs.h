@@ -113,6 +113,27 @@ fp8bs_status fp8bs_gemm(const uint8_t* xq, const float* sx, int64_t lds,
  * on the current device (0 when no split is used). */
 size_t fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
+/* fp8_gemm with a fused epilogue: the bias add of the pages' linear()
+ * ("DeepSeek-V3" repository overview, "FP8 混合精度训练": y += bias after
+ * fp8_gemm) and the re-quantisation of the result back to FP8 that the same
+ * section describes ("结果再量化回 FP8").  The pages' code returns a bf16 y;
+ * this call produces either or both forms in one pass.
+ *   y[m,n]  = bf16_rne( fp8_gemm sum (as fp8bs_gemm) + bias[n] ), the bias
+ *             (bf16 [N], may be NULL) added in fp32 before the rounding.
+ *   yq, sy  = the bf16 y quantised exactly as fp8bs_act_quant quantises an
+ *             input: per row and per group of 128 columns, s = amax/448,
+ *             code = e4m3(y / s) -- ready to feed the next fp8 GEMM.
+ * y (ldy >= N, ldy % 8 == 0, 16-byte aligned) may be NULL when yq is given;
+ * yq [M, ldyq] (ldyq >= N, ldyq % 16 == 0) and sy [M, ldsy] (ldsy >= N/128,
+ * ldsy % 4 == 0), both 16-byte aligned, may be NULL (both) when y is given.
+ * At least one of y and yq is required (FP8BS_ERR_INVALID_ARG otherwise).
+ * yq requires N % 128 == 0 (FP8BS_ERR_UNSUPPORTED otherwise) and runs with
+ * 256-column tiles.  This call never splits K, so it needs no workspace.
+ * Operand rules and errors otherwise as fp8bs_gemm. */
+fp8bs_status fp8bs_gemm_fused(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* wq, const float* sw,
+                              const uint16_t* bias, int64_t M, int64_t N, int64_t K, uint16_t* y, int64_t ldy,
+                              uint8_t* yq, int64_t ldyq, float* sy, int64_t ldsy, fp8bs_stream_t stream);
+
 /* grouped fp8_gemm for MoE experts (256 routed experts, top-8 -- "MoE 架构详解"):
  * for each expert g, rows offsets[g] .. offsets[g+1]-1 of xq/sx/y are
  * multiplied by expert g's weight, exactly as fp8bs_gemm.

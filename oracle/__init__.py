@@ -43,6 +43,7 @@ def load(mutant: int = 0) -> ctypes.CDLL:
             "orc_weight_quant": [_P, _I64, _I64, _P, _P],
             "orc_weight_dequant": [_P, _P, _I64, _I64, _P],
             "orc_gemm_rows": [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P],
+            "orc_add_bias_rows": [_P, _I64, _I64, _P],
             "orc_grouped_gemm_rows": [_P, _I64, _P, _I64, _P, _P, _P, ctypes.c_int32,
                                       _I64, _I64, _P, _I64, _P, _P],
         }.items():
@@ -120,8 +121,9 @@ class Oracle:
         return w
 
     # -- gemm --------------------------------------------------------------
-    def gemm(self, xq, sx, wq, sw, rows=None):
-        """Returns (y_ref fp64 [len(rows), N], L fp64 [len(rows), N])."""
+    def gemm(self, xq, sx, wq, sw, rows=None, bias=None):
+        """Returns (y_ref fp64 [len(rows), N], L fp64 [len(rows), N]); with
+        bias (bf16 bits [N]) y_ref includes y += bias."""
         xq = np.ascontiguousarray(xq, dtype=np.uint8)
         sx = np.ascontiguousarray(sx, dtype=np.float32)
         wq = np.ascontiguousarray(wq, dtype=np.uint8)
@@ -135,6 +137,10 @@ class Oracle:
         L = np.zeros((rows.size, N), dtype=np.float64)
         self.lib.orc_gemm_rows(_ptr(xq), K, _ptr(sx), sx.shape[1], _ptr(wq), _ptr(sw),
                                N, K, _ptr(rows), rows.size, _ptr(y), _ptr(L))
+        if bias is not None:
+            b = np.ascontiguousarray(bias, dtype=np.uint16)
+            assert b.shape == (N,)
+            self.lib.orc_add_bias_rows(_ptr(y), rows.size, N, _ptr(b))
         return y, L
 
     def grouped_gemm(self, xq, sx, wq, sw, offsets, rows=None):

@@ -306,6 +306,19 @@ void orc_gemm_rows(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds,
     free(xd);
 }
 
+/* bias: the pages' linear() adds the bias after fp8_gemm ("DeepSeek-V3"
+ * repository overview, section "FP8 混合精度训练", the linear() excerpt:
+ * y += bias).  y[r][n] += bf16 value of bias[n], in fp64. */
+void orc_add_bias_rows(double* y, int64_t nrows, int64_t N, const uint16_t* bias) {
+    for (int64_t r = 0; r < nrows; r++)
+        for (int64_t n = 0; n < N; n++)
+#if ORC_MUTANT == 6
+            y[r * N + n] -= (double)orc_bf16_to_f32(bias[n]); /* mutant: bias subtracted */
+#else
+            y[r * N + n] += (double)orc_bf16_to_f32(bias[n]);
+#endif
+}
+
 /* grouped_gemm: the same product per expert g over token rows
  * offsets[g] .. offsets[g+1]-1 of xq/sx, with expert weights
  * wq + g*N*K (row-major [N, K]) and scales sw + g*ceil(N/128)*(K/128).

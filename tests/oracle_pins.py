@@ -399,6 +399,25 @@ def pin_grouped(o):
     assert abs(Fraction(float(y[m, n])) - ex) <= Fraction(2) ** -45 * Fraction(float(L[m, n]))
 
 
+def pin_gemm_bias(o):
+    """linear()'s bias: with an all-zero weight the output is the bias
+    exactly; otherwise adding the bias changes each output by the bias's bf16
+    value (fp64, up to one rounding of the sum)."""
+    rng = np.random.default_rng(22)
+    case = synth.tiny(0)
+    N = case.w.shape[0]
+    bias = synth.normal_bf16(rng, (N,), 1.0)
+    bias_f = f32_of_bf16(bias).astype(np.float64)
+    xq, sx = o.act_quant(case.x)
+    wq0, sw0 = o.weight_quant(np.zeros_like(case.w))
+    y0, _ = o.gemm(xq, sx, wq0, sw0, bias=bias)
+    assert np.array_equal(y0, np.broadcast_to(bias_f, y0.shape))
+    wq, sw = o.weight_quant(case.w)
+    y, _ = o.gemm(xq, sx, wq, sw)
+    yb, _ = o.gemm(xq, sx, wq, sw, bias=bias)
+    assert np.all(np.abs((yb - y) - bias_f) <= 2.0 ** -52 * (np.abs(y) + np.abs(bias_f)))
+
+
 ALL_PINS = [
     pin_codec_midpoints,
     pin_act_quant_rank1,
@@ -413,4 +432,5 @@ ALL_PINS = [
     pin_gemm_diag,
     pin_gemm_vs_dequant_matmul,
     pin_grouped,
+    pin_gemm_bias,
 ]

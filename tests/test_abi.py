@@ -68,6 +68,25 @@ def test_gemm_validation():
     assert g(A, A, 4, A, A, 1 << 31, 8, 128, A, 8, None, 0, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
 
 
+def test_gemm_fused_validation():
+    f = lib.fp8bs_gemm_fused
+    ok = fp8bs.FP8BS_OK
+    # (xq, sx, lds, wq, sw, bias, M, N, K, y, ldy, yq, ldyq, sy, ldsy, stream)
+    assert f(A, A, 4, A, A, None, 0, 256, 128, A, 256, None, 0, None, 0, None) == ok  # M == 0: no-op
+    assert f(A, A, 4, A, A, None, 4, 256, 128, None, 0, None, 0, None, 0, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert f(A, A, 4, A, A, None, 4, 256, 100, A, 256, None, 0, None, 0, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    # yq needs whole 128-column groups, an sy, and 16-byte rows
+    assert f(A, A, 4, A, A, None, 4, 200, 128, None, 0, A, 208, A, 4, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    assert f(A, A, 4, A, A, None, 4, 256, 128, None, 0, A, 256, None, 4, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert f(A, A, 4, A, A, None, 4, 256, 128, None, 0, A, 200, A, 4, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert f(A, A, 4, A, A, None, 4, 256, 128, None, 0, A, 264, A, 4, None) == fp8bs.FP8BS_ERR_MISALIGNED
+    assert f(A, A, 4, A, A, None, 4, 256, 128, None, 0, A, 256, A, 1, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert f(A, A, 4, A, A, None, 4, 256, 128, None, 0, A, 256, A + 4, 4, None) == fp8bs.FP8BS_ERR_MISALIGNED
+    # y rules as fp8bs_gemm; the bias needs 2-byte alignment only
+    assert f(A, A, 4, A, A, None, 4, 256, 128, A, 260, None, 0, None, 0, None) == fp8bs.FP8BS_ERR_MISALIGNED
+    assert f(A, A, 4, A, A, A + 1, 4, 256, 128, A, 256, None, 0, None, 0, None) == fp8bs.FP8BS_ERR_MISALIGNED
+
+
 def test_grouped_validation():
     gg = lib.fp8bs_grouped_gemm
     assert gg(A, A, 4, A, A, None, 4, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG

@@ -5,6 +5,7 @@
   3 ties rounded away from zero in the encoder
   4 weight-scale grid read transposed
   5 last K chunk dropped from the GEMM
+  6 bias subtracted instead of added
 """
 import pytest
 
@@ -12,7 +13,7 @@ from oracle import Oracle
 from oracle_pins import ALL_PINS
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6])
 def test_mutant_is_caught(mutant):
     o = Oracle(mutant)
     assert o.lib.orc_mutant_id() == mutant
