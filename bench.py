@@ -674,11 +674,36 @@ def run_reference(args, rank, local, world):
         cfg = {"workload": "moe_grouped"}
     else:
         case = make_case(args.workload)
-        M = case.x.shape[0]
-        rows = oracle_rows_for(orc, case, budget / (K + W))
-        step = lambda i: oracle_sample_step(orc, case, (np.arange(rows) + i * rows) % M)  # noqa: E731
-        sample = (f"{rows} of {M} rows per step: weight_quant(W) + act_quant(rows) + gemm(rows) + "
-                  f"weight_dequant(W)")
+        M, N, Kd = case.x.shape[0], case.w.shape[0], case.x.shape[1]
+        nblk = (N + 127) // 128
+        # set-up, untimed: the quantised weight the sampled GEMM rows use
+        wq_all, sw_all = orc.weight_quant(case.w)
+
+        def step(i, rows):
+            # one 128-row weight block quantised and dequantised (rotating),
+            # act_quant + gemm of `rows` activation rows against the whole W
+            b = i % nblk
+            wq_b, sw_b = orc.weight_quant(case.w[128 * b:128 * (b + 1)])
+            orc.weight_dequant(wq_b, sw_b)
+            rs = (np.arange(rows) + i * rows) % M
+            xq, sx = orc.act_quant(case.x[rs])
+            orc.gemm(xq, sx, wq_all, sw_all)
+            return 2.0 * rows * N * Kd
+
+        # size the step so that K + W steps take about `budget` seconds
+        t0 = time.perf_counter()
+        step(0, 1)
+        t1 = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        step(0, 5)
+        t5 = time.perf_counter() - t0
+        per_row = max((t5 - t1) / 4, 1e-4)
+        fixed = max(t1 - per_row, 0.0)
+        rows = int(max(1, min(M, (budget / (K + W) - fixed) / per_row)))
+        step_fn = step
+        step = lambda i: step_fn(i, rows)  # noqa: E731
+        sample = (f"{rows} of {M} rows per step: weight_quant + weight_dequant of one 128-row block of W "
+                  f"(rotating), act_quant(rows), gemm(rows) against the whole quantised W")
         M_, N_, K_ = case.shape
         cfg = {"workload": case.name, "M": M_, "N": N_, "K": K_}
     for i in range(W):

@@ -487,13 +487,14 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
         // ------------------------------------------------------------ promotion + epilogue
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R::kRegsPromo));
         constexpr int COLS = BN / nwg_for(BN);  // columns per warpgroup
-        // A warpgroup holding up to 96 columns loads a whole chunk at once and
-        // releases the TMEM buffer before its FMAs (WHOLE); with 128 columns
-        // it walks 16-column slices, loading slice c+1 during slice c's FMAs.
+        // A warpgroup holding 64 or 80 columns loads its share of a chunk at
+        // once and releases the TMEM buffer before its FMAs (WHOLE); with 128
+        // columns (no room for 128 more registers) it walks 16-column slices,
+        // loading slice c+1 during slice c's FMAs, and releases at the end.
         constexpr bool WHOLE = COLS <= 96;
         constexpr int SW = 16;
         static_assert(COLS % 16 == 0, "promotion columns come in 16-column slices");
-        constexpr int NCH = COLS / SW;      // TMEM slices per chunk
+        constexpr int NCH = COLS / SW;      // 16-column slices (and scale groups) per warpgroup
         constexpr int SP = SW / 2;          // packed pairs per slice
         // A warpgroup's columns (at most 128) touch at most two 128-column
         // weight-scale blocks; each 16-column slice lies inside one of them.
@@ -580,8 +581,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                 if (!warp_wait(tfull_bar(b), bph, ctl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * L::BUF_COLS + col0);
-                // promotion: acc += f * P_kb, slice by slice of 32 columns; the
-                // TMEM load of slice c+1 overlaps the FMAs of slice c
+                // promotion: acc += f * P_kb
                 if constexpr (WHOLE) {
                     uint64_t pr[COLS / 2];
                     tmem_ld_cols_pairs(taddr, pr);

@@ -111,22 +111,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// ---------------------------------------------------------------- cp.async
-
-// 4-byte asynchronous copy global -> shared (L1-allocating).  The copies a
-// thread issues are grouped by cp_async_commit; cp_async_wait<N> returns once
-// at most N of the thread's most recent groups are still pending, after which
-// the thread sees the data (other threads after a __syncwarp/__syncthreads).
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
@@ -208,124 +192,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&r)[64]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr)
-        : "memory");
-}
-
-// Load 32 consecutive fp32 TMEM columns of this warp's 32 lanes as 16
-// packed pairs (column 2j in the low half of p[j]) and wait for them.
-__device__ __forceinline__ void tmem_ld_x32_pairs(uint32_t taddr, uint64_t (&p)[16]) {
-    asm volatile(
-        "{\n\t.reg .b32 t<32>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {t0, t1};\n\t"
-        "mov.b64 %1, {t2, t3};\n\t"
-        "mov.b64 %2, {t4, t5};\n\t"
-        "mov.b64 %3, {t6, t7};\n\t"
-        "mov.b64 %4, {t8, t9};\n\t"
-        "mov.b64 %5, {t10, t11};\n\t"
-        "mov.b64 %6, {t12, t13};\n\t"
-        "mov.b64 %7, {t14, t15};\n\t"
-        "mov.b64 %8, {t16, t17};\n\t"
-        "mov.b64 %9, {t18, t19};\n\t"
-        "mov.b64 %10, {t20, t21};\n\t"
-        "mov.b64 %11, {t22, t23};\n\t"
-        "mov.b64 %12, {t24, t25};\n\t"
-        "mov.b64 %13, {t26, t27};\n\t"
-        "mov.b64 %14, {t28, t29};\n\t"
-        "mov.b64 %15, {t30, t31};\n\t"
-        "}"
-        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
-        : "r"(taddr)
-        : "memory");
-}
-
-// acc[j] += f2 * cur[j] on packed fp32 pairs (fma.rn.f32x2: two IEEE
-// fused multiply-adds) while the next 32 TMEM columns load into nxt; the
-// load is waited for before the block ends, so nxt is complete on return.
-__device__ __forceinline__ void tmem_ld_x32_pairs_fma(uint32_t taddr_next, uint64_t (&nxt)[16], uint64_t (&acc)[16],
-                                                      const uint64_t (&cur)[16], uint64_t f2) {
-    asm volatile(
-        "{\n\t.reg .b32 t<32>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%49];\n\t"
-        "fma.rn.f32x2 %16, %48, %32, %16;\n\t"
-        "fma.rn.f32x2 %17, %48, %33, %17;\n\t"
-        "fma.rn.f32x2 %18, %48, %34, %18;\n\t"
-        "fma.rn.f32x2 %19, %48, %35, %19;\n\t"
-        "fma.rn.f32x2 %20, %48, %36, %20;\n\t"
-        "fma.rn.f32x2 %21, %48, %37, %21;\n\t"
-        "fma.rn.f32x2 %22, %48, %38, %22;\n\t"
-        "fma.rn.f32x2 %23, %48, %39, %23;\n\t"
-        "fma.rn.f32x2 %24, %48, %40, %24;\n\t"
-        "fma.rn.f32x2 %25, %48, %41, %25;\n\t"
-        "fma.rn.f32x2 %26, %48, %42, %26;\n\t"
-        "fma.rn.f32x2 %27, %48, %43, %27;\n\t"
-        "fma.rn.f32x2 %28, %48, %44, %28;\n\t"
-        "fma.rn.f32x2 %29, %48, %45, %29;\n\t"
-        "fma.rn.f32x2 %30, %48, %46, %30;\n\t"
-        "fma.rn.f32x2 %31, %48, %47, %31;\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {t0, t1};\n\t"
-        "mov.b64 %1, {t2, t3};\n\t"
-        "mov.b64 %2, {t4, t5};\n\t"
-        "mov.b64 %3, {t6, t7};\n\t"
-        "mov.b64 %4, {t8, t9};\n\t"
-        "mov.b64 %5, {t10, t11};\n\t"
-        "mov.b64 %6, {t12, t13};\n\t"
-        "mov.b64 %7, {t14, t15};\n\t"
-        "mov.b64 %8, {t16, t17};\n\t"
-        "mov.b64 %9, {t18, t19};\n\t"
-        "mov.b64 %10, {t20, t21};\n\t"
-        "mov.b64 %11, {t22, t23};\n\t"
-        "mov.b64 %12, {t24, t25};\n\t"
-        "mov.b64 %13, {t26, t27};\n\t"
-        "mov.b64 %14, {t28, t29};\n\t"
-        "mov.b64 %15, {t30, t31};\n\t"
-        "}"
-        : "=l"(nxt[0]), "=l"(nxt[1]), "=l"(nxt[2]), "=l"(nxt[3]), "=l"(nxt[4]), "=l"(nxt[5]), "=l"(nxt[6]), "=l"(nxt[7]), "=l"(nxt[8]), "=l"(nxt[9]), "=l"(nxt[10]), "=l"(nxt[11]), "=l"(nxt[12]), "=l"(nxt[13]), "=l"(nxt[14]), "=l"(nxt[15]), "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
-        : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(cur[8]), "l"(cur[9]), "l"(cur[10]), "l"(cur[11]), "l"(cur[12]), "l"(cur[13]), "l"(cur[14]), "l"(cur[15]), "l"(f2), "r"(taddr_next)
-        : "memory");
-}
-
-// acc[j] += f2 * cur[j] on packed fp32 pairs.
-__device__ __forceinline__ void fma_pairs(uint64_t (&acc)[16], const uint64_t (&cur)[16], uint64_t f2) {
-    asm volatile(
-        "fma.rn.f32x2 %0, %32, %16, %0;\n\t"
-        "fma.rn.f32x2 %1, %32, %17, %1;\n\t"
-        "fma.rn.f32x2 %2, %32, %18, %2;\n\t"
-        "fma.rn.f32x2 %3, %32, %19, %3;\n\t"
-        "fma.rn.f32x2 %4, %32, %20, %4;\n\t"
-        "fma.rn.f32x2 %5, %32, %21, %5;\n\t"
-        "fma.rn.f32x2 %6, %32, %22, %6;\n\t"
-        "fma.rn.f32x2 %7, %32, %23, %7;\n\t"
-        "fma.rn.f32x2 %8, %32, %24, %8;\n\t"
-        "fma.rn.f32x2 %9, %32, %25, %9;\n\t"
-        "fma.rn.f32x2 %10, %32, %26, %10;\n\t"
-        "fma.rn.f32x2 %11, %32, %27, %11;\n\t"
-        "fma.rn.f32x2 %12, %32, %28, %12;\n\t"
-        "fma.rn.f32x2 %13, %32, %29, %13;\n\t"
-        "fma.rn.f32x2 %14, %32, %30, %14;\n\t"
-        "fma.rn.f32x2 %15, %32, %31, %15;\n\t"
-        ""
-        : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
-        : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(cur[8]), "l"(cur[9]), "l"(cur[10]), "l"(cur[11]), "l"(cur[12]), "l"(cur[13]), "l"(cur[14]), "l"(cur[15]), "l"(f2));
-}
-
 // Load 16 consecutive fp32 TMEM columns of this warp's 32 lanes as 8
 // packed pairs (column 2j in the low half of p[j]) and wait for them.
 __device__ __forceinline__ void tmem_ld_x16_pairs(uint32_t taddr, uint64_t (&p)[8]) {
@@ -392,44 +258,6 @@ __device__ __forceinline__ void fma_pairs(uint64_t (&acc)[8], const uint64_t (&c
         ""
         : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7])
         : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(f2));
-}
-
-// Load 48 consecutive fp32 TMEM columns of this warp's 32 lanes (one
-// wait for all the loads) as 24 packed pairs.
-__device__ __forceinline__ void tmem_ld_cols_pairs(uint32_t taddr, uint64_t (&p)[24]) {
-    asm volatile(
-        "{\n\t.reg .b32 t<48>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%24];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t32,t33,t34,t35,t36,t37,t38,t39,t40,t41,t42,t43,t44,t45,t46,t47}, [%25];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {t0, t1};\n\t"
-        "mov.b64 %1, {t2, t3};\n\t"
-        "mov.b64 %2, {t4, t5};\n\t"
-        "mov.b64 %3, {t6, t7};\n\t"
-        "mov.b64 %4, {t8, t9};\n\t"
-        "mov.b64 %5, {t10, t11};\n\t"
-        "mov.b64 %6, {t12, t13};\n\t"
-        "mov.b64 %7, {t14, t15};\n\t"
-        "mov.b64 %8, {t16, t17};\n\t"
-        "mov.b64 %9, {t18, t19};\n\t"
-        "mov.b64 %10, {t20, t21};\n\t"
-        "mov.b64 %11, {t22, t23};\n\t"
-        "mov.b64 %12, {t24, t25};\n\t"
-        "mov.b64 %13, {t26, t27};\n\t"
-        "mov.b64 %14, {t28, t29};\n\t"
-        "mov.b64 %15, {t30, t31};\n\t"
-        "mov.b64 %16, {t32, t33};\n\t"
-        "mov.b64 %17, {t34, t35};\n\t"
-        "mov.b64 %18, {t36, t37};\n\t"
-        "mov.b64 %19, {t38, t39};\n\t"
-        "mov.b64 %20, {t40, t41};\n\t"
-        "mov.b64 %21, {t42, t43};\n\t"
-        "mov.b64 %22, {t44, t45};\n\t"
-        "mov.b64 %23, {t46, t47};\n\t"
-        "}"
-        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23])
-        : "r"(taddr + 0u), "r"(taddr + 32u)
-        : "memory");
 }
 
 // Load 64 consecutive fp32 TMEM columns of this warp's 32 lanes (one
@@ -529,69 +357,6 @@ __device__ __forceinline__ void tmem_ld_cols_pairs(uint32_t taddr, uint64_t (&p)
         "mov.b64 %39, {t78, t79};\n\t"
         "}"
         : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31]), "=l"(p[32]), "=l"(p[33]), "=l"(p[34]), "=l"(p[35]), "=l"(p[36]), "=l"(p[37]), "=l"(p[38]), "=l"(p[39])
-        : "r"(taddr + 0u), "r"(taddr + 32u), "r"(taddr + 64u)
-        : "memory");
-}
-
-// Load 96 consecutive fp32 TMEM columns of this warp's 32 lanes (one
-// wait for all the loads) as 48 packed pairs.
-__device__ __forceinline__ void tmem_ld_cols_pairs(uint32_t taddr, uint64_t (&p)[48]) {
-    asm volatile(
-        "{\n\t.reg .b32 t<96>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%48];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t32,t33,t34,t35,t36,t37,t38,t39,t40,t41,t42,t43,t44,t45,t46,t47,t48,t49,t50,t51,t52,t53,t54,t55,t56,t57,t58,t59,t60,t61,t62,t63}, [%49];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t64,t65,t66,t67,t68,t69,t70,t71,t72,t73,t74,t75,t76,t77,t78,t79,t80,t81,t82,t83,t84,t85,t86,t87,t88,t89,t90,t91,t92,t93,t94,t95}, [%50];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {t0, t1};\n\t"
-        "mov.b64 %1, {t2, t3};\n\t"
-        "mov.b64 %2, {t4, t5};\n\t"
-        "mov.b64 %3, {t6, t7};\n\t"
-        "mov.b64 %4, {t8, t9};\n\t"
-        "mov.b64 %5, {t10, t11};\n\t"
-        "mov.b64 %6, {t12, t13};\n\t"
-        "mov.b64 %7, {t14, t15};\n\t"
-        "mov.b64 %8, {t16, t17};\n\t"
-        "mov.b64 %9, {t18, t19};\n\t"
-        "mov.b64 %10, {t20, t21};\n\t"
-        "mov.b64 %11, {t22, t23};\n\t"
-        "mov.b64 %12, {t24, t25};\n\t"
-        "mov.b64 %13, {t26, t27};\n\t"
-        "mov.b64 %14, {t28, t29};\n\t"
-        "mov.b64 %15, {t30, t31};\n\t"
-        "mov.b64 %16, {t32, t33};\n\t"
-        "mov.b64 %17, {t34, t35};\n\t"
-        "mov.b64 %18, {t36, t37};\n\t"
-        "mov.b64 %19, {t38, t39};\n\t"
-        "mov.b64 %20, {t40, t41};\n\t"
-        "mov.b64 %21, {t42, t43};\n\t"
-        "mov.b64 %22, {t44, t45};\n\t"
-        "mov.b64 %23, {t46, t47};\n\t"
-        "mov.b64 %24, {t48, t49};\n\t"
-        "mov.b64 %25, {t50, t51};\n\t"
-        "mov.b64 %26, {t52, t53};\n\t"
-        "mov.b64 %27, {t54, t55};\n\t"
-        "mov.b64 %28, {t56, t57};\n\t"
-        "mov.b64 %29, {t58, t59};\n\t"
-        "mov.b64 %30, {t60, t61};\n\t"
-        "mov.b64 %31, {t62, t63};\n\t"
-        "mov.b64 %32, {t64, t65};\n\t"
-        "mov.b64 %33, {t66, t67};\n\t"
-        "mov.b64 %34, {t68, t69};\n\t"
-        "mov.b64 %35, {t70, t71};\n\t"
-        "mov.b64 %36, {t72, t73};\n\t"
-        "mov.b64 %37, {t74, t75};\n\t"
-        "mov.b64 %38, {t76, t77};\n\t"
-        "mov.b64 %39, {t78, t79};\n\t"
-        "mov.b64 %40, {t80, t81};\n\t"
-        "mov.b64 %41, {t82, t83};\n\t"
-        "mov.b64 %42, {t84, t85};\n\t"
-        "mov.b64 %43, {t86, t87};\n\t"
-        "mov.b64 %44, {t88, t89};\n\t"
-        "mov.b64 %45, {t90, t91};\n\t"
-        "mov.b64 %46, {t92, t93};\n\t"
-        "mov.b64 %47, {t94, t95};\n\t"
-        "}"
-        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31]), "=l"(p[32]), "=l"(p[33]), "=l"(p[34]), "=l"(p[35]), "=l"(p[36]), "=l"(p[37]), "=l"(p[38]), "=l"(p[39]), "=l"(p[40]), "=l"(p[41]), "=l"(p[42]), "=l"(p[43]), "=l"(p[44]), "=l"(p[45]), "=l"(p[46]), "=l"(p[47])
         : "r"(taddr + 0u), "r"(taddr + 32u), "r"(taddr + 64u)
         : "memory");
 }
