@@ -661,16 +661,38 @@ def run_reference(args, rank, local, world):
     K, W = args.steps, max(3, args.warmup)
     budget = 150.0  # seconds for the whole run
     if args.workload == "moe":
+        import torch
         case = synth.moe()
         counts = np.diff(case.offsets)
         x_rows = case.x_rows
-        experts = np.nonzero(counts)[0]
+        g = int(np.argmax(counts))  # the busiest expert
+        r0, r1 = int(case.offsets[g]), int(case.offsets[g + 1])
+        wg = synth.expert_weight(case, g, "cpu").view(torch.int16).numpy().view(np.uint16)
+        wq_g, sw_g = orc.weight_quant(wg)  # set-up, untimed
+        nblk = (case.n + 127) // 128
+
+        def moe_step(i, rows):
+            # one 128-row block of the expert's weight quantised (rotating),
+            # act_quant + gemm of `rows` of the expert's token rows
+            b = i % nblk
+            orc.weight_quant(wg[128 * b:128 * (b + 1)])
+            rs = r0 + (np.arange(rows) + i * rows) % (r1 - r0)
+            xq, sx = orc.act_quant(x_rows[rs])
+            orc.gemm(xq, sx, wq_g, sw_g)
+            return 2.0 * rows * case.n * case.k
+
         t0 = time.perf_counter()
-        oracle_moe_step(orc, case, experts[:1], x_rows, 1)
-        one = time.perf_counter() - t0
-        rows = max(1, int(budget / (K + W) / max(one, 1e-3)))
-        step = lambda i: oracle_moe_step(orc, case, [experts[i % len(experts)]], x_rows, rows)  # noqa: E731
-        sample = f"one expert per step (weight_quant, act_quant and gemm of <= {rows} rows)"
+        moe_step(0, 1)
+        t1 = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        moe_step(0, 5)
+        t5 = time.perf_counter() - t0
+        per_row = max((t5 - t1) / 4, 1e-4)
+        fixed = max(t1 - per_row, 0.0)
+        rows = int(max(1, min(r1 - r0, (budget / (K + W) - fixed) / per_row)))
+        step = lambda i: moe_step(i, rows)  # noqa: E731
+        sample = (f"expert {g} ({r1 - r0} rows): per step one 128-row block of its weight quantised, "
+                  f"act_quant + gemm of {rows} of its rows")
         cfg = {"workload": "moe_grouped"}
     else:
         case = make_case(args.workload)

@@ -161,7 +161,7 @@ def expert_weight(case: MoECase, g: int, device: str = "cpu") -> torch.Tensor:
     torch generator seeded with expert_seed0 + g on `device` (on a GPU this is
     torch's Philox stream, so the same seed gives the same bits every run)."""
     gen = torch.Generator(device=device)
-    gen.manual_seed(case.expert_seed0 + g)
+    gen.manual_seed(int(case.expert_seed0) + int(g))
     w = torch.randn((case.n, case.k), generator=gen, device=device, dtype=torch.float32)
     return (w * 0.02).to(torch.bfloat16)
 
