@@ -319,9 +319,11 @@ class DenseWork:
 
 
 class MoEWork:
-    """act_quant over the expert-grouped rows -> grouped fp8_gemm."""
+    """act_quant over the expert-grouped rows -> grouped fp8_gemm.
+    swiglu: the grouped GEMM is the expert first stage with w1 and w3 and the
+    SwiGLU activation fused (h = silu(x w1^T) * (x w3^T))."""
 
-    def __init__(self, device):
+    def __init__(self, device, swiglu=False):
         import torch
         from fp8_block_scaled_18_b300 import fp8bs as F
         from fp8_block_scaled_18_b300 import synth
@@ -338,6 +340,12 @@ class MoEWork:
         self.sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device=device)
         for g in range(G):
             F.fp8bs_weight_quant(synth.expert_weight(case, g, device), wq=self.wq[g], sw=self.sw[g])
+        self.swiglu = swiglu
+        if swiglu:
+            self.w3q = torch.empty((G, N, K), dtype=torch.uint8, device=device)
+            self.sw3 = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device=device)
+            for g in range(G):
+                F.fp8bs_weight_quant(synth.expert_weight(case, g, device, which=1), wq=self.w3q[g], sw=self.sw3[g])
         self.off = torch.from_numpy(case.offsets).to(device)
         lds = (K // 128 + 3) // 4 * 4
         self.xq = torch.empty((self.T, K), dtype=torch.uint8, device=device)
@@ -355,6 +363,15 @@ class MoEWork:
                              1, gbytes, "hbm"),
         }
         self.order = ["act_quant", "grouped_gemm"]
+        if swiglu:
+            self.flops = 4.0 * self.T * N * K
+            gbytes3 = 2.0 * G * N * K + 8.0 * G * (N // 128) * (K // 128) + self.T * K + 4.0 * self.T * (K // 128) \
+                + 2.0 * self.T * N
+            self.kernels["grouped_gemm_swiglu"] = (
+                lambda s: F.fp8bs_grouped_gemm_swiglu(self.xq, self.sx, self.wq, self.sw, self.w3q, self.sw3,
+                                                      self.off, h=self.y), 1, gbytes3, "hbm")
+            del self.kernels["grouped_gemm"]
+            self.order = ["act_quant", "grouped_gemm_swiglu"]
         self.grouped_flops = self.flops
         self.experts_nonempty = int((counts > 0).sum())
 
@@ -380,6 +397,11 @@ class MoEWork:
         self.yp.copy_(self.y, non_blocking=True)
 
     def config(self):
+        if self.swiglu:
+            return {"workload": "moe_swiglu", "tokens": 4096, "experts": self.G, "top_k": 8, "rows": self.T,
+                    "I": self.N, "K": self.K,
+                    "step": "act_quant+grouped w1|w3 fp8_gemm with SwiGLU (expert weights pre-quantised)",
+                    "l2": "working set (7.5 GB of expert weights) larger than the 126 MB L2"}
         return {"workload": "moe_grouped", "tokens": 4096, "experts": self.G, "top_k": 8, "rows": self.T,
                 "N": self.N, "K": self.K, "step": "act_quant+grouped_fp8_gemm (expert weights pre-quantised)",
                 "l2": "working set (3.76 GB of expert weights) larger than the 126 MB L2"}
@@ -389,6 +411,8 @@ def make_work(name: str, device):
     from fp8_block_scaled_18_b300 import synth
     if name == "moe":
         return MoEWork(device)
+    if name == "moe_swiglu":
+        return MoEWork(device, swiglu=True)
     if name == "kv_down":
         return DenseWork(synth.kv_down(), device)
     if name == "tiny":
@@ -569,18 +593,24 @@ def oracle_sample_step(orc, case, rows):
     return 2.0 * len(rows) * case.w.shape[0] * case.x.shape[1]
 
 
-def oracle_moe_step(orc, case, experts, x_rows, rows_per_expert):
+def oracle_moe_step(orc, case, experts, x_rows, rows_per_expert, swiglu=False):
+    """Per expert: weight_quant of its weight(s), act_quant and GEMM of up to
+    rows_per_expert of its rows; with swiglu both w1 and w3 and silu(a) * b."""
     import torch
     from fp8_block_scaled_18_b300 import synth
     flops = 0.0
     for g in experts:
         r0, r1 = int(case.offsets[g]), int(case.offsets[g + 1])
         rows = np.arange(r0, min(r1, r0 + rows_per_expert))
-        wb = synth.expert_weight(case, g, "cpu").view(torch.int16).numpy().view(np.uint16)
-        wq, sw = orc.weight_quant(wb)
         xq, sx = orc.act_quant(x_rows[rows])
-        orc.gemm(xq, sx, wq, sw)
-        flops += 2.0 * len(rows) * case.n * case.k
+        outs = []
+        for which in ((0, 1) if swiglu else (0,)):
+            wb = synth.expert_weight(case, g, "cpu", which=which).view(torch.int16).numpy().view(np.uint16)
+            wq, sw = orc.weight_quant(wb)
+            outs.append(orc.gemm(xq, sx, wq, sw)[0])
+            flops += 2.0 * len(rows) * case.n * case.k
+        if swiglu:
+            orc.swiglu(outs[0], outs[1])
     return flops
 
 
@@ -624,7 +654,8 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
     from fp8_block_scaled_18_b300 import synth
     from oracle import Oracle
     orc = Oracle()
-    if workload == "moe":
+    if workload in ("moe", "moe_swiglu"):
+        swiglu = workload == "moe_swiglu"
         case = synth.moe()
         counts = np.diff(case.offsets)
         x_rows = case.x_rows
@@ -632,10 +663,11 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
         t0 = time.perf_counter()
         flops, n = 0.0, 0
         while time.perf_counter() - t0 < seconds and n < len(experts):
-            flops += oracle_moe_step(orc, case, [experts[n]], x_rows, 32)
+            flops += oracle_moe_step(orc, case, [experts[n]], x_rows, 32, swiglu=swiglu)
             n += 1
         dt = time.perf_counter() - t0
-        sample = f"{n} experts x <=32 rows: weight_quant of the expert, act_quant, gemm"
+        sample = (f"{n} experts x <=32 rows: weight_quant of the expert's "
+                  f"{'w1 and w3' if swiglu else 'weight'}, act_quant, gemm{' x2, silu(a) * b' if swiglu else ''}")
     else:
         case = make_case(workload)
         M = case.x.shape[0]

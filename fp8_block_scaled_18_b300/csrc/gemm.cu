@@ -138,6 +138,7 @@ struct Params {
     // bf16 rounding; yq / sy = the bf16 output quantised per row per 128
     // columns, as act_quant would quantise it
     const uint16_t* bias;    // bf16 [N] or nullptr
+    const float* sw3;        // SwiGLU grouped: w3's weight scales (p.sw holds w1's)
     uint8_t* yq;             // e4m3 [M, ldyq] or nullptr
     int64_t ldyq;
     float* sy;               // fp32 [M, ldsy]
@@ -260,7 +261,13 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, const 
 }
 
 // MODE: how tiles map to work.
-enum : int { kDense = 0, kSplitK = 1, kGrouped = 2 };
+// kGroupedSwiglu: grouped, each tile = 128 columns of w1 (gate) next to the
+// same 128 columns of w3 (up), output h = silu(gate) * up.
+enum : int { kDense = 0, kSplitK = 1, kGrouped = 2, kGroupedSwiglu = 3 };
+__host__ __device__ constexpr bool is_grouped(int mode) { return mode == kGrouped || mode == kGroupedSwiglu; }
+// output columns one tile covers: BN, or 128 h columns for SwiGLU tiles
+template <int BN, int MODE>
+__host__ __device__ constexpr int tile_cols() { return MODE == kGroupedSwiglu ? 128 : BN; }
 
 // Walks the work of one CTA: tiles strided over the grid; for split-K the
 // work unit is (tile, split) and covers the split's range of K chunks.
@@ -270,8 +277,8 @@ struct WorkCursor {
     __device__ __forceinline__ void begin(const Params&) { t = blockIdx.x; }
     __device__ __forceinline__ bool next(const Params& p, const int* prefix, int num_tiles, Tile& tl) {
         if (t >= num_tiles) return false;
-        if (MODE == kGrouped) {
-            tl = grouped_tile<BN>(p, prefix, t);
+        if (is_grouped(MODE)) {
+            tl = grouped_tile<tile_cols<BN, MODE>()>(p, prefix, t);
         } else if (MODE == kSplitK) {
             const int split = t % p.splits;
             tl = dense_tile<BN>(p, t / p.splits);
@@ -286,6 +293,8 @@ struct WorkCursor {
     }
 };
 
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&v);
@@ -294,7 +303,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <int BN, int STAGES, int MODE>
 __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmS, const __grid_constant__ Params p) {
+                    const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmS,
+                    const __grid_constant__ Params p) {
     using L = Layout<BN, STAGES>;
     using R = Roles<nwg_for(BN)>;
     constexpr int kEpiWarps = R::kEpiWarps;
@@ -322,6 +332,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
     if (threadIdx.x == 32) {  // the descriptors are kernel parameters: fetch them while the set-up runs
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (MODE == kGroupedSwiglu) tma_prefetch_desc(&tmB3);
         tma_prefetch_desc(&tmS);
     }
     if (threadIdx.x == 0) {
@@ -347,8 +358,10 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
     grid_dependency_wait();
     allow_dependents();
     if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
-    constexpr bool GROUPED = MODE == kGrouped;
-    if (GROUPED && warp == kEpiWarp0) build_tile_table<BN>(p, prefix, lane);
+    constexpr bool GROUPED = is_grouped(MODE);
+    constexpr bool SWIGLU = MODE == kGroupedSwiglu;
+    static_assert(!SWIGLU || BN == 256, "SwiGLU tiles are 128 gate + 128 up columns");
+    if (GROUPED && warp == kEpiWarp0) build_tile_table<tile_cols<BN, MODE>()>(p, prefix, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -375,7 +388,13 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full_bar(s), L::STAGE_BYTES);
                     tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * BK, tl.m0);
-                    tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * BK, tl.b_row);
+                    if constexpr (SWIGLU) {  // gate rows, then the same rows of w3
+                        tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * BK, tl.b_row);
+                        tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES + 128 * BK, &tmB3, full_bar(s), kb * BK,
+                                    tl.b_row);
+                    } else {
+                        tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * BK, tl.b_row);
+                    }
                 }
                 __syncwarp();
             }
@@ -440,8 +459,15 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
             // weight scale of block fb + bi, chunk c of a scale block; blocks
             // past N and chunks past K are never used and read as 0
             const int bi = lane / kScaleChunks;
-            const bool sw_lane = lane < kSwBlocks * kScaleChunks && fb + bi < nblk;
-            const float* swr = p.sw + static_cast<int64_t>(tl.sw_base + (sw_lane ? fb + bi : 0)) * p.KB;
+            bool sw_lane;
+            const float* swr;
+            if constexpr (SWIGLU) {  // slot rows 0 and 1: the tile's w1 and w3 blocks
+                sw_lane = lane < 2 * kScaleChunks && fb < nblk;
+                swr = (bi == 0 ? p.sw : p.sw3) + static_cast<int64_t>(tl.sw_base + fb) * p.KB;
+            } else {
+                sw_lane = lane < kSwBlocks * kScaleChunks && fb + bi < nblk;
+                swr = p.sw + static_cast<int64_t>(tl.sw_base + (sw_lane ? fb + bi : 0)) * p.KB;
+            }
             auto load_sw = [&](int q) {
                 const int kb = q * kScaleChunks + lane % kScaleChunks;
                 return sw_lane && kb < p.KB ? __ldg(swr + kb) : 0.0f;
@@ -501,13 +527,18 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
         static_assert(COLS <= 128 && 128 % SW == 0, "slice-to-scale-block mapping");
         // Tiles of 256 columns start on a block boundary, so each warpgroup's
         // 128 columns share one weight scale per chunk.
-        constexpr bool ONE_BLOCK = COLS == 128 && BN % 128 == 0;
-        constexpr int NF = ONE_BLOCK ? 1 : NCH;  // distinct scale factors per chunk
+        constexpr bool ONE_BLOCK = COLS == 128 && BN % 128 == 0 && !SWIGLU;
+        // SwiGLU tiles: a warpgroup's 8 slices are 64 gate columns (w1's
+        // scale) then the same 64 columns of up (w3's scale), 128 TMEM
+        // columns apart.
+        constexpr int NF = SWIGLU ? 2 : ONE_BLOCK ? 1 : NCH;  // distinct scale factors per chunk
+        auto fsel = [](int c) { return SWIGLU ? (c >= NCH / 2 ? 1 : 0) : ONE_BLOCK ? 0 : c; };
+        auto slice_col = [](int c) { return SW * c + (SWIGLU && c >= NCH / 2 ? 64 : 0); };
         const int ew = warp - kEpiWarp0;
         const int wg = ew >> 2;
         const int quarter = warp & 3;       // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
-        const int col0 = wg * COLS;
+        const int col0 = SWIGLU ? wg * 64 : wg * COLS;  // first TMEM column of the warpgroup
         const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
         // Scales come from the loader's slots (sfull/sempty per block of
         // kScaleChunks chunks).
@@ -528,12 +559,16 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
             const int n_first = tl.n0 + col0;
             const int n_last = min(n_first + COLS, p.N) - 1;
             const int fb = tl.n0 / 128;
-            const int i0 = n_first < p.N ? n_first / 128 - fb : 0;
-            const int i1 = n_first < p.N ? n_last / 128 - fb : 0;
+            int i0 = n_first < p.N ? n_first / 128 - fb : 0;
+            int i1 = n_first < p.N ? n_last / 128 - fb : 0;
+            if (SWIGLU) {                   // slot rows: 0 = w1's block, 1 = w3's
+                i0 = 0;
+                i1 = 1;
+            }
             uint32_t upper = 0;             // bit c: slice c lies in block i1
 #pragma unroll
             for (int c = 0; c < NCH; ++c)
-                if (n_first < p.N && (n_first + SW * c) / 128 - fb != i0) upper |= 1u << c;
+                if (SWIGLU ? c >= NCH / 2 : (n_first < p.N && (n_first + SW * c) / 128 - fb != i0)) upper |= 1u << c;
             const int nk = tl.kb1 - tl.kb0;
 
             // running sums as packed fp32 pairs: acc[j] = (column 2j, column 2j+1)
@@ -577,7 +612,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                 const uint64_t f2lo = pack_f32x2(f_lo, f_lo), f2hi = pack_f32x2(f_hi, f_hi);
                 uint64_t f2[NF];  // fp32(sx * sw) of each slice, as a packed pair
 #pragma unroll
-                for (int c = 0; c < NF; ++c) f2[c] = ((upper >> c) & 1u) ? f2hi : f2lo;
+                for (int c = 0; c < NF; ++c) f2[c] = SWIGLU ? (c ? f2hi : f2lo) : ((upper >> c) & 1u) ? f2hi : f2lo;
                 if (!warp_wait(tfull_bar(b), bph, ctl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * L::BUF_COLS + col0);
@@ -591,7 +626,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < NCH; ++c)
                         fma_pairs(*reinterpret_cast<uint64_t(*)[SP]>(&acc[SP * c]),
-                                  *reinterpret_cast<uint64_t(*)[SP]>(&pr[SP * c]), f2[ONE_BLOCK ? 0 : c]);
+                                  *reinterpret_cast<uint64_t(*)[SP]>(&pr[SP * c]), f2[fsel(c)]);
                     continue;
                 }
                 uint64_t bufA[SP], bufB[SP];  // slices alternate between two buffers
@@ -601,9 +636,9 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                     uint64_t(&a)[SP] = *reinterpret_cast<uint64_t(*)[SP]>(&acc[SP * c]);
                     uint64_t(&cur)[SP] = (c & 1) ? bufB : bufA;
                     uint64_t(&nxt)[SP] = (c & 1) ? bufA : bufB;
-                    const uint64_t fc = f2[ONE_BLOCK ? 0 : c];
+                    const uint64_t fc = f2[fsel(c)];
                     if (c + 1 < NCH) {
-                        tmem_ld_x16_pairs_fma(taddr + SW * (c + 1), nxt, a, cur, fc);
+                        tmem_ld_x16_pairs_fma(taddr + slice_col(c + 1), nxt, a, cur, fc);
                     } else {
                         fma_pairs(a, cur, fc);
                     }
@@ -615,7 +650,28 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
             if (!ok) break;
             if (!row_ok) continue;
             const int nbase = tl.n0 + col0;
-            if (MODE == kSplitK) {
+            if constexpr (SWIGLU) {
+                // h = silu(gate) * up over the warpgroup's 64 columns, with the
+                // bf16 roundings of the expert forward on bf16 tensors: each
+                // GEMM output, silu (computed in fp32), and the product
+                uint32_t hw[32];
+#pragma unroll
+                for (int v = 0; v < 32; ++v) {
+                    float hv[2];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float g = bf16_round(j ? hi_f32(acc[v]) : lo_f32(acc[v]));
+                        const float u = bf16_round(j ? hi_f32(acc[32 + v]) : lo_f32(acc[32 + v]));
+                        const float sg = bf16_round(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))));
+                        hv[j] = __fmul_rn(sg, u);
+                    }
+                    hw[v] = pack_bf16x2(hv[0], hv[1]);
+                }
+                uint16_t* hr = p.y + static_cast<int64_t>(m) * p.ldy + nbase;
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    *reinterpret_cast<uint4*>(hr + 8 * v) = make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
+            } else if (MODE == kSplitK) {
                 float* pr = p.partial + (static_cast<int64_t>(tl.tile) * p.M + m) * p.N;
 #pragma unroll
                 for (int v = 0; v < COLS / 4; ++v) {
@@ -649,7 +705,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                         }
                     }
                 }
-                if constexpr (COLS == 128 && BN % 128 == 0) {
+                if constexpr (COLS == 128 && BN % 128 == 0 && !SWIGLU) {
                     // The warpgroup's 128 columns are exactly one output group
                     // (the host asks for yq only with N % 128 == 0).
                     if (p.yq != nullptr && nbase < p.N) {
@@ -835,17 +891,23 @@ cudaError_t ensure_kernel_ready(int device) {
 
 template <int BN, int STAGES, int MODE>
 cudaError_t launch_mode(const GemmArgs& a, Params& p, int grid, const DeviceInfo& dev, cudaStream_t stream) {
-    const int64_t b_rows = MODE == kGrouped ? static_cast<int64_t>(a.G) * a.N : a.N;
-    CUtensorMap tmA, tmB, tmS;
+    const int64_t b_rows = is_grouped(MODE) ? static_cast<int64_t>(a.G) * a.N : a.N;
+    CUtensorMap tmA, tmB, tmB3, tmS;
     cudaError_t e;
     if ((e = make_map(&tmA, a.xq, a.K, a.M, a.K, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&tmB, a.wq, a.K, b_rows, a.K, BN)) != cudaSuccess) return e;
+    if constexpr (MODE == kGroupedSwiglu) {  // two boxes of 128 rows per stage, one from each weight
+        if ((e = make_map(&tmB, a.wq, a.K, b_rows, a.K, 128)) != cudaSuccess) return e;
+        if ((e = make_map(&tmB3, a.wq3, a.K, b_rows, a.K, 128)) != cudaSuccess) return e;
+    } else {
+        if ((e = make_map(&tmB, a.wq, a.K, b_rows, a.K, BN)) != cudaSuccess) return e;
+        tmB3 = tmB;  // unused
+    }
     // sx [M, lds] fp32: boxes of kScaleChunks chunks x BM rows
     if ((e = make_tmap_2d(&tmS, a.sx, 4, a.lds, a.M, a.lds * 4, kScaleChunks, BM, false)) != cudaSuccess) return e;
     if ((e = ensure_kernel_ready<BN, STAGES, MODE>(dev.device)) != cudaSuccess) return e;
     return launch_pdl(fp8_gemm_kernel<BN, STAGES, MODE>, dim3(grid), dim3(Roles<nwg_for(BN)>::kThreads),
                       Layout<BN, STAGES>::ALLOC,
-                      stream, tmA, tmB, tmS, p);
+                      stream, tmA, tmB, tmB3, tmS, p);
 }
 
 template <int MODE>
@@ -880,6 +942,10 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
     if (a.offsets != nullptr) {
         p.offsets = a.offsets;
         p.G = a.G;
+        if (a.wq3 != nullptr) {
+            p.sw3 = a.sw3;
+            return launch_mode<256, kStages256, kGroupedSwiglu>(a, p, dev.num_sms, dev, stream);
+        }
         return launch_mode<256, kStages256, kGrouped>(a, p, dev.num_sms, dev, stream);
     }
     const bool fused = a.bias != nullptr || a.yq != nullptr;

@@ -78,6 +78,10 @@ struct GemmArgs {
     size_t ws_bytes;
     // fused epilogue (dense only; no split-K): bias bf16 [N] or nullptr; yq
     // e4m3 [M, ldyq] + sy fp32 [M, ldsy] or nullptr (then N % 128 == 0)
+    // SwiGLU grouped (then y = h [M, ldy], N = the intermediate size): w3's
+    // operand and scales, laid out like wq / sw
+    const uint8_t* wq3 = nullptr;
+    const float* sw3 = nullptr;
     const uint16_t* bias = nullptr;
     uint8_t* yq = nullptr;
     int64_t ldyq = 0;

@@ -36,6 +36,7 @@ _SIGS = {
     "fp8bs_gemm_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fp8bs_gemm_noalloc": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm": (_ST, [_P, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
+    "fp8bs_grouped_gemm_swiglu": (_ST, [_P, _P, _I64, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_sync_status": (_ST, [_P]),
     "fp8bs_status_string": (ctypes.c_char_p, [_ST]),
     "fp8bs_e4m3_encode_f32": (_ST, [_P, _I64, _P, _P]),
@@ -236,6 +237,28 @@ def fp8bs_grouped_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw:
                                   N, K, _bf16_ptr(y, "y"), _rows_stride(y, "y"), _stream(stream)),
            "fp8bs_grouped_gemm")
     return y
+
+
+def fp8bs_grouped_gemm_swiglu(xq: torch.Tensor, sx: torch.Tensor, w1q: torch.Tensor, sw1: torch.Tensor,
+                              w3q: torch.Tensor, sw3: torch.Tensor, offsets: torch.Tensor,
+                              h: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """h [T, I] bf16 = silu(x w1[g]^T) * (x w3[g]^T) per expert (bf16 steps);
+    w1q, w3q: [G, I, K] uint8, sw1, sw3: [G, I/128, K/128] fp32."""
+    T, K = xq.shape
+    G, I = w1q.shape[0], w1q.shape[1]
+    if w3q.shape != w1q.shape or sw3.shape != sw1.shape:
+        raise ValueError("w1 and w3 operands must have the same shapes")
+    if offsets.dtype != torch.int32 or offsets.numel() != G + 1 or not offsets.is_cuda:
+        raise ValueError("offsets must be a CUDA int32 tensor of G + 1 elements")
+    if h is None:
+        h = _out_rows(T, I, xq.device)
+    _check(lib.fp8bs_grouped_gemm_swiglu(_dev(xq, torch.uint8, "xq"), _dev(sx, torch.float32, "sx"),
+                                         _rows_stride(sx, "sx"), _dev(w1q, torch.uint8, "w1q"),
+                                         _dev(sw1, torch.float32, "sw1"), _dev(w3q, torch.uint8, "w3q"),
+                                         _dev(sw3, torch.float32, "sw3"), offsets.data_ptr(), G, T, I, K,
+                                         _bf16_ptr(h, "h"), _rows_stride(h, "h"), _stream(stream)),
+           "fp8bs_grouped_gemm_swiglu")
+    return h
 
 
 def fp8bs_sync_status(stream=None) -> int:

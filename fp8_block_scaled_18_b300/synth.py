@@ -156,12 +156,14 @@ def moe(seed: int = 4, tokens: int = 4096, n_experts: int = N_EXPERTS, n: int = 
     return MoECase(x, flat_t[order], offsets, n_experts, n, k, expert_seed0)
 
 
-def expert_weight(case: MoECase, g: int, device: str = "cpu") -> torch.Tensor:
+def expert_weight(case: MoECase, g: int, device: str = "cpu", which: int = 0) -> torch.Tensor:
     """Expert g's W [N, K] ~N(0,0.02) as a bf16 torch tensor, drawn from a
-    torch generator seeded with expert_seed0 + g on `device` (on a GPU this is
-    torch's Philox stream, so the same seed gives the same bits every run)."""
+    torch generator seeded with expert_seed0 + g (+ 100003 * which, so that
+    which = 1 gives a second, independent weight per expert, e.g. the up
+    projection next to the gate) on `device` (on a GPU this is torch's Philox
+    stream, so the same seed gives the same bits every run)."""
     gen = torch.Generator(device=device)
-    gen.manual_seed(int(case.expert_seed0) + int(g))
+    gen.manual_seed(int(case.expert_seed0) + int(g) + 100003 * int(which))
     w = torch.randn((case.n, case.k), generator=gen, device=device, dtype=torch.float32)
     return (w * 0.02).to(torch.bfloat16)
 

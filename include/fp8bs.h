@@ -173,6 +173,24 @@ fp8bs_status fp8bs_gemm_noalloc(const uint8_t* xq, const float* sx, int64_t lds,
                                 int64_t M, int64_t N, int64_t K,
                                 uint16_t* y, int64_t ldy, fp8bs_stream_t stream);
 
+/* MoE expert first stage with the SwiGLU activation fused (the pages' Expert
+ * forward, "DeepSeek-V3" repository overview, MoE section: w2(silu(w1(x)) *
+ * w3(x)); this call computes the part before w2).  For each expert g and
+ * each of its rows m (offsets_dev as fp8bs_grouped_gemm):
+ *   a = fp8_gemm(xq, sx, w1q[g], sw1[g]),  b = fp8_gemm(xq, sx, w3q[g], sw3[g])
+ *   h[m, i] = bf16( bf16(silu(bf16(a))) * bf16(b) ),  silu(v) = v / (1 + e^-v)
+ * i.e. the bf16 roundings of the expert forward run on bf16 tensors; silu
+ * is evaluated in fp32.  w1q, w3q: e4m3 [G, I, K]; sw1, sw3: fp32
+ * [G, I/128, K/128] (each weight quantised on its own, as fp8bs_weight_quant
+ * does per expert).  h: bf16 [total_M, ldh].  I % 128 == 0 (else
+ * FP8BS_ERR_UNSUPPORTED).  Feed h to fp8bs_act_quant and
+ * fp8bs_grouped_gemm with w2 for the expert's output.  Other operand rules
+ * and errors as fp8bs_grouped_gemm. */
+fp8bs_status fp8bs_grouped_gemm_swiglu(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* w1q,
+                                       const float* sw1, const uint8_t* w3q, const float* sw3,
+                                       const int32_t* offsets_dev, int32_t G, int64_t total_M, int64_t I,
+                                       int64_t K, uint16_t* h, int64_t ldh, fp8bs_stream_t stream);
+
 /* Synchronise `stream`, then report and clear this device's status word:
  * FP8BS_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,
  * FP8BS_ERR_CUDA if the stream reports a CUDA error, else FP8BS_OK. */

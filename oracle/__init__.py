@@ -44,6 +44,7 @@ def load(mutant: int = 0) -> ctypes.CDLL:
             "orc_weight_dequant": [_P, _P, _I64, _I64, _P],
             "orc_gemm_rows": [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P],
             "orc_add_bias_rows": [_P, _I64, _I64, _P],
+            "orc_swiglu": [_P, _P, _I64, _P],
             "orc_grouped_gemm_rows": [_P, _I64, _P, _I64, _P, _P, _P, ctypes.c_int32,
                                       _I64, _I64, _P, _I64, _P, _P],
         }.items():
@@ -143,6 +144,17 @@ class Oracle:
             self.lib.orc_add_bias_rows(_ptr(y), rows.size, N, _ptr(b))
         return y, L
 
+    def swiglu(self, a, b):
+        """h = silu(a) * b, elementwise, fp64."""
+        return _swiglu(self.lib, a, b)
+
+    def grouped_swiglu(self, xq, sx, w1q, sw1, w3q, sw3, offsets, rows=None):
+        """The expert first stage: returns (h, a, b, La, Lb), a and b the
+        grouped GEMMs with w1 and w3, h = silu(a) * b (all fp64)."""
+        a, La = self.grouped_gemm(xq, sx, w1q, sw1, offsets, rows=rows)
+        b, Lb = self.grouped_gemm(xq, sx, w3q, sw3, offsets, rows=rows)
+        return self.swiglu(a, b), a, b, La, Lb
+
     def grouped_gemm(self, xq, sx, wq, sw, offsets, rows=None):
         """wq: [G, N, K] u8, sw: [G, ceil(N/128), K/128], offsets int32 [G+1]."""
         xq = np.ascontiguousarray(xq, dtype=np.uint8)
@@ -160,6 +172,14 @@ class Oracle:
                                        _ptr(offsets), G, N, K, _ptr(rows), rows.size,
                                        _ptr(y), _ptr(L))
         return y, L
+
+
+def _swiglu(lib, a, b):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    h = np.empty_like(a)
+    lib.orc_swiglu(_ptr(a), _ptr(b), a.size, _ptr(h))
+    return h
 
 
 def gemm_tolerance(y_ref: np.ndarray, L: np.ndarray) -> np.ndarray:

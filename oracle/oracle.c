@@ -319,6 +319,20 @@ void orc_add_bias_rows(double* y, int64_t nrows, int64_t N, const uint16_t* bias
 #endif
 }
 
+/* The expert activation between w1/w3 and w2 (the pages' Expert forward,
+ * "DeepSeek-V3" repository overview, MoE section: w2(silu(w1(x)) * w3(x))):
+ * h = silu(a) * b with silu(v) = v / (1 + exp(-v)), in fp64. */
+void orc_swiglu(const double* a, const double* b, int64_t n, double* h) {
+    for (int64_t i = 0; i < n; i++) {
+#if ORC_MUTANT == 7
+        double s = a[i] / (1.0 + exp(a[i])); /* mutant: sign of the exponent flipped */
+#else
+        double s = a[i] / (1.0 + exp(-a[i]));
+#endif
+        h[i] = s * b[i];
+    }
+}
+
 /* grouped_gemm: the same product per expert g over token rows
  * offsets[g] .. offsets[g+1]-1 of xq/sx, with expert weights
  * wq + g*N*K (row-major [N, K]) and scales sw + g*ceil(N/128)*(K/128).

@@ -418,6 +418,21 @@ def pin_gemm_bias(o):
     assert np.all(np.abs((yb - y) - bias_f) <= 2.0 ** -52 * (np.abs(y) + np.abs(bias_f)))
 
 
+def pin_swiglu(o):
+    """The expert activation h = silu(a) * b against scipy's logistic
+    function (silu(v) = v * expit(v)), its zero, its linear tail for large
+    v and its vanishing tail for very negative v."""
+    from scipy.special import expit
+    rng = np.random.default_rng(23)
+    a = np.concatenate([rng.standard_normal(1000) * 4, [0.0, 1.0, -1.0, 20.0, 40.0, -40.0]])
+    b = rng.standard_normal(a.size)
+    h = o.swiglu(a, b)
+    assert np.allclose(h, a * expit(a) * b, rtol=1e-14, atol=1e-300)
+    assert o.swiglu(np.array([0.0]), np.array([3.0]))[0] == 0.0
+    assert abs(o.swiglu(np.array([40.0]), np.array([1.0]))[0] - 40.0) < 1e-12
+    assert abs(o.swiglu(np.array([-40.0]), np.array([1.0]))[0]) < 1e-15
+
+
 ALL_PINS = [
     pin_codec_midpoints,
     pin_act_quant_rank1,
@@ -433,4 +448,5 @@ ALL_PINS = [
     pin_gemm_vs_dequant_matmul,
     pin_grouped,
     pin_gemm_bias,
+    pin_swiglu,
 ]

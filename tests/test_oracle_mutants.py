@@ -6,6 +6,7 @@
   4 weight-scale grid read transposed
   5 last K chunk dropped from the GEMM
   6 bias subtracted instead of added
+  7 silu with the exponent's sign flipped
 """
 import pytest
 
@@ -13,7 +14,7 @@ from oracle import Oracle
 from oracle_pins import ALL_PINS
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7])
 def test_mutant_is_caught(mutant):
     o = Oracle(mutant)
     assert o.lib.orc_mutant_id() == mutant
