@@ -367,9 +367,14 @@ class MoEWork:
             self.flops = 4.0 * self.T * N * K
             gbytes3 = 2.0 * G * N * K + 8.0 * G * (N // 128) * (K // 128) + self.T * K + 4.0 * self.T * (K // 128) \
                 + 2.0 * self.T * N
+            # h leaves as FP8 (1x128 groups): the operand of the w2 GEMM
+            self.hq = torch.empty((self.T, N), dtype=torch.uint8, device=device)
+            self.sh = torch.empty((self.T, max(4, (N // 128 + 3) // 4 * 4)), dtype=torch.float32, device=device)
+            gbytes3 -= self.T * N  # one byte per h element instead of two
             self.kernels["grouped_gemm_swiglu"] = (
                 lambda s: F.fp8bs_grouped_gemm_swiglu(self.xq, self.sx, self.wq, self.sw, self.w3q, self.sw3,
-                                                      self.off, h=self.y), 1, gbytes3, "hbm")
+                                                      self.off, want_h=False, want_fp8=True, hq=self.hq,
+                                                      sh=self.sh), 1, gbytes3, "hbm")
             del self.kernels["grouped_gemm"]
             self.order = ["act_quant", "grouped_gemm_swiglu"]
         self.grouped_flops = self.flops
@@ -386,21 +391,31 @@ class MoEWork:
         import torch
         self.xp = self.x_host.pin_memory()
         self.offp = torch.from_numpy(self.case.offsets).pin_memory()
-        self.yp = torch.empty((self.T, self.N), dtype=torch.bfloat16).pin_memory()
         self.h2d = self.xp.numel() * 2 + self.offp.numel() * 4
-        self.d2h = self.yp.numel() * 2
+        if self.swiglu:  # FP8 h and its scales come back
+            self.yp = torch.empty((self.T, self.N), dtype=torch.uint8).pin_memory()
+            self.shp = torch.empty(self.sh.shape, dtype=torch.float32).pin_memory()
+            self.d2h = self.yp.numel() + self.shp.numel() * 4
+        else:
+            self.yp = torch.empty((self.T, self.N), dtype=torch.bfloat16).pin_memory()
+            self.d2h = self.yp.numel() * 2
 
     def e2e_step(self, i):
         self.x.copy_(self.xp, non_blocking=True)
         self.off.copy_(self.offp, non_blocking=True)
         self.step(i)
-        self.yp.copy_(self.y, non_blocking=True)
+        if self.swiglu:
+            self.yp.copy_(self.hq, non_blocking=True)
+            self.shp.copy_(self.sh, non_blocking=True)
+        else:
+            self.yp.copy_(self.y, non_blocking=True)
 
     def config(self):
         if self.swiglu:
             return {"workload": "moe_swiglu", "tokens": 4096, "experts": self.G, "top_k": 8, "rows": self.T,
                     "I": self.N, "K": self.K,
-                    "step": "act_quant+grouped w1|w3 fp8_gemm with SwiGLU (expert weights pre-quantised)",
+                    "step": "act_quant+grouped w1|w3 fp8_gemm with SwiGLU, h out as FP8 (expert weights "
+                            "pre-quantised)",
                     "l2": "working set (7.5 GB of expert weights) larger than the 126 MB L2"}
         return {"workload": "moe_grouped", "tokens": 4096, "experts": self.G, "top_k": 8, "rows": self.T,
                 "N": self.N, "K": self.K, "step": "act_quant+grouped_fp8_gemm (expert weights pre-quantised)",

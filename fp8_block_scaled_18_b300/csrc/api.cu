@@ -162,22 +162,35 @@ fp8bs_status fp8bs_grouped_gemm(const uint8_t* xq, const float* sx, int64_t lds,
 fp8bs_status fp8bs_grouped_gemm_swiglu(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* w1q,
                                        const float* sw1, const uint8_t* w3q, const float* sw3,
                                        const int32_t* offsets_dev, int32_t G, int64_t total_M, int64_t I,
-                                       int64_t K, uint16_t* h, int64_t ldh, fp8bs_stream_t stream) {
+                                       int64_t K, uint16_t* h, int64_t ldh, uint8_t* hq, int64_t ldhq, float* sh,
+                                       int64_t ldsh, fp8bs_stream_t stream) {
     if (G < 0 || total_M < 0 || I < 0) return FP8BS_ERR_INVALID_ARG;
     if (fp8bs_status st = check_k(K)) return st;
     if (total_M == 0 || I == 0 || G == 0) return FP8BS_OK;
     if (I % 128) return FP8BS_ERR_UNSUPPORTED;  // whole 128-column tiles of h
     if (!offsets_dev || !w3q || !sw3) return FP8BS_ERR_INVALID_ARG;
+    if (!h && !hq) return FP8BS_ERR_INVALID_ARG;  // nothing to write
     if (G > kMaxGroups) return FP8BS_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(G) * I > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
-    if (fp8bs_status st = check_gemm_common(xq, sx, lds, w1q, sw1, total_M, I, K, h, ldh)) return st;
+    // y's rules apply to h when given; check them with a stand-in otherwise
+    if (fp8bs_status st = check_gemm_common(xq, sx, lds, w1q, sw1, total_M, I, K,
+                                            h ? h : reinterpret_cast<uint16_t*>(hq), h ? ldh : I))
+        return st;
     if (!aligned16(w3q) || (reinterpret_cast<uintptr_t>(sw3) & 3u) || (reinterpret_cast<uintptr_t>(offsets_dev) & 3u))
         return FP8BS_ERR_MISALIGNED;
+    if (hq) {
+        if (!sh || ldhq < I || ldsh < I / 128) return FP8BS_ERR_INVALID_ARG;
+        if (!aligned16(hq) || ldhq % 16 || !aligned16(sh) || ldsh % 4) return FP8BS_ERR_MISALIGNED;
+    }
     DeviceInfo d;
     if (fp8bs_status st = device(&d)) return st;
     GemmArgs a{xq, sx, lds, w1q, sw1, total_M, I, K, h, ldh, offsets_dev, G, nullptr, 0};
     a.wq3 = w3q;
     a.sw3 = sw3;
+    a.yq = hq;
+    a.ldyq = ldhq;
+    a.sy = sh;
+    a.ldsy = ldsh;
     return from_cuda(launch_gemm(a, d, cs(stream)));
 }
 

@@ -105,7 +105,8 @@ struct Layout {
     // full[S], empty[S], tfull[NBUF], tempty[NBUF], done[2], sfull[4], sempty[4]
     static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
     // + one drain barrier per issuer + sfull/sempty per scale slot
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + kMmaWarps + 2 * kScaleSlots;
+    // ... + hbar[2] (SwiGLU FP8 output: the two warpgroups' row amaxes, by tile parity)
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + kMmaWarps + 2 * kScaleSlots + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_TABLE = (OFF_ABORT + 4 + 15) & ~15;  // grouped: tile prefix [G+1]
@@ -121,7 +122,10 @@ struct Layout {
     static constexpr int OFF_BIAS = (OFF_SWS + kScaleSlots * SW_SLOT + 15) & ~15;
     static constexpr int BIAS_SLOT = BN * 2;
     static constexpr int BIAS_BYTES = kScaleSlots * BIAS_SLOT;
-    static constexpr int BYTES = OFF_BIAS + BIAS_BYTES;
+    // SwiGLU FP8 output: per tile parity, per warpgroup, the amax of each row's 64 values
+    static constexpr int OFF_HAMAX = OFF_BIAS + BIAS_BYTES;
+    static constexpr int HAMAX_BYTES = 2 * 2 * BM * 4;
+    static constexpr int BYTES = OFF_HAMAX + HAMAX_BYTES;
     static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;                  // allocation: a power of two
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
@@ -326,6 +330,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
     auto done_bar = [&](int w) { return bar0 + 8u * (2 * STAGES + 2 * NBUF + w); };
     auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * NBUF + kMmaWarps + s); };
     auto sempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * NBUF + kMmaWarps + kScaleSlots + s); };
+    auto h_bar = [&](int par) { return bar0 + 8u * (2 * STAGES + 2 * NBUF + kMmaWarps + 2 * kScaleSlots + par); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
     int* prefix = reinterpret_cast<int*>(smem + L::OFF_TABLE);
 
@@ -349,6 +354,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
             mbar_init(sfull_bar(s), 1 + 32);  // the TMA's byte count + one arrival per loader lane
             mbar_init(sempty_bar(s), kEpiWarps);
         }
+        for (int par = 0; par < 2; ++par) mbar_init(h_bar(par), kEpiWarps);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -545,6 +551,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
         const float* sx_slots = reinterpret_cast<const float*>(smem + L::OFF_SX);
         const float* sw_slots = reinterpret_cast<const float*>(smem + L::OFF_SWS);
         uint32_t ss = 0;                    // scale blocks consumed
+        uint32_t h_tiles = 0;               // SwiGLU FP8 output: tiles exchanged (barrier parity, phase)
         uint32_t it = 0;
         bool ok = true;
         WorkCursor<BN, MODE> wc;
@@ -648,7 +655,6 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                 if (lane == 0) mbar_arrive(tempty_bar(b));
             }
             if (!ok) break;
-            if (!row_ok) continue;
             const int nbase = tl.n0 + col0;
             if constexpr (SWIGLU) {
                 // h = silu(gate) * up over the warpgroup's 64 columns, with the
@@ -667,11 +673,52 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                     }
                     hw[v] = pack_bf16x2(hv[0], hv[1]);
                 }
-                uint16_t* hr = p.y + static_cast<int64_t>(m) * p.ldy + nbase;
+                GroupScale gs{};
+                bool zero = true;
+                if (p.yq != nullptr) {
+                    // FP8 h: a row's 128-column group is split between the two
+                    // warpgroups (64 columns each).  Each warp posts its rows'
+                    // amax, arrives once on the tile parity's barrier (all
+                    // lanes take part, before rows past the expert drop out)
+                    // and reads the other warpgroup's after a bounded wait.
+                    uint32_t amax2 = 0;
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    *reinterpret_cast<uint4*>(hr + 8 * v) = make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
-            } else if (MODE == kSplitK) {
+                    for (int i = 0; i < 8; ++i)
+                        amax2 = absmax_bits8(make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]), amax2);
+                    const float amax_own = bits_to_amax(amax2);
+                    const uint32_t par = h_tiles & 1u;
+                    float* hamax = reinterpret_cast<float*>(smem + L::OFF_HAMAX) + par * (2 * BM);
+                    hamax[wg * BM + row] = amax_own;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(h_bar(par));
+                    if (!warp_wait(h_bar(par), (h_tiles >> 1) & 1u, ctl)) { ok = false; break; }
+                    ++h_tiles;
+                    const float amax = fmaxf(amax_own, hamax[(1 - wg) * BM + row]);
+                    gs = group_scale(amax);
+                    zero = amax == 0.0f;
+                }
+                if (!row_ok) continue;
+                if (p.yq != nullptr) {
+                    uint8_t* qr = p.yq + static_cast<int64_t>(m) * p.ldyq + nbase;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint2 c0 = encode8(make_uint4(hw[8 * i], hw[8 * i + 1], hw[8 * i + 2], hw[8 * i + 3]), gs, zero);
+                        const uint2 c1 = encode8(make_uint4(hw[8 * i + 4], hw[8 * i + 5], hw[8 * i + 6], hw[8 * i + 7]), gs, zero);
+                        *reinterpret_cast<uint4*>(qr + 16 * i) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+                    }
+                    if (wg == 0) p.sy[static_cast<int64_t>(m) * p.ldsy + tl.n0 / 128] = gs.s;
+                }
+                if (p.y != nullptr) {
+                    uint16_t* hr = p.y + static_cast<int64_t>(m) * p.ldy + nbase;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        *reinterpret_cast<uint4*>(hr + 8 * v) =
+                            make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
+                }
+                continue;
+            }
+            if (!row_ok) continue;
+            if (MODE == kSplitK) {
                 float* pr = p.partial + (static_cast<int64_t>(tl.tile) * p.M + m) * p.N;
 #pragma unroll
                 for (int v = 0; v < COLS / 4; ++v) {
@@ -944,6 +991,10 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
         p.G = a.G;
         if (a.wq3 != nullptr) {
             p.sw3 = a.sw3;
+            p.yq = a.yq;
+            p.ldyq = a.ldyq;
+            p.sy = a.sy;
+            p.ldsy = a.ldsy;
             return launch_mode<256, kStages256, kGroupedSwiglu>(a, p, dev.num_sms, dev, stream);
         }
         return launch_mode<256, kStages256, kGrouped>(a, p, dev.num_sms, dev, stream);

@@ -36,7 +36,8 @@ _SIGS = {
     "fp8bs_gemm_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fp8bs_gemm_noalloc": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm": (_ST, [_P, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
-    "fp8bs_grouped_gemm_swiglu": (_ST, [_P, _P, _I64, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
+    "fp8bs_grouped_gemm_swiglu": (_ST, [_P, _P, _I64, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P,
+                                        _I64, _P, _I64, _P]),
     "fp8bs_sync_status": (_ST, [_P]),
     "fp8bs_status_string": (ctypes.c_char_p, [_ST]),
     "fp8bs_e4m3_encode_f32": (_ST, [_P, _I64, _P, _P]),
@@ -241,24 +242,38 @@ def fp8bs_grouped_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw:
 
 def fp8bs_grouped_gemm_swiglu(xq: torch.Tensor, sx: torch.Tensor, w1q: torch.Tensor, sw1: torch.Tensor,
                               w3q: torch.Tensor, sw3: torch.Tensor, offsets: torch.Tensor,
-                              h: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                              h: Optional[torch.Tensor] = None, want_h: bool = True, want_fp8: bool = False,
+                              hq: Optional[torch.Tensor] = None, sh: Optional[torch.Tensor] = None, stream=None):
     """h [T, I] bf16 = silu(x w1[g]^T) * (x w3[g]^T) per expert (bf16 steps);
-    w1q, w3q: [G, I, K] uint8, sw1, sw3: [G, I/128, K/128] fp32."""
+    w1q, w3q: [G, I, K] uint8, sw1, sw3: [G, I/128, K/128] fp32.  Returns h
+    (want_h and not want_fp8), else (h or None, hq [T, I] uint8, sh [T, I/128])."""
     T, K = xq.shape
     G, I = w1q.shape[0], w1q.shape[1]
     if w3q.shape != w1q.shape or sw3.shape != sw1.shape:
         raise ValueError("w1 and w3 operands must have the same shapes")
     if offsets.dtype != torch.int32 or offsets.numel() != G + 1 or not offsets.is_cuda:
         raise ValueError("offsets must be a CUDA int32 tensor of G + 1 elements")
-    if h is None:
+    if want_h and h is None:
         h = _out_rows(T, I, xq.device)
+    if want_fp8:
+        if hq is None:
+            hq = torch.empty((T, (I + 15) // 16 * 16), dtype=torch.uint8, device=xq.device)[:, :I]
+        if sh is None:
+            sh = torch.empty((T, max(4, (I // 128 + 3) // 4 * 4)), dtype=torch.float32, device=xq.device)
     _check(lib.fp8bs_grouped_gemm_swiglu(_dev(xq, torch.uint8, "xq"), _dev(sx, torch.float32, "sx"),
                                          _rows_stride(sx, "sx"), _dev(w1q, torch.uint8, "w1q"),
                                          _dev(sw1, torch.float32, "sw1"), _dev(w3q, torch.uint8, "w3q"),
                                          _dev(sw3, torch.float32, "sw3"), offsets.data_ptr(), G, T, I, K,
-                                         _bf16_ptr(h, "h"), _rows_stride(h, "h"), _stream(stream)),
+                                         None if h is None else _bf16_ptr(h, "h"),
+                                         0 if h is None else _rows_stride(h, "h"),
+                                         None if hq is None else _dev(hq, torch.uint8, "hq"),
+                                         0 if hq is None else _rows_stride(hq, "hq"),
+                                         None if sh is None else _dev(sh, torch.float32, "sh"),
+                                         0 if sh is None else _rows_stride(sh, "sh"), _stream(stream)),
            "fp8bs_grouped_gemm_swiglu")
-    return h
+    if not want_fp8:
+        return h
+    return h, hq, sh[:, :I // 128]
 
 
 def fp8bs_sync_status(stream=None) -> int:

@@ -182,14 +182,20 @@ fp8bs_status fp8bs_gemm_noalloc(const uint8_t* xq, const float* sx, int64_t lds,
  * i.e. the bf16 roundings of the expert forward run on bf16 tensors; silu
  * is evaluated in fp32.  w1q, w3q: e4m3 [G, I, K]; sw1, sw3: fp32
  * [G, I/128, K/128] (each weight quantised on its own, as fp8bs_weight_quant
- * does per expert).  h: bf16 [total_M, ldh].  I % 128 == 0 (else
- * FP8BS_ERR_UNSUPPORTED).  Feed h to fp8bs_act_quant and
- * fp8bs_grouped_gemm with w2 for the expert's output.  Other operand rules
- * and errors as fp8bs_grouped_gemm. */
+ * does per expert).  Outputs, at least one of them (FP8BS_ERR_INVALID_ARG
+ * otherwise):
+ *   h  bf16 [total_M, ldh] (ldh >= I, ldh % 8 == 0, 16-byte aligned), or NULL;
+ *   hq e4m3 [total_M, ldhq] and sh fp32 [total_M, ldsh]: h quantised exactly
+ *      as fp8bs_act_quant quantises an input (per row, per 128 columns;
+ *      ldhq >= I, ldhq % 16 == 0; ldsh >= I/128, ldsh % 4 == 0; both 16-byte
+ *      aligned) -- the operand of the w2 GEMM -- or both NULL.
+ * I % 128 == 0 (else FP8BS_ERR_UNSUPPORTED).  Other operand rules and errors
+ * as fp8bs_grouped_gemm. */
 fp8bs_status fp8bs_grouped_gemm_swiglu(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* w1q,
                                        const float* sw1, const uint8_t* w3q, const float* sw3,
                                        const int32_t* offsets_dev, int32_t G, int64_t total_M, int64_t I,
-                                       int64_t K, uint16_t* h, int64_t ldh, fp8bs_stream_t stream);
+                                       int64_t K, uint16_t* h, int64_t ldh, uint8_t* hq, int64_t ldhq, float* sh,
+                                       int64_t ldsh, fp8bs_stream_t stream);
 
 /* Synchronise `stream`, then report and clear this device's status word:
  * FP8BS_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,

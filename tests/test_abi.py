@@ -87,6 +87,25 @@ def test_gemm_fused_validation():
     assert f(A, A, 4, A, A, A + 1, 4, 256, 128, A, 256, None, 0, None, 0, None) == fp8bs.FP8BS_ERR_MISALIGNED
 
 
+def test_grouped_swiglu_validation():
+    f = lib.fp8bs_grouped_gemm_swiglu
+    # (xq, sx, lds, w1q, sw1, w3q, sw3, off, G, T, I, K, h, ldh, hq, ldhq, sh, ldsh, stream)
+    args = [A, A, 4, A, A, A, A, A, 4, 64, 256, 128, A, 256, None, 0, None, 0, None]
+    assert f(*args[:9], 0, *args[10:]) == fp8bs.FP8BS_OK                         # no rows: no-op
+    bad = list(args); bad[10] = 200
+    assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # I % 128
+    bad = list(args); bad[5] = None
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # no w3
+    bad = list(args); bad[12] = None
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # neither h nor hq
+    bad = list(args); bad[14], bad[15], bad[16], bad[17] = A, 256, None, 4
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # hq without sh
+    bad = list(args); bad[14], bad[15], bad[16], bad[17] = A, 264, A, 4
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # ldhq % 16
+    bad = list(args); bad[6] = A + 2
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # sw3 alignment
+
+
 def test_grouped_validation():
     gg = lib.fp8bs_grouped_gemm
     assert gg(A, A, 4, A, A, None, 4, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG

@@ -46,13 +46,18 @@ def _case(orc, counts, I, K, seed):
     return xq, sx, np.stack(w1q), np.stack(sw1), np.stack(w3q), np.stack(sw3), off
 
 
-def _check(orc, h, xq, sx, w1q, sw1, w3q, sw3, off, rows, what):
+def _bound(orc, xq, sx, w1q, sw1, w3q, sw3, off, rows):
     h_ref, a, b, La, Lb = orc.grouped_swiglu(xq, sx, w1q, sw1, w3q, sw3, off, rows=rows)
     ta, tb = gemm_tolerance(a, La), gemm_tolerance(b, Lb)
     s_abs = np.abs(orc.swiglu(a, np.ones_like(a)))
     S = s_abs + 1.1 * ta
     B = np.abs(b) + tb
     bound = (1.1 * ta + (2.0 ** -8 + 2.0 ** -20) * S) * B + s_abs * tb + 2.0 ** -8 * (1 + 2.0 ** -8) * S * B
+    return h_ref, bound
+
+
+def _check(orc, h, xq, sx, w1q, sw1, w3q, sw3, off, rows, what):
+    h_ref, bound = _bound(orc, xq, sx, w1q, sw1, w3q, sw3, off, rows)
     hf = (host(h)[rows].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     bad = np.abs(hf - h_ref) > bound + 1e-30
     assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} outside the bound"
@@ -102,3 +107,31 @@ def test_swiglu_matches_two_grouped_gemms(F, orc):
     # kernel; the bf16 result then differs by at most one bf16 step
     diff = np.abs(hh.astype(np.int32) - hr.astype(np.int32))
     assert diff.max() <= 1 and (diff == 0).mean() > 0.99
+
+
+@pytest.mark.parametrize("counts,I,K", [([3, 0, 130, 1, 40], 256, 384), ([200, 1, 129, 77], 512, 1024)])
+def test_swiglu_fp8_out(F, orc, counts, I, K):
+    """h quantised in the same pass (a row's 128-column group spans both
+    promotion warpgroups): bit-identical to act_quant of the bf16 h, the same
+    without h, and within the bound plus half an e4m3 step of the oracle."""
+    import ml_dtypes
+    xq, sx, w1q, sw1, w3q, sw3, off = _case(orc, counts, I=I, K=K, seed=44 + I)
+    d = [dev(t) for t in (xq, sx, w1q, sw1, w3q, sw3)]
+    offd = torch.from_numpy(off).cuda()
+    h, hq, sh = F.fp8bs_grouped_gemm_swiglu(*d, offd, want_fp8=True)
+    _, hq2, sh2 = F.fp8bs_grouped_gemm_swiglu(*d, offd, want_h=False, want_fp8=True)
+    xq2, sx2 = F.fp8bs_act_quant(h)
+    assert F.fp8bs_sync_status() == 0
+    hq_h, sh_h = host(hq), host(sh)
+    assert np.array_equal(hq_h, host(xq2))
+    assert np.array_equal(sh_h.view(np.uint32), host(sx2)[:, : I // 128].view(np.uint32))
+    assert np.array_equal(host(hq2), hq_h)
+    assert np.array_equal(host(sh2).view(np.uint32), sh_h.view(np.uint32))
+    rows = np.arange(off[-1])
+    h_ref, bound = _bound(orc, xq, sx, w1q, sw1, w3q, sw3, off, rows)
+    v = np.arange(256, dtype=np.uint8).view(ml_dtypes.float8_e4m3fn).astype(np.float64)
+    s = np.repeat(sh_h.astype(np.float64), 128, axis=1)
+    deq = v[hq_h] * s
+    full = bound + np.ldexp(np.abs(h_ref) + bound, -4) * (1 + 2.0 ** -20) + np.ldexp(s, -10) + 1e-30
+    bad = np.abs(deq - h_ref) > full
+    assert not bad.any(), f"{int(bad.sum())} fp8 h outside the bound"
