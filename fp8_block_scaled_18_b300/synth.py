@@ -6,7 +6,7 @@ from here, so they see identical bits.  Shapes follow the "DeepSeek-V3"
 repository overview (pomoai hub): dim 7168, q_lora_rank 1536,
 kv_lora_rank 512 + qk_rope_head_dim 64 (the MLA excerpt's wkv_a output, 576),
 256 routed experts with top-8, 8 expert groups of which 4 are kept, sigmoid
-scoring (config block of "671B 参数如何「激活」37B？").
+scoring, routing weights scaled by 2.5 (config block of "671B 参数如何「激活」37B？").
 
 bf16 tensors are returned as uint16 bit patterns (numpy), rounded from fp32
 by torch's round-to-nearest-even cast.
@@ -25,6 +25,7 @@ N_EXPERTS = 256
 TOP_K = 8
 N_GROUPS = 8
 TOPK_GROUPS = 4
+ROUTE_SCALE = 2.5
 MOE_INTER = 2048
 Q_SWEEP_M = (1, 16, 64, 512, 4096, 16384)
 
@@ -108,6 +109,8 @@ class MoECase:
     n: int
     k: int
     expert_seed0: int
+    weight_of_row: np.ndarray = None   # fp32 [T]: routing weight of each grouped row
+    rows_of_token: np.ndarray = None   # int32 [tokens, top_k]: the grouped rows of each token
 
     @property
     def x_rows(self) -> np.ndarray:
@@ -116,11 +119,14 @@ class MoECase:
 
 
 def route(x_bits: np.ndarray, gate_w_bits: np.ndarray, bias: np.ndarray,
-          n_groups: int = N_GROUPS, topk_groups: int = TOPK_GROUPS, top_k: int = TOP_K):
+          n_groups: int = N_GROUPS, topk_groups: int = TOPK_GROUPS, top_k: int = TOP_K,
+          with_weights: bool = False, route_scale: float = ROUTE_SCALE):
     """Sigmoid-scored, group-limited top-k routing (harness only: it decides
     which rows each expert receives).  The bias steers selection only.  The
     group score is the largest biased score in the group; ties go to the lower
-    index.  Returns expert ids [tokens, top_k]."""
+    index.  Returns expert ids [tokens, top_k]; with_weights also the routing
+    weights: the selected (unbiased) scores normalised to sum 1, times
+    route_scale (fp32 [tokens, top_k])."""
     x = torch.from_numpy(bf16_bits_to_f32(x_bits))
     wg = torch.from_numpy(bf16_bits_to_f32(gate_w_bits))
     scores = torch.sigmoid(x @ wg.T).numpy()                  # fp32 [T, E]
@@ -132,7 +138,12 @@ def route(x_bits: np.ndarray, gate_w_bits: np.ndarray, bias: np.ndarray,
     mask = np.full((T, n_groups), -np.inf, dtype=np.float32)
     np.put_along_axis(mask, gorder, 0.0, axis=1)
     masked = biased + np.repeat(mask, per, axis=1)
-    return np.argsort(-masked, axis=1, kind="stable")[:, :top_k]
+    experts = np.argsort(-masked, axis=1, kind="stable")[:, :top_k]
+    if not with_weights:
+        return experts
+    w = np.take_along_axis(scores, experts, axis=1).astype(np.float32)
+    w = (w / w.sum(axis=1, keepdims=True) * np.float32(route_scale)).astype(np.float32)
+    return experts, w
 
 
 def moe(seed: int = 4, tokens: int = 4096, n_experts: int = N_EXPERTS, n: int = MOE_INTER,
@@ -145,15 +156,19 @@ def moe(seed: int = 4, tokens: int = 4096, n_experts: int = N_EXPERTS, n: int = 
     gw = normal_bf16(rng, (n_experts, k), 0.02)
     bias = rng.uniform(-0.1, 0.1, size=n_experts).astype(np.float32)
     groups = min(N_GROUPS, n_experts)
-    experts = route(x, gw, bias, n_groups=groups, topk_groups=max(1, groups // 2),
-                    top_k=min(TOP_K, n_experts))
+    experts, weights = route(x, gw, bias, n_groups=groups, topk_groups=max(1, groups // 2),
+                             top_k=min(TOP_K, n_experts), with_weights=True)
     flat_e = experts.reshape(-1)
     flat_t = np.repeat(np.arange(tokens, dtype=np.int64), experts.shape[1])
     order = np.argsort(flat_e, kind="stable")
     counts = np.bincount(flat_e, minlength=n_experts)
     offsets = np.zeros(n_experts + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
-    return MoECase(x, flat_t[order], offsets, n_experts, n, k, expert_seed0)
+    row_of_pair = np.empty_like(order)
+    row_of_pair[order] = np.arange(order.size)
+    return MoECase(x, flat_t[order], offsets, n_experts, n, k, expert_seed0,
+                   weights.reshape(-1)[order].astype(np.float32),
+                   row_of_pair.reshape(tokens, experts.shape[1]).astype(np.int32))
 
 
 def expert_weight(case: MoECase, g: int, device: str = "cpu", which: int = 0) -> torch.Tensor:

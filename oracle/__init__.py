@@ -47,6 +47,8 @@ def load(mutant: int = 0) -> ctypes.CDLL:
             "orc_swiglu": [_P, _P, _I64, _P],
             "orc_grouped_gemm_rows": [_P, _I64, _P, _I64, _P, _P, _P, ctypes.c_int32,
                                       _I64, _I64, _P, _I64, _P, _P],
+            "orc_moe_dispatch": [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P],
+            "orc_moe_combine": [_P, _I64, _I64, _P, _P, _I64, ctypes.c_int32, _I64, _P, _I64, _P, _P],
         }.items():
             fn = getattr(lib, name)
             fn.restype = None
@@ -171,6 +173,42 @@ class Oracle:
         self.lib.orc_grouped_gemm_rows(_ptr(xq), K, _ptr(sx), sx.shape[1], _ptr(wq), _ptr(sw),
                                        _ptr(offsets), G, N, K, _ptr(rows), rows.size,
                                        _ptr(y), _ptr(L))
+        return y, L
+
+
+    def moe_dispatch(self, xq, sx, token_of_row):
+        """Gather quantised token rows into routed order: returns
+        (xr [R, K] u8, sr [R, K/128] fp32); rows of out-of-range ids are 0."""
+        xq = np.ascontiguousarray(xq, dtype=np.uint8)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        tor = np.ascontiguousarray(token_of_row, dtype=np.int32)
+        tokens, K = xq.shape
+        R = tor.size
+        xr = np.empty((R, K), dtype=np.uint8)
+        sr = np.empty((R, K // 128), dtype=np.float32)
+        self.lib.orc_moe_dispatch(_ptr(xq), K, _ptr(sx), sx.shape[1], tokens, K, _ptr(tor), R,
+                                  _ptr(xr), _ptr(sr))
+        return xr, sr
+
+    def moe_combine(self, yk, weight_of_row, rows_of_token, z=None):
+        """y [tokens, dim] = z + sum_k w[r_k] yk[r_k] (fp64) and its magnitude
+        sum L; yk [R, dim] (any real dtype, widened to fp64 exactly),
+        weight_of_row fp32 [R], rows_of_token int32 [tokens, topk]."""
+        yk = np.ascontiguousarray(yk, dtype=np.float64)
+        w = np.ascontiguousarray(weight_of_row, dtype=np.float32)
+        rt = np.ascontiguousarray(rows_of_token, dtype=np.int32)
+        R, dim = yk.shape
+        tokens, topk = rt.shape
+        assert w.size == R
+        y = np.empty((tokens, dim), dtype=np.float64)
+        L = np.empty((tokens, dim), dtype=np.float64)
+        zp = None
+        if z is not None:
+            z = np.ascontiguousarray(z, dtype=np.float64)
+            assert z.shape == (tokens, dim)
+            zp = _ptr(z)
+        self.lib.orc_moe_combine(_ptr(yk), dim, R, _ptr(w), _ptr(rt), tokens, topk, dim, zp, dim,
+                                 _ptr(y), _ptr(L))
         return y, L
 
 

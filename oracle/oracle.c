@@ -355,4 +355,63 @@ void orc_grouped_gemm_rows(const uint8_t* xq, int64_t ldq, const float* sx, int6
     }
 }
 
+/* MoE dispatch: the routed expert computation runs on the token rows
+ * gathered expert by expert (page 2 section 2-2: every token keeps its
+ * selected experts, none is dropped, so each of a token's top-k selections
+ * contributes one row).  Row r of the output is the quantised token
+ * token_of_row[r]: its e4m3 codes and its per-128-channel scales, copied
+ * unchanged.  A token id outside [0, tokens) yields an all-zero row.
+ *   xq [tokens, ldq] e4m3, sx [tokens, lds] fp32 -> xr [R, K], sr [R, K/128]. */
+void orc_moe_dispatch(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds, int64_t tokens,
+                      int64_t K, const int32_t* token_of_row, int64_t R, uint8_t* xr, float* sr) {
+    int64_t KB = K / ORC_BLOCK;
+    for (int64_t r = 0; r < R; r++) {
+        int64_t t = token_of_row[r];
+        int ok = t >= 0 && t < tokens;
+        for (int64_t k = 0; k < K; k++) xr[r * K + k] = ok ? xq[t * ldq + k] : 0;
+        for (int64_t kb = 0; kb < KB; kb++)
+#if ORC_MUTANT == 9
+            sr[r * KB + kb] = ok ? sx[(r % tokens) * lds + kb] : 0.0f; /* mutant: scale of the wrong row */
+#else
+            sr[r * KB + kb] = ok ? sx[t * lds + kb] : 0.0f;
+#endif
+    }
+}
+
+/* MoE combine: the layer's output for token t is the sum, over its top-k
+ * selected experts, of each expert's output weighted by the token's gate
+ * value for that expert -- the sigmoid affinity s, not the bias-adjusted
+ * score, which only steers the selection (page 2 section 2-2; sigmoid scoring
+ * and the route_scale factor 2.5 are in the config block of
+ * "671B 参数如何「激活」37B？") -- plus the shared experts' output, which every
+ * token receives (page 3, the shared-expert paragraph on DeepSeekMoE):
+ *   y[t,d] = z[t,d] + sum_{k<topk} w[r_k] * yk[r_k, d],  r_k = rows_of_token[t,k],
+ * in fp64.  L[t,d] = |z[t,d]| + sum_k |w[r_k] yk[r_k,d]| (for error bounds).
+ * yk [R, ldyk] fp64 (the expert outputs, one row per routed pair); w [R] the
+ * gate value of each row; z [tokens, ldz] fp64 or NULL (= 0).  A row id
+ * outside [0, R) contributes nothing. */
+void orc_moe_combine(const double* yk, int64_t ldyk, int64_t R, const float* w, const int32_t* rows_of_token,
+                     int64_t tokens, int32_t topk, int64_t dim, const double* z, int64_t ldz,
+                     double* y, double* L) {
+    for (int64_t t = 0; t < tokens; t++) {
+        for (int64_t d = 0; d < dim; d++) {
+            double acc = z ? z[t * ldz + d] : 0.0;
+            double mag = fabs(acc);
+#if ORC_MUTANT == 8
+            for (int32_t k = 0; k + 1 < topk; k++) { /* mutant: last routed expert dropped */
+#else
+            for (int32_t k = 0; k < topk; k++) {
+#endif
+                int64_t r = rows_of_token[t * topk + k];
+                if (r < 0 || r >= R) continue;
+                double term = (double)w[r] * yk[r * ldyk + d];
+                acc += term;
+                mag += fabs(term);
+            }
+            y[t * dim + d] = acc;
+            L[t * dim + d] = mag;
+        }
+    }
+}
+
 int orc_mutant_id(void) { return ORC_MUTANT; }

@@ -433,6 +433,62 @@ def pin_swiglu(o):
     assert abs(o.swiglu(np.array([-40.0]), np.array([1.0]))[0]) < 1e-15
 
 
+def pin_moe_dispatch(o):
+    """Dispatch is a row gather: each routed row equals its token's codes and
+    scales (numpy fancy indexing), and -- because the quantisation is per
+    token row -- dispatching act_quant(x) equals act_quant of the gathered
+    bf16 rows, bit for bit.  An out-of-range id gives a zero row."""
+    case = synth.moe(seed=5, tokens=48, n_experts=16, n=256, k=384)
+    xq, sx = o.act_quant(case.x_tokens)
+    xr, sr = o.moe_dispatch(xq, sx, case.token_of_row)
+    assert np.array_equal(xr, xq[case.token_of_row])
+    assert np.array_equal(sr.view(np.uint32), sx[case.token_of_row, :3].view(np.uint32))
+    xq2, sx2 = o.act_quant(case.x_rows)
+    assert np.array_equal(xr, xq2) and np.array_equal(sr.view(np.uint32), sx2[:, :3].view(np.uint32))
+    bad = np.array([2, -1, 48, 0], dtype=np.int32)
+    xb, sb = o.moe_dispatch(xq, sx, bad)
+    assert not xb[1:3].any() and not sb[1:3].any()
+    assert np.array_equal(xb[[0, 3]], xq[[2, 0]])
+
+
+def _combine_matrix(rows_of_token, w, R):
+    """The combine as a [tokens, R] scatter matrix S (S[t, r_k] = w[r_k])."""
+    tokens, topk = rows_of_token.shape
+    S = np.zeros((tokens, R))
+    np.add.at(S, (np.repeat(np.arange(tokens), topk), rows_of_token.reshape(-1)),
+              w[rows_of_token.reshape(-1)].astype(np.float64))
+    return S
+
+
+def pin_moe_combine(o):
+    """Combine = S @ Yk + z with the scatter matrix of the routing (numpy
+    matmul, a different formulation of the same sum); with every expert
+    output row equal to one vector c and gates that sum to 2.5 per token
+    (the route_scale), y = 2.5 c + z exactly; with one routed expert of gate 1,
+    y = that expert's row + z exactly."""
+    case = synth.moe(seed=6, tokens=40, n_experts=32, n=256, k=256)
+    R = case.token_of_row.size
+    rng = np.random.default_rng(24)
+    dim = 96
+    yk = f32_of_bf16(synth.normal_bf16(rng, (R, dim), 1.0)).astype(np.float64)
+    z = f32_of_bf16(synth.normal_bf16(rng, (40, dim), 1.0)).astype(np.float64)
+    y, L = o.moe_combine(yk, case.weight_of_row, case.rows_of_token, z=z)
+    ref = _combine_matrix(case.rows_of_token, case.weight_of_row, R) @ yk + z
+    assert np.all(np.abs(y - ref) <= 1e-13 * L)
+    assert np.all(L >= np.abs(y) * (1 - 1e-12))
+    # closed form: gates 1.25, 0.5, 0.5, 0.25 (sum 2.5, exact), rows all c
+    tokens, topk = 6, 4
+    rt = np.arange(tokens * topk, dtype=np.int32).reshape(tokens, topk)[:, ::-1].copy()
+    w = np.tile(np.array([0.25, 0.5, 0.5, 1.25], dtype=np.float32), tokens)
+    c = f32_of_bf16(synth.normal_bf16(rng, (dim,), 1.0)).astype(np.float64)
+    y2, _ = o.moe_combine(np.tile(c, (tokens * topk, 1)), w, rt)
+    assert np.array_equal(y2, np.tile(2.5 * c, (tokens, 1)))
+    # top-1 with gate 1: the expert row itself, plus z
+    rt1 = rng.permutation(R)[:40].astype(np.int32).reshape(40, 1)
+    y3, _ = o.moe_combine(yk, np.ones(R, dtype=np.float32), rt1, z=z)
+    assert np.array_equal(y3, yk[rt1[:, 0]] + z)
+
+
 ALL_PINS = [
     pin_codec_midpoints,
     pin_act_quant_rank1,
@@ -449,4 +505,6 @@ ALL_PINS = [
     pin_grouped,
     pin_gemm_bias,
     pin_swiglu,
+    pin_moe_dispatch,
+    pin_moe_combine,
 ]

@@ -7,6 +7,8 @@
   5 last K chunk dropped from the GEMM
   6 bias subtracted instead of added
   7 silu with the exponent's sign flipped
+  8 MoE combine dropping the last routed expert
+  9 MoE dispatch taking the scales of the wrong row
 """
 import pytest
 
@@ -14,7 +16,7 @@ from oracle import Oracle
 from oracle_pins import ALL_PINS
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_mutant_is_caught(mutant):
     o = Oracle(mutant)
     assert o.lib.orc_mutant_id() == mutant
