@@ -56,7 +56,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="kv_down",
-                    help="kv_down | tiny | q_down_m<M> | large_square | moe")
+                    help="kv_down | tiny | q_down_m<M>[_fused] | large_square | moe | moe_swiglu | moe_layer")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -422,12 +422,139 @@ class MoEWork:
                 "l2": "working set (3.76 GB of expert weights) larger than the 126 MB L2"}
 
 
+class MoELayerWork:
+    """The routed-expert layer end to end on the device, router excluded:
+    act_quant of the tokens, dispatch into expert order, the w1|w3 SwiGLU
+    stage with FP8 h, the w2 grouped GEMM, the shared expert (SwiGLU stage
+    over all tokens, dense w2 GEMM) and the gated combine with the shared
+    output added.  Expert and shared weights are quantised once, before
+    timing; routing (expert ids, gate values) comes from the generator."""
+
+    def __init__(self, device):
+        import torch
+        from fp8_block_scaled_18_b300 import fp8bs as F
+        from fp8_block_scaled_18_b300 import synth
+        self.F = F
+        case = synth.moe()
+        self.case = case
+        G, I, D = case.n_experts, case.n, case.k
+        tokens = case.x_tokens.shape[0]
+        self.G, self.I, self.D, self.tokens = G, I, D, tokens
+        self.T = T = int(case.offsets[-1])
+        self.topk = case.rows_of_token.shape[1]
+        self.x_host = torch.from_numpy(case.x_tokens.view(np.int16)).view(torch.bfloat16)
+        self.x = self.x_host.to(device)
+
+        def quant(which, gs):
+            n, k = (D, I) if which == 2 else (I, D)
+            wq = torch.empty((len(gs), n, k), dtype=torch.uint8, device=device)
+            sw = torch.empty((len(gs), n // 128, k // 128), dtype=torch.float32, device=device)
+            for j, g in enumerate(gs):
+                F.fp8bs_weight_quant(synth.expert_weight(case, g, device, which=which), wq=wq[j], sw=sw[j])
+            return wq, sw
+
+        routed, shared = list(range(G)), [G]
+        self.w1q, self.sw1 = quant(0, routed)
+        self.w3q, self.sw3 = quant(1, routed)
+        self.w2q, self.sw2 = quant(2, routed)
+        self.s1q, self.ss1 = quant(0, shared)
+        self.s3q, self.ss3 = quant(1, shared)
+        s2q, ss2 = quant(2, shared)
+        self.s2q, self.ss2 = s2q[0], ss2[0]
+        self.off = torch.from_numpy(case.offsets).to(device)
+        self.off1 = torch.tensor([0, tokens], dtype=torch.int32, device=device)
+        self.tor = torch.from_numpy(case.token_of_row.astype(np.int32)).to(device)
+        self.rot = torch.from_numpy(case.rows_of_token).to(device)
+        self.wrow = torch.from_numpy(case.weight_of_row).to(device)
+        ldk = (D // 128 + 3) // 4 * 4
+        ldi = max(4, (I // 128 + 3) // 4 * 4)
+        e = lambda *shape, dt=torch.uint8: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+        self.xq, self.sx = e(tokens, D), e(tokens, ldk, dt=torch.float32)
+        self.xr, self.sr = e(T, D), e(T, ldk, dt=torch.float32)
+        self.hq, self.sh = e(T, I), e(T, ldi, dt=torch.float32)
+        self.yk = e(T, D, dt=torch.bfloat16)
+        self.hsq, self.shs = e(tokens, I), e(tokens, ldi, dt=torch.float32)
+        self.z = e(tokens, D, dt=torch.bfloat16)
+        self.y = e(tokens, D, dt=torch.bfloat16)
+        self.R = 1
+        KBd, KBi = D // 128, I // 128
+        wsc = lambda n, k: 4.0 * (n // 128) * (k // 128)  # noqa: E731  (scales of one weight)
+        self.kernels = {
+            "act_quant": (lambda s: F.fp8bs_act_quant(self.x, xq=self.xq, sx=self.sx), 1,
+                          3.0 * tokens * D + 4.0 * tokens * KBd, "hbm"),
+            # reads each token once (its repeats come from L2), writes every routed row
+            "moe_dispatch": (lambda s: F.fp8bs_moe_dispatch(self.xq, self.sx, self.tor, xq_rows=self.xr,
+                                                            sx_rows=self.sr), 1,
+                             tokens * D + 4.0 * tokens * KBd + T * D + 4.0 * T * KBd, "hbm"),
+            "grouped_gemm_swiglu": (
+                lambda s: F.fp8bs_grouped_gemm_swiglu(self.xr, self.sr, self.w1q, self.sw1, self.w3q, self.sw3,
+                                                      self.off, want_h=False, want_fp8=True, hq=self.hq,
+                                                      sh=self.sh), 1,
+                2.0 * G * I * D + 2 * G * wsc(I, D) + T * D + 4.0 * T * KBd + T * I + 4.0 * T * KBi, "hbm"),
+            "grouped_gemm_w2": (
+                lambda s: F.fp8bs_grouped_gemm(self.hq, self.sh, self.w2q, self.sw2, self.off, y=self.yk), 1,
+                1.0 * G * D * I + G * wsc(D, I) + T * I + 4.0 * T * KBi + 2.0 * T * D, "hbm"),
+            "shared_swiglu": (
+                lambda s: F.fp8bs_grouped_gemm_swiglu(self.xq, self.sx, self.s1q, self.ss1, self.s3q, self.ss3,
+                                                      self.off1, want_h=False, want_fp8=True, hq=self.hsq,
+                                                      sh=self.shs), 1, 4.0 * tokens * I * D, "tensor"),
+            "shared_w2": (lambda s: F.fp8bs_gemm(self.hsq, self.shs, self.s2q, self.ss2, y=self.z), 1,
+                          2.0 * tokens * D * I, "tensor"),
+            "moe_combine": (lambda s: F.fp8bs_moe_combine(self.yk, self.wrow, self.rot, z=self.z, y=self.y), 1,
+                            2.0 * T * D + 4.0 * tokens * D + 4.0 * T + 4.0 * tokens * self.topk + 2.0 * tokens * D,
+                            "hbm"),
+        }
+        self.order = ["act_quant", "moe_dispatch", "grouped_gemm_swiglu", "grouped_gemm_w2", "shared_swiglu",
+                      "shared_w2", "moe_combine"]
+        self.flops = T * (4.0 * I * D + 2.0 * D * I) + tokens * (4.0 * I * D + 2.0 * D * I)
+        self.grouped_flops = T * (4.0 * I * D + 2.0 * D * I)
+        self.experts_nonempty = int((np.diff(case.offsets) > 0).sum())
+
+    def step(self, i):
+        for k in self.order:
+            self.kernels[k][0](None)
+
+    def launches_per_step(self):
+        return len(self.order)
+
+    def e2e_setup(self):
+        import torch
+        # per step: the tokens and this batch's routing come in, the layer output goes back
+        self.xp = self.x_host.pin_memory()
+        self.offp = torch.from_numpy(self.case.offsets).pin_memory()
+        self.torp = self.tor.cpu().pin_memory()
+        self.rotp = self.rot.cpu().pin_memory()
+        self.wrowp = self.wrow.cpu().pin_memory()
+        self.yp = torch.empty(self.y.shape, dtype=torch.bfloat16).pin_memory()
+        self.h2d = sum(t.numel() * t.element_size() for t in (self.xp, self.offp, self.torp, self.rotp, self.wrowp))
+        self.d2h = self.yp.numel() * 2
+
+    def e2e_step(self, i):
+        self.x.copy_(self.xp, non_blocking=True)
+        self.off.copy_(self.offp, non_blocking=True)
+        self.tor.copy_(self.torp, non_blocking=True)
+        self.rot.copy_(self.rotp, non_blocking=True)
+        self.wrow.copy_(self.wrowp, non_blocking=True)
+        self.step(i)
+        self.yp.copy_(self.y, non_blocking=True)
+
+    def config(self):
+        return {"workload": "moe_layer", "tokens": self.tokens, "experts": self.G, "top_k": self.topk,
+                "rows": self.T, "dim": self.D, "I": self.I, "shared_experts": 1,
+                "step": "act_quant, dispatch, grouped w1|w3 SwiGLU (FP8 h), grouped w2, shared expert "
+                        "(SwiGLU + dense w2), gated combine (expert and shared weights pre-quantised; "
+                        "routing from the generator)",
+                "l2": "working set (11.3 GB of expert weights) larger than the 126 MB L2"}
+
+
 def make_work(name: str, device):
     from fp8_block_scaled_18_b300 import synth
     if name == "moe":
         return MoEWork(device)
     if name == "moe_swiglu":
         return MoEWork(device, swiglu=True)
+    if name == "moe_layer":
+        return MoELayerWork(device)
     if name == "kv_down":
         return DenseWork(synth.kv_down(), device)
     if name == "tiny":
@@ -629,6 +756,34 @@ def oracle_moe_step(orc, case, experts, x_rows, rows_per_expert, swiglu=False):
     return flops
 
 
+def _expert_weights_q(orc, case, g, whichs):
+    import torch
+    from fp8_block_scaled_18_b300 import synth
+    out = []
+    for which in whichs:
+        wb = synth.expert_weight(case, g, "cpu", which=which).view(torch.int16).numpy().view(np.uint16)
+        out.append(orc.weight_quant(wb))
+    return out
+
+
+def oracle_layer_rows(orc, case, wts, rows):
+    """The routed layer's oracle pass for some of one expert's rows: act_quant
+    of their tokens, the w1 and w3 GEMMs, silu(a) * b, h rounded to bf16 and
+    quantised, the w2 GEMM, and the gated combine of those rows (each taken
+    alone).  wts = the expert's quantised (w1, w3, w2).  Returns flops."""
+    from fp8_block_scaled_18_b300 import synth
+    (w1q, sw1), (w3q, sw3), (w2q, sw2) = wts
+    toks = case.token_of_row[rows]
+    xq, sx = orc.act_quant(case.x_tokens[toks])
+    a, _ = orc.gemm(xq, sx, w1q, sw1)
+    b, _ = orc.gemm(xq, sx, w3q, sw3)
+    h = orc.swiglu(a, b)
+    hq, sh = orc.act_quant(synth.to_bf16_bits(h.astype(np.float32)))
+    yk, _ = orc.gemm(hq, sh, w2q, sw2)
+    orc.moe_combine(yk, case.weight_of_row[rows], np.arange(len(rows), dtype=np.int32).reshape(-1, 1))
+    return len(rows) * (6.0 * case.n * case.k)
+
+
 def make_case(workload: str):
     from fp8_block_scaled_18_b300 import synth
     if workload == "kv_down":
@@ -669,7 +824,22 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
     from fp8_block_scaled_18_b300 import synth
     from oracle import Oracle
     orc = Oracle()
-    if workload in ("moe", "moe_swiglu"):
+    if workload == "moe_layer":
+        case = synth.moe()
+        counts = np.diff(case.offsets)
+        experts = np.nonzero(counts)[0]
+        t0 = time.perf_counter()
+        flops, n = 0.0, 0
+        while time.perf_counter() - t0 < seconds and n < len(experts):
+            g = int(experts[n])
+            wts = _expert_weights_q(orc, case, g, (0, 1, 2))
+            r0, r1 = int(case.offsets[g]), int(case.offsets[g + 1])
+            flops += oracle_layer_rows(orc, case, wts, np.arange(r0, min(r1, r0 + 32)))
+            n += 1
+        dt = time.perf_counter() - t0
+        sample = (f"{n} experts x <=32 rows: weight_quant of the expert's w1, w3 and w2, act_quant, gemm x2, "
+                  f"silu(a) * b, act_quant(h), gemm (w2), gated combine; TFLOP/s over the sampled GEMM work")
+    elif workload in ("moe", "moe_swiglu"):
         swiglu = workload == "moe_swiglu"
         case = synth.moe()
         counts = np.diff(case.offsets)
@@ -707,26 +877,62 @@ def run_reference(args, rank, local, world):
     orc = Oracle()
     K, W = args.steps, max(3, args.warmup)
     budget = 150.0  # seconds for the whole run
-    if args.workload == "moe":
+    if args.workload == "moe_layer":
+        case = synth.moe()
+        counts = np.diff(case.offsets)
+        g = int(np.argmax(counts))  # the busiest expert
+        r0, r1 = int(case.offsets[g]), int(case.offsets[g + 1])
+        wts = _expert_weights_q(orc, case, g, (0, 1, 2))  # set-up, untimed
+        import torch
+        wg = synth.expert_weight(case, g, "cpu").view(torch.int16).numpy().view(np.uint16)
+        nblk = (case.n + 127) // 128
+
+        def layer_step(i, rows):
+            # one 128-row block of the expert's w1 quantised (rotating), then
+            # `rows` of its rows through the layer
+            b = i % nblk
+            orc.weight_quant(wg[128 * b:128 * (b + 1)])
+            rs = r0 + (np.arange(rows) + i * rows) % (r1 - r0)
+            return oracle_layer_rows(orc, case, wts, rs)
+
+        t0 = time.perf_counter()
+        layer_step(0, 1)
+        t1 = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        layer_step(0, 5)
+        t5 = time.perf_counter() - t0
+        per_row = max((t5 - t1) / 4, 1e-4)
+        fixed = max(t1 - per_row, 0.0)
+        rows = int(max(1, min(r1 - r0, (budget / (K + W) - fixed) / per_row)))
+        step = lambda i: layer_step(i, rows)  # noqa: E731
+        sample = (f"expert {g} ({r1 - r0} rows): per step one 128-row block of its w1 quantised, "
+                  f"{rows} of its rows through act_quant, w1/w3 gemm, silu * b, act_quant(h), w2 gemm, combine")
+        cfg = {"workload": "moe_layer"}
+    elif args.workload in ("moe", "moe_swiglu"):
         import torch
         case = synth.moe()
         counts = np.diff(case.offsets)
         x_rows = case.x_rows
         g = int(np.argmax(counts))  # the busiest expert
         r0, r1 = int(case.offsets[g]), int(case.offsets[g + 1])
+        swiglu = args.workload == "moe_swiglu"
         wg = synth.expert_weight(case, g, "cpu").view(torch.int16).numpy().view(np.uint16)
-        wq_g, sw_g = orc.weight_quant(wg)  # set-up, untimed
+        # set-up, untimed: the expert's quantised weight(s)
+        wts = _expert_weights_q(orc, case, g, (0, 1) if swiglu else (0,))
         nblk = (case.n + 127) // 128
 
         def moe_step(i, rows):
             # one 128-row block of the expert's weight quantised (rotating),
-            # act_quant + gemm of `rows` of the expert's token rows
+            # act_quant + gemm of `rows` of the expert's token rows (with
+            # SwiGLU: the w1 and w3 GEMMs and silu(a) * b)
             b = i % nblk
             orc.weight_quant(wg[128 * b:128 * (b + 1)])
             rs = r0 + (np.arange(rows) + i * rows) % (r1 - r0)
             xq, sx = orc.act_quant(x_rows[rs])
-            orc.gemm(xq, sx, wq_g, sw_g)
-            return 2.0 * rows * case.n * case.k
+            outs = [orc.gemm(xq, sx, wq, sw)[0] for wq, sw in wts]
+            if swiglu:
+                orc.swiglu(outs[0], outs[1])
+            return 2.0 * rows * case.n * case.k * len(wts)
 
         t0 = time.perf_counter()
         moe_step(0, 1)
@@ -739,8 +945,8 @@ def run_reference(args, rank, local, world):
         rows = int(max(1, min(r1 - r0, (budget / (K + W) - fixed) / per_row)))
         step = lambda i: moe_step(i, rows)  # noqa: E731
         sample = (f"expert {g} ({r1 - r0} rows): per step one 128-row block of its weight quantised, "
-                  f"act_quant + gemm of {rows} of its rows")
-        cfg = {"workload": "moe_grouped"}
+                  f"act_quant + gemm of {rows} of its rows" + (" against w1 and w3, silu(a) * b" if swiglu else ""))
+        cfg = {"workload": "moe_swiglu" if swiglu else "moe_grouped"}
     else:
         case = make_case(args.workload)
         M, N, Kd = case.x.shape[0], case.w.shape[0], case.x.shape[1]

@@ -194,6 +194,52 @@ fp8bs_status fp8bs_grouped_gemm_swiglu(const uint8_t* xq, const float* sx, int64
     return from_cuda(launch_gemm(a, d, cs(stream)));
 }
 
+fp8bs_status fp8bs_moe_dispatch(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds, int64_t tokens,
+                                int64_t K, const int32_t* token_of_row, int64_t R, uint8_t* xq_rows,
+                                int64_t ldq_rows, float* sx_rows, int64_t lds_rows, fp8bs_stream_t stream) {
+    if (tokens < 0 || R < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (R == 0) return FP8BS_OK;
+    if (tokens == 0) return FP8BS_ERR_INVALID_ARG;  // no id could be in range
+    if (R > kMaxRows || tokens > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
+    if (!xq || !sx || !token_of_row || !xq_rows || !sx_rows) return FP8BS_ERR_INVALID_ARG;
+    if (ldq < K || ldq_rows < K || lds < K / 128 || lds_rows < K / 128) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(xq_rows) || ldq % 16 || ldq_rows % 16 ||
+        (reinterpret_cast<uintptr_t>(sx) & 3u) || (reinterpret_cast<uintptr_t>(sx_rows) & 3u) ||
+        (reinterpret_cast<uintptr_t>(token_of_row) & 3u))
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_moe_dispatch(xq, ldq, sx, lds, tokens, K, token_of_row, R, xq_rows, ldq_rows, sx_rows,
+                                         lds_rows, d, cs(stream)));
+}
+
+fp8bs_status fp8bs_moe_combine(const uint16_t* yk, int64_t ldyk, int64_t R, const float* weight_of_row,
+                               const int32_t* rows_of_token, int64_t tokens, int32_t topk, int64_t dim,
+                               const uint16_t* z, int64_t ldz, uint16_t* y, int64_t ldy, fp8bs_stream_t stream) {
+    if (tokens < 0 || topk < 0 || dim < 0 || R < 0) return FP8BS_ERR_INVALID_ARG;
+    if (tokens == 0 || dim == 0) return FP8BS_OK;
+    if (dim % 8) return FP8BS_ERR_UNSUPPORTED;  // 16-byte chunks of 8 outputs
+    if (!y || ldy < dim) return FP8BS_ERR_INVALID_ARG;
+    if (topk > 0 && (R == 0 || !yk || !weight_of_row || !rows_of_token || ldyk < dim)) return FP8BS_ERR_INVALID_ARG;
+    if (z && ldz < dim) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(y) || ldy % 8) return FP8BS_ERR_MISALIGNED;
+    if (topk > 0 && (!aligned16(yk) || ldyk % 8 || (reinterpret_cast<uintptr_t>(weight_of_row) & 3u) ||
+                     (reinterpret_cast<uintptr_t>(rows_of_token) & 3u)))
+        return FP8BS_ERR_MISALIGNED;
+    if (z && (!aligned16(z) || ldz % 8)) return FP8BS_ERR_MISALIGNED;
+    if (z && !(z == y && ldz == ldy)) {  // z may be y itself, but no other overlap
+        const uintptr_t z0 = reinterpret_cast<uintptr_t>(z), y0 = reinterpret_cast<uintptr_t>(y);
+        const uintptr_t z1 = z0 + 2 * static_cast<uintptr_t>((tokens - 1) * ldz + dim);
+        const uintptr_t y1 = y0 + 2 * static_cast<uintptr_t>((tokens - 1) * ldy + dim);
+        if (z0 < y1 && y0 < z1) return FP8BS_ERR_INVALID_ARG;
+    }
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_moe_combine(yk, ldyk, R, weight_of_row, rows_of_token, tokens, topk, dim, z, ldz, y, ldy,
+                                        d, cs(stream)));
+}
+
 fp8bs_status fp8bs_sync_status(fp8bs_stream_t stream) {
     if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
     DeviceInfo d;
@@ -205,7 +251,7 @@ fp8bs_status fp8bs_sync_status(fp8bs_stream_t stream) {
     if (word == 0) return FP8BS_OK;
     if (cudaMemsetAsync(d.err, 0, sizeof(unsigned), cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
     if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
-    return FP8BS_ERR_TIMEOUT;
+    return (word & kDevErrIndex) && !(word & ~kDevErrIndex) ? FP8BS_ERR_INDEX : FP8BS_ERR_TIMEOUT;
 }
 
 const char* fp8bs_status_string(fp8bs_status status) {
@@ -216,6 +262,7 @@ const char* fp8bs_status_string(fp8bs_status status) {
         case FP8BS_ERR_MISALIGNED: return "FP8BS_ERR_MISALIGNED: pointer or leading dimension not 16-byte aligned";
         case FP8BS_ERR_CUDA: return "FP8BS_ERR_CUDA: CUDA runtime error";
         case FP8BS_ERR_TIMEOUT: return "FP8BS_ERR_TIMEOUT: a kernel's bounded wait expired";
+        case FP8BS_ERR_INDEX: return "FP8BS_ERR_INDEX: a routed row or token id was out of range";
     }
     return "FP8BS: unknown status";
 }

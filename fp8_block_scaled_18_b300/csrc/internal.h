@@ -10,6 +10,11 @@
 
 namespace fp8bs {
 
+// Status-word bit set by the MoE gathers when a routed row or token id lies
+// outside its range (the wait-timeout bits, 1 and 2, are defined with the
+// bounded waits in ptx.cuh).
+constexpr unsigned kDevErrIndex = 4u;
+
 struct DeviceInfo {
     int device;
     int num_sms;
@@ -59,6 +64,15 @@ cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N,
 cudaError_t launch_e4m3_encode(const float* v, int64_t n, uint8_t* q, const DeviceInfo& dev,
                                cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, const DeviceInfo& dev, cudaStream_t stream);
+
+// MoE dispatch and combine (moe.cu).
+cudaError_t launch_moe_dispatch(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds, int64_t tokens,
+                                int64_t K, const int32_t* token_of_row, int64_t R, uint8_t* xr, int64_t ldr,
+                                float* sr, int64_t ldsr, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_moe_combine(const uint16_t* yk, int64_t ldyk, int64_t R, const float* w,
+                               const int32_t* rows_of_token, int64_t tokens, int32_t topk, int64_t dim,
+                               const uint16_t* z, int64_t ldz, uint16_t* y, int64_t ldy, const DeviceInfo& dev,
+                               cudaStream_t stream);
 
 // Dense and grouped GEMM (gemm.cu).
 struct GemmArgs {

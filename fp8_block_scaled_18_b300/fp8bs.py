@@ -38,6 +38,8 @@ _SIGS = {
     "fp8bs_grouped_gemm": (_ST, [_P, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm_swiglu": (_ST, [_P, _P, _I64, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P,
                                         _I64, _P, _I64, _P]),
+    "fp8bs_moe_dispatch": (_ST, [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
+    "fp8bs_moe_combine": (_ST, [_P, _I64, _I64, _P, _P, _I64, _I32, _I64, _P, _I64, _P, _I64, _P]),
     "fp8bs_sync_status": (_ST, [_P]),
     "fp8bs_status_string": (ctypes.c_char_p, [_ST]),
     "fp8bs_e4m3_encode_f32": (_ST, [_P, _I64, _P, _P]),
@@ -55,6 +57,7 @@ FP8BS_ERR_UNSUPPORTED = 2
 FP8BS_ERR_MISALIGNED = 3
 FP8BS_ERR_CUDA = 4
 FP8BS_ERR_TIMEOUT = 5
+FP8BS_ERR_INDEX = 6
 
 
 class Fp8bsError(RuntimeError):
@@ -274,6 +277,53 @@ def fp8bs_grouped_gemm_swiglu(xq: torch.Tensor, sx: torch.Tensor, w1q: torch.Ten
     if not want_fp8:
         return h
     return h, hq, sh[:, :I // 128]
+
+
+def fp8bs_moe_dispatch(xq: torch.Tensor, sx: torch.Tensor, token_of_row: torch.Tensor, K: Optional[int] = None,
+                       xq_rows: Optional[torch.Tensor] = None, sx_rows: Optional[torch.Tensor] = None,
+                       stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Gather quantised token rows into routed order: xq [tokens, K] uint8,
+    sx [tokens, lds] fp32, token_of_row int32 [R] on the device ->
+    (xq_rows [R, K] uint8, sx_rows [R, lds'] fp32)."""
+    tokens = xq.shape[0]
+    K = xq.shape[1] if K is None else K
+    if token_of_row.dtype != torch.int32 or token_of_row.dim() != 1 or not token_of_row.is_contiguous():
+        raise ValueError("token_of_row must be a contiguous 1-D int32 tensor")
+    R = token_of_row.numel()
+    if xq_rows is None:
+        xq_rows = torch.empty((R, (K + 15) // 16 * 16), dtype=torch.uint8, device=xq.device)[:, :K]
+    if sx_rows is None:
+        sx_rows = torch.empty((R, max(4, (K // 128 + 3) // 4 * 4)), dtype=torch.float32, device=xq.device)
+    _check(lib.fp8bs_moe_dispatch(_dev(xq, torch.uint8, "xq"), _rows_stride(xq, "xq"),
+                                  _dev(sx, torch.float32, "sx"), _rows_stride(sx, "sx"), tokens, K,
+                                  _dev(token_of_row, torch.int32, "token_of_row"), R,
+                                  _dev(xq_rows, torch.uint8, "xq_rows"), _rows_stride(xq_rows, "xq_rows"),
+                                  _dev(sx_rows, torch.float32, "sx_rows"), _rows_stride(sx_rows, "sx_rows"),
+                                  _stream(stream)), "fp8bs_moe_dispatch")
+    return xq_rows, sx_rows
+
+
+def fp8bs_moe_combine(yk: torch.Tensor, weight_of_row: torch.Tensor, rows_of_token: torch.Tensor,
+                      z: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """y [tokens, dim] bf16 = z + sum_k weight_of_row[r_k] * yk[r_k] (fp32,
+    k in order), r_k = rows_of_token[t, k]; yk [R, dim] bf16, weight_of_row
+    fp32 [R], rows_of_token int32 [tokens, topk], z bf16 [tokens, dim] or
+    None.  y may be z itself (in-place add)."""
+    R, dim = yk.shape
+    if rows_of_token.dtype != torch.int32 or rows_of_token.dim() != 2 or not rows_of_token.is_contiguous():
+        raise ValueError("rows_of_token must be a contiguous 2-D int32 tensor")
+    if weight_of_row.numel() != R or not weight_of_row.is_contiguous():
+        raise ValueError("weight_of_row must be a contiguous tensor of R elements")
+    tokens, topk = rows_of_token.shape
+    if y is None:
+        y = _out_rows(tokens, dim, yk.device)
+    _check(lib.fp8bs_moe_combine(_bf16_ptr(yk, "yk"), _rows_stride(yk, "yk"), R,
+                                 _dev(weight_of_row, torch.float32, "weight_of_row"),
+                                 _dev(rows_of_token, torch.int32, "rows_of_token"), tokens, topk, dim,
+                                 None if z is None else _bf16_ptr(z, "z"), 0 if z is None else _rows_stride(z, "z"),
+                                 _bf16_ptr(y, "y"), _rows_stride(y, "y"), _stream(stream)), "fp8bs_moe_combine")
+    return y
 
 
 def fp8bs_sync_status(stream=None) -> int:

@@ -176,10 +176,13 @@ def expert_weight(case: MoECase, g: int, device: str = "cpu", which: int = 0) ->
     torch generator seeded with expert_seed0 + g (+ 100003 * which, so that
     which = 1 gives a second, independent weight per expert, e.g. the up
     projection next to the gate) on `device` (on a GPU this is torch's Philox
-    stream, so the same seed gives the same bits every run)."""
+    stream, so the same seed gives the same bits every run).  which = 2 is
+    the down projection w2, [K, N] (model width by intermediate size); the
+    index g = n_experts stands for the shared expert."""
     gen = torch.Generator(device=device)
     gen.manual_seed(int(case.expert_seed0) + int(g) + 100003 * int(which))
-    w = torch.randn((case.n, case.k), generator=gen, device=device, dtype=torch.float32)
+    shape = (case.k, case.n) if which == 2 else (case.n, case.k)
+    w = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
     return (w * 0.02).to(torch.bfloat16)
 
 

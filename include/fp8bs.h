@@ -58,7 +58,8 @@ typedef enum {
     FP8BS_ERR_UNSUPPORTED = 2,  /* K % 128 != 0, size beyond the 32-bit index range, no sm_103 device */
     FP8BS_ERR_MISALIGNED = 3,   /* pointer or leading dimension breaks the 16-byte rule */
     FP8BS_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
-    FP8BS_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (see fp8bs_sync_status) */
+    FP8BS_ERR_TIMEOUT = 5,      /* a kernel's bounded wait expired (see fp8bs_sync_status) */
+    FP8BS_ERR_INDEX = 6         /* a device-side row or token id was out of range (see fp8bs_sync_status) */
 } fp8bs_status;
 
 /* act_quant: per row m and group g of 128 channels (per token, per 128
@@ -197,9 +198,58 @@ fp8bs_status fp8bs_grouped_gemm_swiglu(const uint8_t* xq, const float* sx, int64
                                        int64_t K, uint16_t* h, int64_t ldh, uint8_t* hq, int64_t ldhq, float* sh,
                                        int64_t ldsh, fp8bs_stream_t stream);
 
+/* MoE dispatch: gather the quantised token rows into routed (expert-grouped)
+ * order, the operand layout of fp8bs_grouped_gemm and
+ * fp8bs_grouped_gemm_swiglu.  Every token keeps all of its selected experts
+ * (no token dropping: DeepSeek-V3 notes, page 2 section 2-2), so a token
+ * routed to k experts appears in k rows.  For r < R, t = token_of_row[r]:
+ *   xq_rows[r, 0:K] = xq[t, 0:K]   (e4m3 codes, copied unchanged)
+ *   sx_rows[r, 0:K/128] = sx[t, 0:K/128]   (the per-128-channel scales)
+ * Quantisation is per token row, so the result equals fp8bs_act_quant of the
+ * gathered bf16 rows bit for bit, at 1/k of the quantisation work.
+ *   xq [tokens, ldq] (ldq >= K, ldq % 16 == 0, 16-byte aligned), sx [tokens, lds]
+ *      (lds >= K/128, 4-byte aligned): as fp8bs_act_quant writes them
+ *   token_of_row int32 [R] device (4-byte aligned): source token of each row
+ *   xq_rows [R, ldq_rows] (ldq_rows >= K, ldq_rows % 16 == 0, 16-byte aligned),
+ *   sx_rows [R, lds_rows] (lds_rows >= K/128, 4-byte aligned); scale columns
+ *      >= K/128 untouched.
+ * K % 128 == 0 (else FP8BS_ERR_UNSUPPORTED); tokens == 0 with R > 0 is
+ * FP8BS_ERR_INVALID_ARG.  A token id outside [0, tokens) is not read: that
+ * row is written as zeros (codes and scales) and the next fp8bs_sync_status()
+ * reports FP8BS_ERR_INDEX. */
+fp8bs_status fp8bs_moe_dispatch(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds, int64_t tokens,
+                                int64_t K, const int32_t* token_of_row, int64_t R, uint8_t* xq_rows,
+                                int64_t ldq_rows, float* sx_rows, int64_t lds_rows, fp8bs_stream_t stream);
+
+/* MoE combine: each token's output is its selected experts' outputs weighted
+ * by its gate values -- the sigmoid affinities, not the bias-adjusted scores,
+ * which only steer the selection (DeepSeek-V3 notes, page 2 section 2-2) --
+ * plus an optional dense term z, e.g. the shared experts' output that every
+ * token receives (page 3, the DeepSeekMoE shared-expert paragraph) or the
+ * residual.  For each token t and column d, r_k = rows_of_token[t, k]:
+ *   y[t, d] = bf16_rne( acc ),  acc = z[t, d] (0 if z is NULL), then for
+ *   k = 0 .. topk-1 in that order acc = fma(weight_of_row[r_k], yk[r_k, d], acc)
+ * in fp32 (one rounding per term, one to bf16 at the end).  So
+ *   |y - y_exact| <= 2^-8 |y_exact| + (topk + 1) 2^-24 (|z| + sum_k |w yk|).
+ *   yk bf16 [R, ldyk] (ldyk >= dim, ldyk % 8 == 0, 16-byte aligned): the
+ *      expert outputs in routed order (fp8bs_grouped_gemm's y)
+ *   weight_of_row fp32 [R] (4-byte aligned): the gate value of each routed row
+ *   rows_of_token int32 [tokens, topk] dense (4-byte aligned): the routed rows of each token
+ *   z bf16 [tokens, ldz] (ldz >= dim, ldz % 8 == 0, 16-byte aligned) or NULL;
+ *      z may be y itself (same pointer and ldz == ldy), no other overlap
+ *      (FP8BS_ERR_INVALID_ARG)
+ *   y bf16 [tokens, ldy] (ldy >= dim, ldy % 8 == 0, 16-byte aligned).
+ * dim % 8 == 0 (else FP8BS_ERR_UNSUPPORTED).  topk == 0 gives y = bf16(z) (or
+ * zeros).  A row id outside [0, R) contributes nothing and the next
+ * fp8bs_sync_status() reports FP8BS_ERR_INDEX. */
+fp8bs_status fp8bs_moe_combine(const uint16_t* yk, int64_t ldyk, int64_t R, const float* weight_of_row,
+                               const int32_t* rows_of_token, int64_t tokens, int32_t topk, int64_t dim,
+                               const uint16_t* z, int64_t ldz, uint16_t* y, int64_t ldy, fp8bs_stream_t stream);
+
 /* Synchronise `stream`, then report and clear this device's status word:
  * FP8BS_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,
- * FP8BS_ERR_CUDA if the stream reports a CUDA error, else FP8BS_OK. */
+ * else FP8BS_ERR_INDEX if a MoE gather met an out-of-range id, FP8BS_ERR_CUDA
+ * if the stream reports a CUDA error, else FP8BS_OK. */
 fp8bs_status fp8bs_sync_status(fp8bs_stream_t stream);
 
 /* Static, human-readable name of a status. */

@@ -21,7 +21,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
-    for s in range(6):
+    for s in range(7):
         assert fp8bs.fp8bs_status_string(s).startswith("FP8BS")
     assert fp8bs.fp8bs_status_string(99) == "FP8BS: unknown status"
     assert fp8bs.fp8bs_version() == (0 << 16) | (1 << 8)
@@ -116,6 +116,59 @@ def test_grouped_validation():
     assert gg(A, A, 4, A, A, A, 4, 16, 8, 136, A, 8, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
 
 
+def test_moe_dispatch_validation():
+    f = lib.fp8bs_moe_dispatch
+    # (xq, ldq, sx, lds, tokens, K, token_of_row, R, xq_rows, ldq_rows, sx_rows, lds_rows, stream)
+    args = [A, 256, A, 4, 16, 256, A, 32, A, 256, A, 4, None]
+    ok = fp8bs.FP8BS_OK
+    assert f(*args[:7], 0, *args[8:]) == ok                                       # no rows: no-op
+    bad = list(args); bad[5] = 200
+    assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # K % 128
+    bad = list(args); bad[4] = 0
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # rows but no tokens
+    bad = list(args); bad[6] = None
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # no map
+    bad = list(args); bad[9] = 128
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # ldq_rows < K
+    bad = list(args); bad[11] = 1
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # lds_rows < K/128
+    bad = list(args); bad[1] = 264
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # ldq % 16
+    bad = list(args); bad[8] = A + 8
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # xq_rows alignment
+    bad = list(args); bad[6] = A + 2
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # map alignment
+    bad = list(args); bad[7] = -1
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG
+
+
+def test_moe_combine_validation():
+    f = lib.fp8bs_moe_combine
+    # (yk, ldyk, R, w, rows_of_token, tokens, topk, dim, z, ldz, y, ldy, stream)
+    Y = A + 0x100000  # y far from z
+    args = [A, 128, 64, A, A, 8, 8, 128, None, 0, Y, 128, None]
+    ok = fp8bs.FP8BS_OK
+    assert f(*args[:5], 0, *args[6:]) == ok                                       # no tokens: no-op
+    bad = list(args); bad[7] = 100
+    assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # dim % 8
+    bad = list(args); bad[2] = 0
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # routed but no rows
+    bad = list(args); bad[10] = None
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # no y
+    bad = list(args); bad[1] = 64
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # ldyk < dim
+    bad = list(args); bad[1] = 132
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # ldyk % 8
+    bad = list(args); bad[3] = A + 2
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # w alignment
+    bad = list(args); bad[8], bad[9] = Y + 256, 128
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # z overlaps y
+    bad = list(args); bad[8], bad[9] = A + 0x200008, 128
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # z alignment
+    bad = list(args); bad[6] = -1
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG
+
+
 def test_debug_calls_validation():
     assert lib.fp8bs_debug_wait_timeout(0, None) == fp8bs.FP8BS_ERR_INVALID_ARG
     assert lib.fp8bs_e4m3_encode_f32(A, -1, A, None) == fp8bs.FP8BS_ERR_INVALID_ARG
@@ -130,3 +183,6 @@ def test_valid_call_without_a_device_fails_loudly():
         pytest.skip("a GPU is present")
     assert lib.fp8bs_act_quant(A, 4, 128, 128, A, 128, A, 4, None) == fp8bs.FP8BS_ERR_CUDA
     assert lib.fp8bs_gemm_workspace_size(1, 1536, 7168) == 0
+    # in-place combine (z is y) passes validation and then needs the device
+    assert lib.fp8bs_moe_combine(A, 128, 64, A, A, 8, 8, 128, A + 0x100000, 128, A + 0x100000, 128,
+                                 None) == fp8bs.FP8BS_ERR_CUDA
