@@ -48,6 +48,14 @@ def test_grouped_small(F, orc, counts, N, K):
     _grouped_small(F, orc, counts, N, K, seed=len(counts) + N)
 
 
+def test_grouped_token_tile_edges(F, orc):
+    """Experts whose row counts sit on the edges of the token tiles (16-row
+    MMA width steps, 32-row load boxes, the two 128-column promotion halves,
+    256-row tiles)."""
+    counts = [1, 16, 17, 31, 32, 33, 127, 128, 129, 255, 256, 257, 511, 0, 2]
+    _grouped_small(F, orc, counts, 256, 256, seed=17)
+
+
 def test_grouped_many_experts(F, orc):
     rng = np.random.default_rng(3)
     counts = rng.poisson(60, size=64)
