@@ -49,6 +49,9 @@ def load(mutant: int = 0) -> ctypes.CDLL:
                                       _I64, _I64, _P, _I64, _P, _P],
             "orc_moe_dispatch": [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P],
             "orc_moe_combine": [_P, _I64, _I64, _P, _P, _I64, ctypes.c_int32, _I64, _P, _I64, _P, _P],
+            "orc_moe_gate": [_P, _P, _P, _I64, _I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                             ctypes.c_int32, ctypes.c_double, _P, _P, _P],
+            "orc_moe_route": [_P, _P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P],
         }.items():
             fn = getattr(lib, name)
             fn.restype = None
@@ -210,6 +213,38 @@ class Oracle:
         self.lib.orc_moe_combine(_ptr(yk), dim, R, _ptr(w), _ptr(rt), tokens, topk, dim, zp, dim,
                                  _ptr(y), _ptr(L))
         return y, L
+
+
+    def moe_gate(self, x_bits, wg_bits, bias, n_groups=8, topk_groups=4, top_k=8, route_scale=2.5,
+                 want_scores=False):
+        """Router in fp64: returns (ids int32 [T, top_k] in descending biased
+        score, gate values fp64 [T, top_k]) and, if asked, the affinities
+        [T, E]."""
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        wg = np.ascontiguousarray(wg_bits, dtype=np.uint16)
+        b = np.ascontiguousarray(bias, dtype=np.float32)
+        T, dim = x.shape
+        E = wg.shape[0]
+        assert wg.shape[1] == dim and b.size == E and E % n_groups == 0
+        ids = np.empty((T, top_k), dtype=np.int32)
+        w = np.empty((T, top_k), dtype=np.float64)
+        s = np.empty((T, E), dtype=np.float64) if want_scores else None
+        self.lib.orc_moe_gate(_ptr(x), _ptr(wg), _ptr(b), T, dim, E, n_groups, topk_groups, top_k,
+                              float(route_scale), _ptr(ids), _ptr(w), None if s is None else _ptr(s))
+        return (ids, w, s) if want_scores else (ids, w)
+
+    def moe_route(self, ids, w, n_experts):
+        """Stable counting sort of the selections by expert: returns
+        (offsets [E+1], token_of_row [R], rows_of_token [T, k], weight_of_row [R])."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        T, k = ids.shape
+        off = np.empty(n_experts + 1, dtype=np.int32)
+        tor = np.empty(T * k, dtype=np.int32)
+        rot = np.empty((T, k), dtype=np.int32)
+        wor = np.empty(T * k, dtype=np.float32)
+        self.lib.orc_moe_route(_ptr(ids), _ptr(w), T, k, n_experts, _ptr(off), _ptr(tor), _ptr(rot), _ptr(wor))
+        return off, tor, rot, wor
 
 
 def _swiglu(lib, a, b):

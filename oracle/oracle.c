@@ -414,4 +414,98 @@ void orc_moe_combine(const double* yk, int64_t ldyk, int64_t R, const float* w, 
     }
 }
 
+/* MoE gate (router): sigmoid affinities s = sigmoid(x . wg_e) for the E
+ * routed experts (config block of "671B 参数如何「激活」37B？": sigmoid scoring,
+ * 8 expert groups of which 4 are kept, top-8 of 256, route_scale 2.5); the
+ * per-expert bias steers the selection only (page 2 section 2-2: selection
+ * looks at affinity + bias, the FFN output keeps the original gating
+ * values).  Readings where the pages are silent: a group's score is the
+ * largest biased score in it; ties go to the lower index; the gate values
+ * are the selected (unbiased) affinities normalised to sum 1, times
+ * route_scale.  All in fp64 from the bf16 inputs.  ids [T, top_k] are the
+ * selected experts in descending biased score; w [T, top_k] their gate
+ * values; s_out [T, E] (may be NULL) the affinities. */
+void orc_moe_gate(const uint16_t* x, const uint16_t* wg, const float* bias, int64_t T, int64_t dim, int32_t E,
+                  int32_t n_groups, int32_t topk_groups, int32_t top_k, double route_scale, int32_t* ids,
+                  double* w, double* s_out) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)E);
+    double* b = (double*)malloc(sizeof(double) * (size_t)E);
+    int* keep = (int*)malloc(sizeof(int) * (size_t)E);
+    double* gscore = (double*)malloc(sizeof(double) * (size_t)n_groups);
+    int* gsel = (int*)malloc(sizeof(int) * (size_t)n_groups);
+    int32_t per = E / n_groups;
+    for (int64_t t = 0; t < T; t++) {
+        for (int32_t e = 0; e < E; e++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < dim; k++)
+                acc += (double)orc_bf16_to_f32(x[t * dim + k]) * (double)orc_bf16_to_f32(wg[(int64_t)e * dim + k]);
+            s[e] = 1.0 / (1.0 + exp(-acc));
+#if ORC_MUTANT == 10
+            b[e] = s[e];                                  /* mutant: the bias ignored in the selection */
+#else
+            b[e] = s[e] + (double)bias[e];
+#endif
+            if (s_out) s_out[t * E + e] = s[e];
+        }
+        for (int32_t g = 0; g < n_groups; g++) {
+            double m = -INFINITY;
+            for (int32_t i = 0; i < per; i++) if (b[g * per + i] > m) m = b[g * per + i];
+            gscore[g] = m;
+            gsel[g] = 0;
+        }
+        for (int32_t r = 0; r < topk_groups; r++) {          /* the best remaining group, lower index on ties */
+            int32_t best = -1;
+            for (int32_t g = 0; g < n_groups; g++)
+                if (!gsel[g] && (best < 0 || gscore[g] > gscore[best])) best = g;
+            gsel[best] = 1;
+        }
+        for (int32_t e = 0; e < E; e++) keep[e] = gsel[e / per];
+        double ssum = 0.0;
+        for (int32_t r = 0; r < top_k; r++) {                /* the best remaining kept expert */
+            int32_t best = -1;
+            for (int32_t e = 0; e < E; e++)
+                if (keep[e] && (best < 0 || b[e] > b[best])) best = e;
+            ids[t * top_k + r] = best;
+            keep[best] = 0;
+            ssum += s[best];
+        }
+        for (int32_t r = 0; r < top_k; r++)
+#if ORC_MUTANT == 11
+            w[t * top_k + r] = s[ids[t * top_k + r]] * route_scale; /* mutant: not normalised */
+#else
+            w[t * top_k + r] = s[ids[t * top_k + r]] / ssum * route_scale;
+#endif
+    }
+    free(s); free(b); free(keep); free(gscore); free(gsel);
+}
+
+/* MoE routing tables: the (token, k) selections grouped by expert, tokens
+ * in order within an expert (a stable counting sort), so that each expert's
+ * rows are contiguous for the grouped GEMM:
+ *   offsets [E+1]: rows of expert e are offsets[e] .. offsets[e+1]-1
+ *   token_of_row [T*top_k], weight_of_row [T*top_k] (the pair's gate value),
+ *   rows_of_token [T, top_k]: the routed row of selection (t, k). */
+void orc_moe_route(const int32_t* ids, const float* w, int64_t T, int32_t top_k, int32_t E, int32_t* offsets,
+                   int32_t* token_of_row, int32_t* rows_of_token, float* weight_of_row) {
+    int32_t* next = (int32_t*)calloc((size_t)E + 1, sizeof(int32_t));
+    for (int32_t e = 0; e <= E; e++) offsets[e] = 0;
+    for (int64_t i = 0; i < T * top_k; i++) offsets[ids[i] + 1]++;
+    for (int32_t e = 0; e < E; e++) offsets[e + 1] += offsets[e];
+    for (int32_t e = 0; e < E; e++) next[e] = offsets[e];
+#if ORC_MUTANT == 12
+    for (int64_t t = T - 1; t >= 0; t--) {                  /* mutant: tokens in reverse within an expert */
+#else
+    for (int64_t t = 0; t < T; t++) {
+#endif
+        for (int32_t k = 0; k < top_k; k++) {
+            int32_t e = ids[t * top_k + k];
+            int32_t r = next[e]++;
+            token_of_row[r] = (int32_t)t;
+            rows_of_token[t * top_k + k] = r;
+            weight_of_row[r] = w[t * top_k + k];
+        }
+    }
+    free(next);
+}
+
 int orc_mutant_id(void) { return ORC_MUTANT; }

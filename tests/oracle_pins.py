@@ -489,6 +489,90 @@ def pin_moe_combine(o):
     assert np.array_equal(y3, yk[rt1[:, 0]] + z)
 
 
+def _gate_case(logits, dim=64):
+    """x [T, dim], wg [E, dim] in bf16 with x . wg_e equal to the given
+    (bf16-representable) logits exactly: x_t = the unit vector e_t-ish
+    encoding, built as x[t] = one-hot of t (T <= dim) and wg[e, t] = logit."""
+    T, E = logits.shape
+    assert T <= dim
+    x = np.zeros((T, dim), dtype=np.float32)
+    x[np.arange(T), np.arange(T)] = 1.0
+    wg = np.zeros((E, dim), dtype=np.float32)
+    wg[:, :T] = logits.T
+    return bf16_bits(x), bf16_bits(wg)
+
+
+def pin_moe_gate(o):
+    """Router, constructed cases whose answer is fixed by design: logits
+    placed exactly (one-hot tokens), affinities against scipy's logistic
+    function; the best groups are kept and an expert outside them is not
+    chosen even when its score is higher than a chosen one; the bias moves the
+    selection but not the gate values; the gate values are the chosen
+    affinities normalised to 2.5."""
+    from scipy.special import expit
+    E, G = 16, 4                                   # 4 groups of 4 experts, keep 2, top-3
+    lg = np.full((2, E), -4.0, dtype=np.float32)
+    # token 0: group 0 = {0.5, 3, -1, 0.25}, group 1 = {2, 1.5, 1.75, 0}, group 2 = {2.5, -2, -2, -2}, group 3 low
+    lg[0, :12] = [0.5, 3.0, -1.0, 0.25, 2.0, 1.5, 1.75, 0.0, 2.5, -2.0, -2.0, -2.0]
+    # token 1: same, but the bias lifts expert 15 (group 3) to the top
+    lg[1] = lg[0]
+    x, wg = _gate_case(lg)
+    bias = np.zeros(E, dtype=np.float32)
+    ids, w, s = o.moe_gate(x, wg, bias, n_groups=G, topk_groups=2, top_k=3, want_scores=True)
+    assert np.allclose(s, expit(lg.astype(np.float64)), rtol=1e-15, atol=0)
+    # group maxima: g0 3.0, g2 2.5, g1 2.0 -> keep g0, g2; top-3 of {0.5,3,-1,.25,2.5,-2,-2,-2} = 1, 8, 0
+    assert ids[0].tolist() == [1, 8, 0]
+    # expert 4 (logit 2.0 > 0.5) is not chosen: its group is not kept
+    ref = expit(np.array([3.0, 2.5, 0.5]))
+    assert np.allclose(w[0], ref / ref.sum() * 2.5, rtol=1e-14)
+    assert abs(w[0].sum() - 2.5) < 1e-14
+    bias[15] = 0.99                                  # affinity expit(-4) = 0.018 + 0.99: top of group 3
+    ids_b, w_b = o.moe_gate(x, wg, bias, n_groups=G, topk_groups=2, top_k=3)
+    # group 3 (1.008) now outranks group 2 (0.924), which drops out with expert 8
+    assert ids_b[1].tolist() == [15, 1, 0]
+    ref_b = expit(np.array([-4.0, 3.0, 0.5]))
+    assert np.allclose(w_b[1], ref_b / ref_b.sum() * 2.5, rtol=1e-14)   # unbiased values weight the output
+    # ties: equal logits in one group go to the lower index
+    lt = np.zeros((1, E), dtype=np.float32)
+    x2, wg2 = _gate_case(lt)
+    ids_t, _ = o.moe_gate(x2, wg2, np.zeros(E, dtype=np.float32), n_groups=G, topk_groups=2, top_k=3)
+    assert ids_t[0].tolist() == [0, 1, 2]
+    # random data: gate values sum to route_scale, ids distinct and inside kept groups
+    rng = np.random.default_rng(25)
+    xr = synth.normal_bf16(rng, (8, 256), 1.0)
+    wr = synth.normal_bf16(rng, (64, 256), 0.05)
+    br = rng.uniform(-0.1, 0.1, 64).astype(np.float32)
+    ids_r, w_r = o.moe_gate(xr, wr, br)
+    assert np.allclose(w_r.sum(axis=1), 2.5, rtol=1e-14)
+    assert all(len(set(r)) == 8 for r in ids_r.tolist())
+    assert all(len(set(e // 8 for e in r)) <= 4 for r in ids_r.tolist())
+
+
+def pin_moe_route(o):
+    """Routing tables against numpy's stable argsort of the selections by
+    expert: offsets from the expert counts, tokens in order within an
+    expert, rows_of_token the inverse map, gate values carried along."""
+    rng = np.random.default_rng(26)
+    T, k, E = 50, 4, 12
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[:, 0] = 3                                     # a busy expert; expert 11 may stay empty
+    ids[ids == 11] = 10
+    for t in range(T):                                # keep selections distinct per token
+        if len(set(ids[t].tolist())) < k:
+            ids[t] = [3, 0, 1, 2]
+    w = rng.uniform(0.1, 1.0, size=(T, k)).astype(np.float32)
+    off, tor, rot, wor = o.moe_route(ids, w, E)
+    flat = ids.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    assert np.array_equal(off, np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+    assert np.array_equal(tor, (np.arange(T * k) // k)[order])
+    assert np.array_equal(wor.view(np.uint32), w.reshape(-1)[order].view(np.uint32))
+    inv = np.empty_like(order)
+    inv[order] = np.arange(order.size)
+    assert np.array_equal(rot.reshape(-1), inv)
+    assert off[11] == off[12]
+
+
 ALL_PINS = [
     pin_codec_midpoints,
     pin_act_quant_rank1,
@@ -507,4 +591,6 @@ ALL_PINS = [
     pin_swiglu,
     pin_moe_dispatch,
     pin_moe_combine,
+    pin_moe_gate,
+    pin_moe_route,
 ]

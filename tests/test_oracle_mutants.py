@@ -9,6 +9,9 @@
   7 silu with the exponent's sign flipped
   8 MoE combine dropping the last routed expert
   9 MoE dispatch taking the scales of the wrong row
+ 10 router ignoring the bias in the selection
+ 11 router gate values not normalised
+ 12 routing tables with tokens in reverse order within an expert
 """
 import pytest
 
@@ -16,7 +19,7 @@ from oracle import Oracle
 from oracle_pins import ALL_PINS
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12])
 def test_mutant_is_caught(mutant):
     o = Oracle(mutant)
     assert o.lib.orc_mutant_id() == mutant
