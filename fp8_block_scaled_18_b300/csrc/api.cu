@@ -240,6 +240,43 @@ fp8bs_status fp8bs_moe_combine(const uint16_t* yk, int64_t ldyk, int64_t R, cons
                                         d, cs(stream)));
 }
 
+fp8bs_status fp8bs_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, const float* bias, int64_t T,
+                            int64_t dim, int32_t E, int32_t n_groups, int32_t topk_groups, int32_t top_k,
+                            float route_scale, int32_t* ids, float* weights, fp8bs_stream_t stream) {
+    if (T < 0 || dim < 0 || E <= 0 || n_groups <= 0 || topk_groups <= 0 || top_k <= 0) return FP8BS_ERR_INVALID_ARG;
+    if (E % 16 || E > 256 || dim == 0 || dim % 64) return FP8BS_ERR_UNSUPPORTED;
+    if (E % n_groups || n_groups > 32 || topk_groups > n_groups) return FP8BS_ERR_INVALID_ARG;
+    if (top_k > 16 || top_k > topk_groups * (E / n_groups)) return FP8BS_ERR_INVALID_ARG;
+    if (T == 0) return FP8BS_OK;
+    if (T > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
+    if (!x || !wg || !ids || !weights || ldx < dim) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(wg) || ldx % 8 || (reinterpret_cast<uintptr_t>(bias) & 3u) ||
+        (reinterpret_cast<uintptr_t>(ids) & 3u) || (reinterpret_cast<uintptr_t>(weights) & 3u))
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_moe_gate(x, ldx, wg, bias, T, dim, E, n_groups, topk_groups, top_k, route_scale, ids,
+                                     weights, d, cs(stream)));
+}
+
+fp8bs_status fp8bs_moe_route(const int32_t* ids, const float* weights, int64_t T, int32_t top_k, int32_t E,
+                             int32_t* offsets, int32_t* token_of_row, int32_t* rows_of_token, float* weight_of_row,
+                             fp8bs_stream_t stream) {
+    if (T < 0 || top_k <= 0 || E <= 0) return FP8BS_ERR_INVALID_ARG;
+    if (E > 256) return FP8BS_ERR_UNSUPPORTED;
+    if (!offsets) return FP8BS_ERR_INVALID_ARG;
+    if (T > 0 && (!ids || !weights || !token_of_row || !rows_of_token || !weight_of_row)) return FP8BS_ERR_INVALID_ARG;
+    if (T * static_cast<int64_t>(top_k) > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(ids) | reinterpret_cast<uintptr_t>(weights) | reinterpret_cast<uintptr_t>(offsets) |
+         reinterpret_cast<uintptr_t>(token_of_row) | reinterpret_cast<uintptr_t>(rows_of_token) |
+         reinterpret_cast<uintptr_t>(weight_of_row)) & 3u)
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_moe_route(ids, weights, T, top_k, E, offsets, token_of_row, rows_of_token, weight_of_row,
+                                      d, cs(stream)));
+}
+
 fp8bs_status fp8bs_sync_status(fp8bs_stream_t stream) {
     if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
     DeviceInfo d;

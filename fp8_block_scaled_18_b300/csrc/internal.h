@@ -74,6 +74,14 @@ cudaError_t launch_moe_combine(const uint16_t* yk, int64_t ldyk, int64_t R, cons
                                const uint16_t* z, int64_t ldz, uint16_t* y, int64_t ldy, const DeviceInfo& dev,
                                cudaStream_t stream);
 
+// MoE router (router.cu).
+cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, const float* bias, int64_t T,
+                            int64_t dim, int E, int n_groups, int topk_groups, int top_k, float route_scale,
+                            int32_t* ids, float* w, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_moe_route(const int32_t* ids, const float* w, int64_t T, int top_k, int E, int32_t* offsets,
+                             int32_t* token_of_row, int32_t* rows_of_token, float* weight_of_row,
+                             const DeviceInfo& dev, cudaStream_t stream);
+
 // Dense and grouped GEMM (gemm.cu).
 struct GemmArgs {
     const uint8_t* xq;

@@ -40,6 +40,8 @@ _SIGS = {
                                         _I64, _P, _I64, _P]),
     "fp8bs_moe_dispatch": (_ST, [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
     "fp8bs_moe_combine": (_ST, [_P, _I64, _I64, _P, _P, _I64, _I32, _I64, _P, _I64, _P, _I64, _P]),
+    "fp8bs_moe_gate": (_ST, [_P, _I64, _P, _P, _I64, _I64, _I32, _I32, _I32, _I32, ctypes.c_float, _P, _P, _P]),
+    "fp8bs_moe_route": (_ST, [_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P]),
     "fp8bs_sync_status": (_ST, [_P]),
     "fp8bs_status_string": (ctypes.c_char_p, [_ST]),
     "fp8bs_e4m3_encode_f32": (_ST, [_P, _I64, _P, _P]),
@@ -324,6 +326,57 @@ def fp8bs_moe_combine(yk: torch.Tensor, weight_of_row: torch.Tensor, rows_of_tok
                                  None if z is None else _bf16_ptr(z, "z"), 0 if z is None else _rows_stride(z, "z"),
                                  _bf16_ptr(y, "y"), _rows_stride(y, "y"), _stream(stream)), "fp8bs_moe_combine")
     return y
+
+
+def fp8bs_moe_gate(x: torch.Tensor, wg: torch.Tensor, bias: Optional[torch.Tensor] = None, n_groups: int = 8,
+                   topk_groups: int = 4, top_k: int = 8, route_scale: float = 2.5,
+                   ids: Optional[torch.Tensor] = None, weights: Optional[torch.Tensor] = None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Router: x [T, dim] bf16, wg [E, dim] bf16, bias fp32 [E] or None ->
+    (ids int32 [T, top_k], gate values fp32 [T, top_k])."""
+    T, dim = x.shape
+    E = wg.shape[0]
+    if not wg.is_contiguous() or wg.shape[1] != dim:
+        raise ValueError("wg must be a contiguous [E, dim] tensor")
+    if bias is not None and (bias.numel() != E or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous tensor of E elements")
+    if ids is None:
+        ids = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    if weights is None:
+        weights = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    _check(lib.fp8bs_moe_gate(_bf16_ptr(x, "x"), _rows_stride(x, "x"), _bf16_ptr(wg, "wg"),
+                              None if bias is None else _dev(bias, torch.float32, "bias"), T, dim, E, n_groups,
+                              topk_groups, top_k, route_scale, _dev(ids, torch.int32, "ids"),
+                              _dev(weights, torch.float32, "weights"), _stream(stream)), "fp8bs_moe_gate")
+    return ids, weights
+
+
+def fp8bs_moe_route(ids: torch.Tensor, weights: torch.Tensor, n_experts: int,
+                    offsets: Optional[torch.Tensor] = None, token_of_row: Optional[torch.Tensor] = None,
+                    rows_of_token: Optional[torch.Tensor] = None, weight_of_row: Optional[torch.Tensor] = None,
+                    stream=None):
+    """Routing tables from ids / weights [T, top_k]: returns (offsets int32
+    [E+1], token_of_row int32 [R], rows_of_token int32 [T, top_k],
+    weight_of_row fp32 [R]), R = T * top_k."""
+    T, k = ids.shape
+    if not ids.is_contiguous() or not weights.is_contiguous() or weights.shape != ids.shape:
+        raise ValueError("ids and weights must be contiguous [T, top_k] tensors")
+    dev_ = ids.device
+    if offsets is None:
+        offsets = torch.empty(n_experts + 1, dtype=torch.int32, device=dev_)
+    if token_of_row is None:
+        token_of_row = torch.empty(T * k, dtype=torch.int32, device=dev_)
+    if rows_of_token is None:
+        rows_of_token = torch.empty((T, k), dtype=torch.int32, device=dev_)
+    if weight_of_row is None:
+        weight_of_row = torch.empty(T * k, dtype=torch.float32, device=dev_)
+    _check(lib.fp8bs_moe_route(_dev(ids, torch.int32, "ids"), _dev(weights, torch.float32, "weights"), T, k,
+                               n_experts, _dev(offsets, torch.int32, "offsets"),
+                               _dev(token_of_row, torch.int32, "token_of_row"),
+                               _dev(rows_of_token, torch.int32, "rows_of_token"),
+                               _dev(weight_of_row, torch.float32, "weight_of_row"), _stream(stream)),
+           "fp8bs_moe_route")
+    return offsets, token_of_row, rows_of_token, weight_of_row
 
 
 def fp8bs_sync_status(stream=None) -> int:

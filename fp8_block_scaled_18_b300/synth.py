@@ -111,6 +111,8 @@ class MoECase:
     expert_seed0: int
     weight_of_row: np.ndarray = None   # fp32 [T]: routing weight of each grouped row
     rows_of_token: np.ndarray = None   # int32 [tokens, top_k]: the grouped rows of each token
+    gate_w: np.ndarray = None          # bf16 bits [n_experts, K]: the router's weight
+    gate_bias: np.ndarray = None       # fp32 [n_experts]: the router's selection bias
 
     @property
     def x_rows(self) -> np.ndarray:
@@ -168,7 +170,7 @@ def moe(seed: int = 4, tokens: int = 4096, n_experts: int = N_EXPERTS, n: int = 
     row_of_pair[order] = np.arange(order.size)
     return MoECase(x, flat_t[order], offsets, n_experts, n, k, expert_seed0,
                    weights.reshape(-1)[order].astype(np.float32),
-                   row_of_pair.reshape(tokens, experts.shape[1]).astype(np.int32))
+                   row_of_pair.reshape(tokens, experts.shape[1]).astype(np.int32), gw, bias)
 
 
 def expert_weight(case: MoECase, g: int, device: str = "cpu", which: int = 0) -> torch.Tensor:

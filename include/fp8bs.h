@@ -246,6 +246,48 @@ fp8bs_status fp8bs_moe_combine(const uint16_t* yk, int64_t ldyk, int64_t R, cons
                                const int32_t* rows_of_token, int64_t tokens, int32_t topk, int64_t dim,
                                const uint16_t* z, int64_t ldz, uint16_t* y, int64_t ldy, fp8bs_stream_t stream);
 
+/* MoE router (gate): for each token t, the sigmoid affinities
+ * s_e = sigmoid(x_t . wg_e) of the E routed experts, computed from the bf16
+ * operands with fp32 accumulation on the tensor cores (gating stays in
+ * higher precision than FP8: DeepSeek-V3 notes, page 2 section 2-4); the
+ * selection looks at s_e + bias_e, the gate values at s_e alone (page 2
+ * section 2-2).  The experts form n_groups equal groups of consecutive
+ * indices; a group's score is its largest biased affinity; the topk_groups
+ * best groups are kept, and the top_k best biased affinities among their
+ * experts are chosen (ties to the lower index throughout).  Gate values:
+ * w_k = s_k / (sum of the chosen s) * route_scale (DeepSeek-V3: sigmoid
+ * scoring, 8 groups keep 4, top-8 of 256, route_scale 2.5 -- config block
+ * of "671B 参数如何「激活」37B？").  All in fp32; the sigmoid uses expf.
+ *   x  bf16 [T, ldx] (ldx >= dim, ldx % 8 == 0, 16-byte aligned)
+ *   wg bf16 [E, dim] dense, 16-byte aligned; bias fp32 [E] or NULL (zeros)
+ *   ids int32 [T, top_k]: the chosen experts, best biased affinity first
+ *   weights fp32 [T, top_k]: their gate values
+ * dim % 64 == 0 and E % 16 == 0, E <= 256 (else FP8BS_ERR_UNSUPPORTED);
+ * n_groups divides E, n_groups <= 32, 1 <= topk_groups <= n_groups,
+ * 1 <= top_k <= 16 and top_k <= topk_groups * E / n_groups (else
+ * FP8BS_ERR_INVALID_ARG).  Near-ties may resolve differently from an exact
+ * (fp64) router: the logits carry fp32 rounding. */
+fp8bs_status fp8bs_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, const float* bias, int64_t T,
+                            int64_t dim, int32_t E, int32_t n_groups, int32_t topk_groups, int32_t top_k,
+                            float route_scale, int32_t* ids, float* weights, fp8bs_stream_t stream);
+
+/* MoE routing tables: the (token, k) selections grouped by expert, tokens in
+ * order within an expert (a stable counting sort; the same result on every
+ * run) -- the layout fp8bs_moe_dispatch, the grouped GEMMs and
+ * fp8bs_moe_combine take:
+ *   offsets int32 [E+1]: expert e's routed rows are offsets[e] .. offsets[e+1]-1
+ *   token_of_row int32 [T*top_k], weight_of_row fp32 [T*top_k]: per routed row
+ *      its token and gate value
+ *   rows_of_token int32 [T, top_k]: the routed row of selection (t, k)
+ * from ids int32 [T, top_k] and weights fp32 [T, top_k] (fp8bs_moe_gate's
+ * outputs).  E <= 256 (else FP8BS_ERR_UNSUPPORTED); all pointers 4-byte
+ * aligned.  An id outside [0, E) gets no row (rows_of_token -1); a token
+ * naming one expert twice leaves a row with token -1 and gate 0; both set
+ * FP8BS_ERR_INDEX for the next fp8bs_sync_status(). */
+fp8bs_status fp8bs_moe_route(const int32_t* ids, const float* weights, int64_t T, int32_t top_k, int32_t E,
+                             int32_t* offsets, int32_t* token_of_row, int32_t* rows_of_token, float* weight_of_row,
+                             fp8bs_stream_t stream);
+
 /* Synchronise `stream`, then report and clear this device's status word:
  * FP8BS_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,
  * else FP8BS_ERR_INDEX if a MoE gather met an out-of-range id, FP8BS_ERR_CUDA

@@ -169,6 +169,47 @@ def test_moe_combine_validation():
     assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG
 
 
+def test_moe_gate_validation():
+    f = lib.fp8bs_moe_gate
+    # (x, ldx, wg, bias, T, dim, E, n_groups, topk_groups, top_k, route_scale, ids, weights, stream)
+    args = [A, 7168, A, A, 64, 7168, 256, 8, 4, 8, 2.5, A, A, None]
+    assert f(*args[:4], 0, *args[5:]) == fp8bs.FP8BS_OK                          # no tokens: no-op
+    bad = list(args); bad[5] = 7000
+    assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # dim % 64
+    bad = list(args); bad[6] = 264
+    assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # E > 256
+    bad = list(args); bad[7] = 7
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # groups do not divide E
+    bad = list(args); bad[8] = 9
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # keep more groups than exist
+    bad = list(args); bad[9] = 17
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # top_k > 16
+    bad = list(args); bad[7], bad[8], bad[9] = 32, 1, 9
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                 # top_k > experts kept
+    bad = list(args); bad[1] = 7172
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # ldx % 8
+    bad = list(args); bad[2] = A + 8
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # wg alignment
+    bad = list(args); bad[11] = None
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG
+
+
+def test_moe_route_validation():
+    f = lib.fp8bs_moe_route
+    # (ids, weights, T, top_k, E, offsets, token_of_row, rows_of_token, weight_of_row, stream)
+    args = [A, A, 64, 8, 256, A, A, A, A, None]
+    bad = list(args); bad[4] = 300
+    assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # E > 256
+    bad = list(args); bad[3] = 0
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG
+    bad = list(args); bad[6] = None
+    assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG
+    bad = list(args); bad[7] = A + 2
+    assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED
+    bad = list(args); bad[2] = 2 ** 29
+    assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # more routed rows than int32
+
+
 def test_debug_calls_validation():
     assert lib.fp8bs_debug_wait_timeout(0, None) == fp8bs.FP8BS_ERR_INVALID_ARG
     assert lib.fp8bs_e4m3_encode_f32(A, -1, A, None) == fp8bs.FP8BS_ERR_INVALID_ARG
