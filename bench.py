@@ -423,12 +423,13 @@ class MoEWork:
 
 
 class MoELayerWork:
-    """The routed-expert layer end to end on the device, router excluded:
+    """The routed-expert layer end to end on the device: the router (gate
+    logits, group-limited top-8, gate values) and its routing tables,
     act_quant of the tokens, dispatch into expert order, the w1|w3 SwiGLU
     stage with FP8 h, the w2 grouped GEMM, the shared expert (SwiGLU stage
     over all tokens, dense w2 GEMM) and the gated combine with the shared
-    output added.  Expert and shared weights are quantised once, before
-    timing; routing (expert ids, gate values) comes from the generator."""
+    output added.  Expert, shared and gate weights are quantised (or, for the
+    gate, stored in bf16) once, before timing."""
 
     def __init__(self, device):
         import torch
@@ -777,13 +778,14 @@ def _expert_weights_q(orc, case, g, whichs):
 
 
 def oracle_layer_rows(orc, case, wts, rows):
-    """The routed layer's oracle pass for some of one expert's rows: act_quant
-    of their tokens, the w1 and w3 GEMMs, silu(a) * b, h rounded to bf16 and
+    """The routed layer's oracle pass for some of one expert's rows: the router
+    for their tokens, act_quant of the tokens, the w1 and w3 GEMMs, silu(a) * b, h rounded to bf16 and
     quantised, the w2 GEMM, and the gated combine of those rows (each taken
     alone).  wts = the expert's quantised (w1, w3, w2).  Returns flops."""
     from fp8_block_scaled_18_b300 import synth
     (w1q, sw1), (w3q, sw3), (w2q, sw2) = wts
     toks = case.token_of_row[rows]
+    orc.moe_gate(case.x_tokens[toks], case.gate_w, case.gate_bias)  # the router for those tokens
     xq, sx = orc.act_quant(case.x_tokens[toks])
     a, _ = orc.gemm(xq, sx, w1q, sw1)
     b, _ = orc.gemm(xq, sx, w3q, sw3)
@@ -791,7 +793,7 @@ def oracle_layer_rows(orc, case, wts, rows):
     hq, sh = orc.act_quant(synth.to_bf16_bits(h.astype(np.float32)))
     yk, _ = orc.gemm(hq, sh, w2q, sw2)
     orc.moe_combine(yk, case.weight_of_row[rows], np.arange(len(rows), dtype=np.int32).reshape(-1, 1))
-    return len(rows) * (6.0 * case.n * case.k)
+    return len(rows) * (6.0 * case.n * case.k + 2.0 * case.n_experts * case.k)
 
 
 def make_case(workload: str):
@@ -847,7 +849,7 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
             flops += oracle_layer_rows(orc, case, wts, np.arange(r0, min(r1, r0 + 32)))
             n += 1
         dt = time.perf_counter() - t0
-        sample = (f"{n} experts x <=32 rows: weight_quant of the expert's w1, w3 and w2, act_quant, gemm x2, "
+        sample = (f"{n} experts x <=32 rows: weight_quant of the expert's w1, w3 and w2, router, act_quant, gemm x2, "
                   f"silu(a) * b, act_quant(h), gemm (w2), gated combine; TFLOP/s over the sampled GEMM work")
     elif workload in ("moe", "moe_swiglu"):
         swiglu = workload == "moe_swiglu"
@@ -916,7 +918,8 @@ def run_reference(args, rank, local, world):
         rows = int(max(1, min(r1 - r0, (budget / (K + W) - fixed) / per_row)))
         step = lambda i: layer_step(i, rows)  # noqa: E731
         sample = (f"expert {g} ({r1 - r0} rows): per step one 128-row block of its w1 quantised, "
-                  f"{rows} of its rows through act_quant, w1/w3 gemm, silu * b, act_quant(h), w2 gemm, combine")
+                  f"{rows} of its rows through the router, act_quant, w1/w3 gemm, silu * b, act_quant(h), w2 gemm, "
+                  f"combine")
         cfg = {"workload": "moe_layer"}
     elif args.workload in ("moe", "moe_swiglu"):
         import torch
