@@ -6,9 +6,11 @@
 
 One step = one pass of the whole path over one batch of synthetic input:
 dense workloads run weight_quant(W), act_quant(X), fp8_gemm and
-weight_dequant(Wq); the MoE workload runs act_quant over the expert-grouped
-token rows and the grouped fp8_gemm (expert weights quantised once, before
-timing).  The default workload is the MLA KV down-projection
+weight_dequant(Wq) (q_down_m<M>_fused: the GEMM with bias and FP8 output);
+moe runs act_quant over the expert-grouped token rows and the grouped
+fp8_gemm, moe_swiglu the grouped w1|w3 stage with SwiGLU and FP8 h, and
+moe_layer the whole routed layer with its router (expert weights quantised
+once, before timing).  The default workload is the MLA KV down-projection
 (X [4096,7168] x W [576,7168]).
 
 Timing: W warm-up steps, then exactly K steps captured in CUDA graphs and

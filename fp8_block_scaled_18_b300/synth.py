@@ -123,8 +123,10 @@ class MoECase:
 def route(x_bits: np.ndarray, gate_w_bits: np.ndarray, bias: np.ndarray,
           n_groups: int = N_GROUPS, topk_groups: int = TOPK_GROUPS, top_k: int = TOP_K,
           with_weights: bool = False, route_scale: float = ROUTE_SCALE):
-    """Sigmoid-scored, group-limited top-k routing (harness only: it decides
-    which rows each expert receives).  The bias steers selection only.  The
+    """Sigmoid-scored, group-limited top-k routing of the synthetic tokens (an
+    input generator: it decides which rows each expert receives in the
+    workloads that take the routing as given; the library's own router is
+    fp8bs_moe_gate).  The bias steers selection only.  The
     group score is the largest biased score in the group; ties go to the lower
     index.  Returns expert ids [tokens, top_k]; with_weights also the routing
     weights: the selected (unbiased) scores normalised to sum 1, times
