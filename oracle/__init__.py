@@ -52,6 +52,9 @@ def load(mutant: int = 0) -> ctypes.CDLL:
             "orc_moe_gate": [_P, _P, _P, _I64, _I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                              ctypes.c_int32, ctypes.c_double, _P, _P, _P],
             "orc_moe_route": [_P, _P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P],
+            "orc_act_quant_cols": [_P, _I64, _I64, _I64, _P, _I64, _P],
+            "orc_gemm_dgrad_rows": [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P],
+            "orc_gemm_wgrad": [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _P, _P],
         }.items():
             fn = getattr(lib, name)
             fn.restype = None
@@ -245,6 +248,50 @@ class Oracle:
         wor = np.empty(T * k, dtype=np.float32)
         self.lib.orc_moe_route(_ptr(ids), _ptr(w), T, k, n_experts, _ptr(off), _ptr(tor), _ptr(rot), _ptr(wor))
         return off, tor, rot, wor
+
+
+    def act_quant_cols(self, x_bits):
+        """x [M, K] bf16 bits -> (xq [M, K] u8, sx [ceil(M/128), K] fp32):
+        128x1 groups along the rows (the wgrad operands' quantisation)."""
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        M, K = x.shape
+        xq = np.empty((M, K), dtype=np.uint8)
+        sx = np.empty(((M + 127) // 128, K), dtype=np.float32)
+        self.lib.orc_act_quant_cols(_ptr(x), M, K, K, _ptr(xq), K, _ptr(sx))
+        return xq, sx
+
+    def gemm_dgrad(self, dyq, sdy, wq, sw, rows=None):
+        """dX = dY W from dyq [M, N] (1x128 groups, sdy [M, >= N/128]) and the
+        forward's wq [N, K], sw [ceil(N/128), K/128]: (dx, L) fp64 [rows, K]."""
+        dyq = np.ascontiguousarray(dyq, dtype=np.uint8)
+        sdy = np.ascontiguousarray(sdy, dtype=np.float32)
+        wq = np.ascontiguousarray(wq, dtype=np.uint8)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        M, N = dyq.shape
+        N2, K = wq.shape
+        assert N2 == N and N % 128 == 0 and sw.shape == (N // 128, K // 128)
+        rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        dx = np.empty((rows.size, K), dtype=np.float64)
+        L = np.empty((rows.size, K), dtype=np.float64)
+        self.lib.orc_gemm_dgrad_rows(_ptr(dyq), N, _ptr(sdy), sdy.shape[1], _ptr(wq), _ptr(sw), N, K, _ptr(rows),
+                                     rows.size, _ptr(dx), _ptr(L))
+        return dx, L
+
+    def gemm_wgrad(self, dyq, sdy, xq, sx):
+        """dW = dY^T X from 128x1-grouped dyq [M, N] / sdy and xq [M, K] / sx
+        (act_quant_cols): (dw, L) fp64 [N, K]."""
+        dyq = np.ascontiguousarray(dyq, dtype=np.uint8)
+        sdy = np.ascontiguousarray(sdy, dtype=np.float32)
+        xq = np.ascontiguousarray(xq, dtype=np.uint8)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        M, N = dyq.shape
+        M2, K = xq.shape
+        MB = (M + 127) // 128
+        assert M2 == M and sdy.shape == (MB, N) and sx.shape == (MB, K)
+        dw = np.empty((N, K), dtype=np.float64)
+        L = np.empty((N, K), dtype=np.float64)
+        self.lib.orc_gemm_wgrad(_ptr(dyq), N, _ptr(sdy), _ptr(xq), K, _ptr(sx), M, N, K, _ptr(dw), _ptr(L))
+        return dw, L
 
 
 def _swiglu(lib, a, b):

@@ -508,4 +508,113 @@ void orc_moe_route(const int32_t* ids, const float* w, int64_t T, int32_t top_k,
     free(next);
 }
 
+/* ------------------------------------------------------------------ */
+/* Backward GEMMs (training)                                           */
+/* ------------------------------------------------------------------ */
+/* The pages run training in E4M3 in both directions, with block-wise
+ * scaling (88811315.cn post, the Float8 paragraph: E4M3 for forward and
+ * backward alike, instead of E5M2 for gradients), but give no granularity
+ * for the backward GEMMs.  Reading taken: every operand is grouped in 128s
+ * along the contraction dimension of the GEMM it feeds, so each 128-wide
+ * chunk of a dot product carries one scale per row and one per column -- the
+ * forward's structure -- and the weight keeps its 128x128 blocks.
+ *   dgrad  dX = dY W      (contraction over N): dY in 1x128 groups along N
+ *                         (act_quant applied to dY), W's blocks reused.
+ *   wgrad  dW = dY^T X    (contraction over the tokens M): dY and X in 128x1
+ *                         groups along M (act_quant_cols).               */
+
+/* act_quant_cols: per column k and per block mb of 128 rows (the last block
+ * may be ragged: amax over its valid rows, as R6), amax = max |x|,
+ * s = amax/448, q = e4m3(x/s).  x: bf16 bits [M, K] row stride ldx; xq [M, K]
+ * row stride ldq; sx fp32 [ceil(M/128), K] row-major (block mb, column k at
+ * sx[mb*K + k]). */
+void orc_act_quant_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq, float* sx) {
+    int64_t MB = (M + ORC_BLOCK - 1) / ORC_BLOCK;
+    for (int64_t mb = 0; mb < MB; mb++) {
+        int64_t m0 = mb * ORC_BLOCK, m1 = m0 + ORC_BLOCK < M ? m0 + ORC_BLOCK : M;
+#if ORC_MUTANT == 13
+        int64_t m_amax = m1 - 1 > m0 ? m1 - 1 : m1;   /* mutant: the block's last row left out of the amax */
+#else
+        int64_t m_amax = m1;
+#endif
+        for (int64_t k = 0; k < K; k++) {
+            float amax = 0.0f;
+            for (int64_t m = m0; m < m_amax; m++) amax = fmaxf(amax, fabsf(orc_bf16_to_f32(x[m * ldx + k])));
+            float s = orc_scale_from_amax(amax);
+            for (int64_t m = m0; m < m1; m++) xq[m * ldq + k] = orc_quantize_one(orc_bf16_to_f32(x[m * ldx + k]), amax, s);
+            sx[mb * K + k] = s;
+        }
+    }
+}
+
+/* dgrad: dX[m,k] = sum_nb sdy[m,nb] * sw[nb, k/128] * B_nb[m,k],
+ *   B_nb[m,k] = sum_{n in chunk nb} dec(dyq[m,n]) * dec(wq[n,k]),
+ * exact fp64 per chunk as in orc_gemm_rows.  dyq [M, N] row stride ldq,
+ * sdy [M, lds] (1x128 groups along N), wq [N, K], sw [ceil(N/128), K/128];
+ * N % 128 == 0.  Only the listed rows; dx and L are [nrows, K]. */
+void orc_gemm_dgrad_rows(const uint8_t* dyq, int64_t ldq, const float* sdy, int64_t lds, const uint8_t* wq,
+                         const float* sw, int64_t N, int64_t K, const int64_t* rows, int64_t nrows, double* dx,
+                         double* L) {
+    int64_t NB = N / ORC_BLOCK, KB = K / ORC_BLOCK;
+    double* dyd = (double*)malloc(sizeof(double) * (size_t)N);
+    for (int64_t r = 0; r < nrows; r++) {
+        int64_t m = rows[r];
+        for (int64_t n = 0; n < N; n++) dyd[n] = orc_e4m3_decode(dyq[m * ldq + n]);
+        for (int64_t k = 0; k < K; k++) {
+            double acc = 0.0, lsum = 0.0;
+            for (int64_t nb = 0; nb < NB; nb++) {
+                double b = 0.0, babs = 0.0;
+                for (int64_t n = nb * ORC_BLOCK; n < (nb + 1) * ORC_BLOCK; n++) {
+                    double p = dyd[n] * orc_e4m3_decode(wq[n * K + k]);
+                    b += p;
+                    babs += fabs(p);
+                }
+#if ORC_MUTANT == 14
+                double scale = (double)sdy[m * lds + nb] * (double)sw[(k / ORC_BLOCK) * NB + nb]; /* mutant: the weight's block grid read as if stored transposed */
+#else
+                double scale = (double)sdy[m * lds + nb] * (double)sw[nb * KB + k / ORC_BLOCK];
+#endif
+                acc += scale * b;
+                lsum += fabs(scale) * babs;
+            }
+            dx[r * K + k] = acc;
+            L[r * K + k] = lsum;
+        }
+    }
+    free(dyd);
+}
+
+/* wgrad: dW[n,k] = sum_mb sdy[mb,n] * sx[mb,k] * B_mb[n,k],
+ *   B_mb[n,k] = sum_{m in block mb} dec(dyq[m,n]) * dec(xq[m,k]),
+ * exact fp64 per block (a block holds at most 128 products).  dyq [M, N]
+ * row stride ldd, sdy [ceil(M/128), N]; xq [M, K] row stride ldx,
+ * sx [ceil(M/128), K] (both from orc_act_quant_cols); the last block of
+ * tokens may be ragged.  dw and L are [N, K]. */
+void orc_gemm_wgrad(const uint8_t* dyq, int64_t ldd, const float* sdy, const uint8_t* xq, int64_t ldx,
+                    const float* sx, int64_t M, int64_t N, int64_t K, double* dw, double* L) {
+    int64_t MB = (M + ORC_BLOCK - 1) / ORC_BLOCK;
+#if ORC_MUTANT == 15
+    if (M % ORC_BLOCK) MB -= 1; /* mutant: a ragged last block of tokens dropped */
+#endif
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t k = 0; k < K; k++) {
+            double acc = 0.0, lsum = 0.0;
+            for (int64_t mb = 0; mb < MB; mb++) {
+                int64_t m0 = mb * ORC_BLOCK, m1 = m0 + ORC_BLOCK < M ? m0 + ORC_BLOCK : M;
+                double b = 0.0, babs = 0.0;
+                for (int64_t m = m0; m < m1; m++) {
+                    double p = orc_e4m3_decode(dyq[m * ldd + n]) * orc_e4m3_decode(xq[m * ldx + k]);
+                    b += p;
+                    babs += fabs(p);
+                }
+                double scale = (double)sdy[mb * N + n] * (double)sx[mb * K + k];
+                acc += scale * b;
+                lsum += fabs(scale) * babs;
+            }
+            dw[n * K + k] = acc;
+            L[n * K + k] = lsum;
+        }
+    }
+}
+
 int orc_mutant_id(void) { return ORC_MUTANT; }

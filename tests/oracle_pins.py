@@ -573,6 +573,98 @@ def pin_moe_route(o):
     assert off[11] == off[12]
 
 
+def pin_act_quant_cols(o):
+    """128x1 groups along the rows: bit for bit act_quant of the transpose
+    (when M is a multiple of 128), a ragged last block equal to zero-padding
+    it, and a power-of-two closed form (a column whose largest magnitude is
+    448 * 2^a has scale 2^a and codes equal to x / 2^a)."""
+    rng = np.random.default_rng(27)
+    x = synth.activations(rng, 256, 384, n_outlier=3, outlier_scale=20.0)
+    xq, sx = o.act_quant_cols(x)
+    xqt, sxt = o.act_quant(np.ascontiguousarray(x.T))
+    assert np.array_equal(xq, xqt.T)
+    assert np.array_equal(sx.view(np.uint32), np.ascontiguousarray(sxt[:, :2].T).view(np.uint32))
+    xr = synth.activations(rng, 200, 128)
+    xqr, sxr = o.act_quant_cols(xr)
+    pad = np.concatenate([xr, np.zeros((56, 128), dtype=np.uint16)])
+    xqp, sxp = o.act_quant_cols(pad)
+    assert np.array_equal(xqr, xqp[:200]) and np.array_equal(sxr.view(np.uint32), sxp.view(np.uint32))
+    # closed form: column values are e4m3 codes times 2^-3, with 448 present
+    v = e4m3_values()
+    codes = _pos_codes_with_max(rng, 128)
+    col = (v[codes] * 2.0 ** -3).astype(np.float32)
+    xc = bf16_bits(np.stack([col, col * 0], axis=1))
+    qc, sc = o.act_quant_cols(xc)
+    assert sc[0, 0] == np.float32(2.0 ** -3) and np.array_equal(qc[:, 0], codes)
+    assert sc[0, 1] == 0.0
+
+
+def _exact_dgrad(dyq, sdy, wq, sw, m, k):
+    vals = e4m3_values()
+    tot = Fraction(0)
+    for nb in range(dyq.shape[1] // 128):
+        bsum = sum(Fraction(float(vals[dyq[m, n]])) * Fraction(float(vals[wq[n, k]]))
+                   for n in range(nb * 128, (nb + 1) * 128))
+        tot += Fraction(float(sdy[m, nb])) * Fraction(float(sw[nb, k // 128])) * bsum
+    return tot
+
+
+def pin_gemm_dgrad(o):
+    """dX = dY W: bit for bit the forward GEMM with the weight and its block
+    grid transposed (W^T is [K, N] with 128x128 blocks (kb, nb)), the
+    dequantise-then-matmul form, and exact rationals on one element."""
+    rng = np.random.default_rng(28)
+    M, N, K = 40, 256, 384
+    dy = synth.activations(rng, M, N, n_outlier=2, outlier_scale=10.0)
+    w = synth.normal_bf16(rng, (N, K), 0.02)
+    dyq, sdy = o.act_quant(dy)
+    wq, sw = o.weight_quant(w)
+    dx, L = o.gemm_dgrad(dyq, sdy, wq, sw)
+    y_t, L_t = o.gemm(dyq, sdy, np.ascontiguousarray(wq.T), np.ascontiguousarray(sw.T))
+    assert np.array_equal(dx, y_t) and np.array_equal(L, L_t)
+    v = e4m3_values()
+    dyd = v[dyq] * np.repeat(sdy[:, : N // 128].astype(np.float64), 128, 1)
+    wd = v[wq] * np.repeat(np.repeat(sw.astype(np.float64), 128, 0), 128, 1)
+    assert np.all(np.abs(dx - dyd @ wd) <= 1e-12 * L + 1e-300)
+    m, k = 7, 300
+    ex = _exact_dgrad(dyq, sdy, wq, sw, m, k)
+    assert abs(Fraction(float(dx[m, k])) - ex) <= Fraction(2) ** -45 * Fraction(float(L[m, k]))
+
+
+def pin_gemm_wgrad(o):
+    """dW = dY^T X over the tokens with 128x1 groups: the dequantise-then-
+    matmul form (numpy), exact rationals on one element, a ragged last block
+    of tokens (200 = 128 + 72) that matters, and a rank-1 closed form: dY all
+    1.75 = 448 * 2^-8 and X all 3.5 = 448 * 2^-7 (power-of-two scales, code
+    448) give dW = 6.125 M exactly."""
+    rng = np.random.default_rng(29)
+    M, N, K = 200, 64, 96
+    dy = synth.activations(rng, M, N, n_outlier=2, outlier_scale=10.0)
+    x = synth.activations(rng, M, K)
+    dyq, sdy = o.act_quant_cols(dy)
+    xq, sx = o.act_quant_cols(x)
+    dw, L = o.gemm_wgrad(dyq, sdy, xq, sx)
+    v = e4m3_values()
+    dyd = v[dyq] * np.repeat(sdy.astype(np.float64), 128, 0)[:M]
+    xd = v[xq] * np.repeat(sx.astype(np.float64), 128, 0)[:M]
+    assert np.all(np.abs(dw - dyd.T @ xd) <= 1e-12 * L + 1e-300)
+    # the last 72 tokens contribute
+    assert np.abs(dyd[128:].T @ xd[128:]).max() > 1e-3
+    n, k = 5, 77
+    ex = Fraction(0)
+    for mb in range(2):
+        bsum = sum(Fraction(float(v[dyq[m, n]])) * Fraction(float(v[xq[m, k]])) for m in range(mb * 128, min(M, mb * 128 + 128)))
+        ex += Fraction(float(sdy[mb, n])) * Fraction(float(sx[mb, k])) * bsum
+    assert abs(Fraction(float(dw[n, k])) - ex) <= Fraction(2) ** -45 * Fraction(float(L[n, k]))
+    a = bf16_bits(np.full((M, 3), 1.75, dtype=np.float32))
+    b = bf16_bits(np.full((M, 2), 3.5, dtype=np.float32))
+    q1, s1 = o.act_quant_cols(a)
+    q2, s2 = o.act_quant_cols(b)
+    assert np.all(s1 == np.float32(2.0 ** -8)) and np.all(s2 == np.float32(2.0 ** -7))
+    dw1, _ = o.gemm_wgrad(q1, s1, q2, s2)
+    assert np.array_equal(dw1, np.full((3, 2), 6.125 * M))
+
+
 ALL_PINS = [
     pin_codec_midpoints,
     pin_act_quant_rank1,
@@ -593,4 +685,7 @@ ALL_PINS = [
     pin_moe_combine,
     pin_moe_gate,
     pin_moe_route,
+    pin_act_quant_cols,
+    pin_gemm_dgrad,
+    pin_gemm_wgrad,
 ]
