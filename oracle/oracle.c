@@ -19,7 +19,8 @@
  *   infinities, S.1111.111 = NaN, largest finite 448); the pages only say
  *   "float8 e4m3".
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent (the later functions state their own
+ * readings beside their code):
  *   R1 e4m3 = OCP E4M3 ("fn"): saturating encode, max 448.
  *   R2 scale s = amax / 448 in fp32 with IEEE round-to-nearest division, and
  *      the stored scale is the dequantisation multiplier (w ~= dec(q) * s).
