@@ -20,6 +20,16 @@ def test_exports_every_declared_symbol():
         assert required in names
 
 
+def test_binding_covers_the_header():
+    """Every call the header declares has a typed ctypes signature and a
+    Python function of the same name, and the binding declares nothing the
+    header does not."""
+    declared = set(fp8bs.declared_symbols())
+    assert declared == set(fp8bs._SIGS)
+    for n in declared:
+        assert callable(getattr(fp8bs, n)), n
+
+
 def test_status_strings_and_version():
     for s in range(7):
         assert fp8bs.fp8bs_status_string(s).startswith("FP8BS")
