@@ -53,6 +53,7 @@ def load(mutant: int = 0) -> ctypes.CDLL:
                              ctypes.c_int32, ctypes.c_double, _P, _P, _P],
             "orc_moe_route": [_P, _P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P],
             "orc_act_quant_cols": [_P, _I64, _I64, _I64, _P, _I64, _P],
+            "orc_act_quant_pow2": [_P, _I64, _I64, _I64, _P, _I64, _P, _I64],
             "orc_gemm_dgrad_rows": [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P],
             "orc_gemm_wgrad": [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _P, _P],
         }.items():
@@ -249,6 +250,16 @@ class Oracle:
         self.lib.orc_moe_route(_ptr(ids), _ptr(w), T, k, n_experts, _ptr(off), _ptr(tor), _ptr(rot), _ptr(wor))
         return off, tor, rot, wor
 
+
+    def act_quant_pow2(self, x_bits, lds: int | None = None):
+        """act_quant with power-of-two (UE8M0-style) scales, rounded up."""
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        M, K = x.shape
+        lds = lds or max(1, K // 128)
+        xq = np.empty((M, K), dtype=np.uint8)
+        sx = np.zeros((M, lds), dtype=np.float32)
+        self.lib.orc_act_quant_pow2(_ptr(x), M, K, K, _ptr(xq), K, _ptr(sx), lds)
+        return xq, sx
 
     def act_quant_cols(self, x_bits):
         """x [M, K] bf16 bits -> (xq [M, K] u8, sx [ceil(M/128), K] fp32):

@@ -665,6 +665,43 @@ def pin_gemm_wgrad(o):
     assert np.array_equal(dw1, np.full((3, 2), 6.125 * M))
 
 
+def pin_act_quant_pow2(o):
+    """Power-of-two scales: against exact rationals, s is a power of two with
+    s/2 < amax/448 <= s; the codes are ml_dtypes' round-to-nearest-even e4m3
+    of the exact quotient and never exceed 448; a group whose amax is
+    448 * 2^a gets the same scale and codes as the fp32-scale path; all-zero
+    groups get s = 0."""
+    rng = np.random.default_rng(30)
+    x = synth.activations(rng, 64, 512, n_outlier=5, outlier_scale=30.0)
+    x[3, 128:256] = 0
+    xq, sx = o.act_quant_pow2(x)
+    xf = f32_of_bf16(x).astype(np.float64)
+    v = e4m3_values()
+    for m in range(64):
+        for g in range(4):
+            grp = xf[m, 128 * g:128 * (g + 1)]
+            amax = np.abs(grp).max()
+            s = float(sx[m, g])
+            if amax == 0:
+                assert s == 0.0 and not (xq[m, 128 * g:128 * (g + 1)] & 0x7F).any()
+                continue
+            mant, _ = np.frexp(s)
+            assert mant == 0.5, "scale is not a power of two"
+            ratio = Fraction(amax) / 448
+            assert Fraction(s) / 2 < ratio <= Fraction(s)
+            q = grp / s                                     # exact: power-of-two scaling
+            assert np.abs(q).max() <= 448
+            assert np.array_equal(xq[m, 128 * g:128 * (g + 1)], e4m3_code_lib(q))
+            assert np.abs(v[xq[m, 128 * g:128 * (g + 1)]]).max() <= 448
+    # amax = 448 * 2^a: the same as the fp32-scale path
+    codes = _pos_codes_with_max(rng, 128)
+    row = (v[codes] * 2.0 ** -5).astype(np.float32)
+    xb = bf16_bits(row[None, :])
+    q1, s1 = o.act_quant_pow2(xb)
+    q2, s2 = o.act_quant(xb)
+    assert s1[0, 0] == s2[0, 0] == np.float32(2.0 ** -5) and np.array_equal(q1, q2)
+
+
 ALL_PINS = [
     pin_codec_midpoints,
     pin_act_quant_rank1,
@@ -688,4 +725,5 @@ ALL_PINS = [
     pin_act_quant_cols,
     pin_gemm_dgrad,
     pin_gemm_wgrad,
+    pin_act_quant_pow2,
 ]

@@ -15,6 +15,7 @@
  13 column quantisation leaving a block's last row out of the amax
  14 dgrad reading the weight's block grid as if stored transposed
  15 wgrad dropping a ragged last block of tokens
+ 16 power-of-two scales rounded down (the top codes saturate)
 """
 import pytest
 
@@ -22,7 +23,7 @@ from oracle import Oracle
 from oracle_pins import ALL_PINS
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16])
 def test_mutant_is_caught(mutant):
     o = Oracle(mutant)
     assert o.lib.orc_mutant_id() == mutant
