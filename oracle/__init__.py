@@ -18,16 +18,18 @@ from . import build as _build
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _lock = threading.Lock()
-_libs: dict[int, ctypes.CDLL] = {}
+_libs: dict[tuple[int, bool], ctypes.CDLL] = {}
 
 
-def load(mutant: int = 0) -> ctypes.CDLL:
+def load(mutant: int = 0, omp: bool = False) -> ctypes.CDLL:
     """Build (if needed) and load the oracle library; mutant>0 loads a copy
-    with a deliberately planted mistake (used only by the mutant tests)."""
+    with a deliberately planted mistake (used only by the mutant tests);
+    omp=True loads the same source built with OpenMP (the GEMM's rows spread
+    over the host cores; used by the full-size parity tests)."""
     with _lock:
-        if mutant in _libs:
-            return _libs[mutant]
-        lib = ctypes.CDLL(_build.build(mutant))
+        if (mutant, omp) in _libs:
+            return _libs[(mutant, omp)]
+        lib = ctypes.CDLL(_build.build(mutant, omp=omp))
         lib.orc_e4m3_decode.restype = ctypes.c_double
         lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.orc_e4m3_encode.restype = ctypes.c_uint8
@@ -61,7 +63,7 @@ def load(mutant: int = 0) -> ctypes.CDLL:
             fn.restype = None
             fn.argtypes = args
         lib.orc_mutant_id.restype = ctypes.c_int
-        _libs[mutant] = lib
+        _libs[(mutant, omp)] = lib
         return lib
 
 
@@ -73,8 +75,8 @@ def _ptr(a: np.ndarray) -> int:
 class Oracle:
     """numpy front end of one oracle build (mutant=0 is the real one)."""
 
-    def __init__(self, mutant: int = 0):
-        self.lib = load(mutant)
+    def __init__(self, mutant: int = 0, threads: bool = False):
+        self.lib = load(mutant, omp=threads)
         self.mutant = mutant
 
     # -- codec -----------------------------------------------------------

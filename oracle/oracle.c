@@ -266,45 +266,66 @@ void orc_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K
  * product of two fp32 numbers is exact in fp64.  Also returns
  *   L[m,n] = sum_k |dec(xq[m,k]) sx[m,k/128]| * |dec(wq[n,k]) sw[n/128,k/128]|
  * used by the error bound.  Only the rows listed in `rows` (nrows of them)
- * are computed; y and L are [nrows, N] row-major. */
+ * are computed; y and L are [nrows, N] row-major.
+ * Codes are decoded through a table of the 256 decoded values (dec is exact,
+ * so the table changes no value).  Built with -fopenmp (liboracle_omp.so, for full-size
+ * parity checks) the listed rows are shared out between threads; each output
+ * element is still computed by one thread in the order written here. */
 void orc_gemm_rows(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds,
                    const uint8_t* wq, const float* sw,
                    int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
                    double* y, double* L) {
     int64_t KB = K / ORC_BLOCK;
-    double* xd = (double*)malloc(sizeof(double) * (size_t)K);
-    for (int64_t r = 0; r < nrows; r++) {
-        int64_t m = rows[r];
-        for (int64_t k = 0; k < K; k++)
-            xd[k] = orc_e4m3_decode(xq[m * ldq + k]);
-        for (int64_t n = 0; n < N; n++) {
-            const uint8_t* wrow = wq + n * K;
-            double acc = 0.0, lsum = 0.0;
+    double dec[256];
+    for (int c = 0; c < 256; c++)
+        dec[c] = orc_e4m3_decode((uint8_t)c);
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        double* xd = (double*)malloc(sizeof(double) * (size_t)K);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t r = 0; r < nrows; r++) {
+            int64_t m = rows[r];
+            for (int64_t k = 0; k < K; k++)
+                xd[k] = dec[xq[m * ldq + k]];
+            for (int64_t n = 0; n < N; n++) {
+                const uint8_t* wrow = wq + n * K;
+                double acc = 0.0, lsum = 0.0;
 #if ORC_MUTANT == 5
-            int64_t kb_end = KB - 1; /* mutant: last K chunk dropped */
+                int64_t kb_end = KB - 1; /* mutant: last K chunk dropped */
 #else
-            int64_t kb_end = KB;
+                int64_t kb_end = KB;
 #endif
-            for (int64_t kb = 0; kb < kb_end; kb++) {
-                double b = 0.0, babs = 0.0;
-                for (int64_t k = kb * ORC_BLOCK; k < (kb + 1) * ORC_BLOCK; k++) {
-                    double p = xd[k] * orc_e4m3_decode(wrow[k]);
-                    b += p;
-                    babs += fabs(p);
-                }
+                for (int64_t kb = 0; kb < kb_end; kb++) {
+                    double b = 0.0, babs = 0.0;
+                    /* b and babs are exact whatever the order of the terms
+                     * (see above), so the threaded build may split these two
+                     * sums across vector lanes without changing them. */
+#ifdef _OPENMP
+#pragma omp simd reduction(+ : b, babs)
+#endif
+                    for (int64_t k = kb * ORC_BLOCK; k < (kb + 1) * ORC_BLOCK; k++) {
+                        double p = xd[k] * dec[wrow[k]];
+                        b += p;
+                        babs += fabs(p);
+                    }
 #if ORC_MUTANT == 4
-                double scale = (double)sx[m * lds + kb] * (double)sw[kb * ((N + 127) / 128) + n / ORC_BLOCK]; /* mutant: scale grid transposed */
+                    double scale = (double)sx[m * lds + kb] * (double)sw[kb * ((N + 127) / 128) + n / ORC_BLOCK]; /* mutant: scale grid transposed */
 #else
-                double scale = (double)sx[m * lds + kb] * (double)sw[(n / ORC_BLOCK) * KB + kb];
+                    double scale = (double)sx[m * lds + kb] * (double)sw[(n / ORC_BLOCK) * KB + kb];
 #endif
-                acc += scale * b;
-                lsum += fabs(scale) * babs;
+                    acc += scale * b;
+                    lsum += fabs(scale) * babs;
+                }
+                y[r * N + n] = acc;
+                L[r * N + n] = lsum;
             }
-            y[r * N + n] = acc;
-            L[r * N + n] = lsum;
         }
+        free(xd);
     }
-    free(xd);
 }
 
 /* bias: the pages' linear() adds the bias after fp8_gemm ("DeepSeek-V3"
@@ -338,22 +359,39 @@ void orc_swiglu(const double* a, const double* b, int64_t n, double* h) {
  * offsets[g] .. offsets[g+1]-1 of xq/sx, with expert weights
  * wq + g*N*K (row-major [N, K]) and scales sw + g*ceil(N/128)*(K/128).
  * Computes the listed global rows (each must lie in some expert's range);
- * rows outside every range are left untouched. */
+ * rows outside every range are left untouched.  The listed rows of one
+ * expert go to orc_gemm_rows together, so each expert's weight is decoded
+ * once. */
 void orc_grouped_gemm_rows(const uint8_t* xq, int64_t ldq, const float* sx, int64_t lds,
                            const uint8_t* wq, const float* sw, const int32_t* offsets, int32_t G,
                            int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
                            double* y, double* L) {
     int64_t NB = (N + ORC_BLOCK - 1) / ORC_BLOCK, KB = K / ORC_BLOCK;
-    for (int64_t r = 0; r < nrows; r++) {
-        int64_t m = rows[r];
-        for (int32_t g = 0; g < G; g++) {
-            if (m >= offsets[g] && m < offsets[g + 1]) {
-                orc_gemm_rows(xq, ldq, sx, lds, wq + (int64_t)g * N * K, sw + (int64_t)g * NB * KB,
-                              N, K, &m, 1, y + r * N, L + r * N);
-                break;
+    int64_t* sel = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nrows > 0 ? nrows : 1));
+    int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nrows > 0 ? nrows : 1));
+    for (int32_t g = 0; g < G; g++) {
+        int64_t n_sel = 0;
+        for (int64_t r = 0; r < nrows; r++)
+            if (rows[r] >= offsets[g] && rows[r] < offsets[g + 1]) {
+                sel[n_sel] = rows[r];
+                pos[n_sel] = r;
+                n_sel++;
             }
+        if (n_sel == 0)
+            continue;
+        double* yg = (double*)malloc(sizeof(double) * (size_t)n_sel * (size_t)N);
+        double* lg = (double*)malloc(sizeof(double) * (size_t)n_sel * (size_t)N);
+        orc_gemm_rows(xq, ldq, sx, lds, wq + (int64_t)g * N * K, sw + (int64_t)g * NB * KB,
+                      N, K, sel, n_sel, yg, lg);
+        for (int64_t i = 0; i < n_sel; i++) {
+            memcpy(y + pos[i] * N, yg + i * N, sizeof(double) * (size_t)N);
+            memcpy(L + pos[i] * N, lg + i * N, sizeof(double) * (size_t)N);
         }
+        free(yg);
+        free(lg);
     }
+    free(sel);
+    free(pos);
 }
 
 /* MoE dispatch: the routed expert computation runs on the token rows

@@ -19,3 +19,12 @@ def pytest_configure(config):
 def orc():
     from oracle import Oracle
     return Oracle()
+
+
+@pytest.fixture(scope="session")
+def orc_mt():
+    """The same oracle source built with OpenMP: the full-size parity cases
+    compare every output element, which the single-threaded build cannot
+    finish in the test's time."""
+    from oracle import Oracle
+    return Oracle(threads=True)
