@@ -142,6 +142,8 @@ size_t fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     return gemm_workspace_size(M, N, K, d);
 }
 
+size_t fp8bs_grouped_gemm_workspace_size(int32_t, int64_t, int64_t) { return 0; }
+
 fp8bs_status fp8bs_grouped_gemm(const uint8_t* xq, const float* sx, int64_t lds, const uint8_t* wq,
                                 const float* sw, const int32_t* offsets_dev, int32_t G, int64_t total_M,
                                 int64_t N, int64_t K, uint16_t* y, int64_t ldy, fp8bs_stream_t stream) {

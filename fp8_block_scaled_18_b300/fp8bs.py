@@ -36,6 +36,7 @@ _SIGS = {
     "fp8bs_gemm_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fp8bs_gemm_noalloc": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm": (_ST, [_P, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
+    "fp8bs_grouped_gemm_workspace_size": (_SZ, [_I32, _I64, _I64]),
     "fp8bs_grouped_gemm_swiglu": (_ST, [_P, _P, _I64, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P,
                                         _I64, _P, _I64, _P]),
     "fp8bs_moe_dispatch": (_ST, [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
@@ -227,6 +228,10 @@ def fp8bs_gemm_noalloc(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw:
                                   _dev(sw, torch.float32, "sw"), M, N, K, _bf16_ptr(y, "y"),
                                   _rows_stride(y, "y"), _stream(stream)), "fp8bs_gemm_noalloc")
     return y
+
+
+def fp8bs_grouped_gemm_workspace_size(G: int, N: int, K: int) -> int:
+    return lib.fp8bs_grouped_gemm_workspace_size(G, N, K)
 
 
 def fp8bs_grouped_gemm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,

@@ -37,7 +37,9 @@
  *     the device status word and reported by fp8bs_sync_status().
  *   - M (or total rows) == 0 is a no-op returning FP8BS_OK.
  *   - Thread-safe: calls keep no mutable host state except per-device caches
- *     filled once under a lock.
+ *     filled once under a lock.  Those caches (device symbol addresses, kernel
+ *     attributes) belong to the device's context: do not call the library
+ *     again in a process that reset a device with cudaDeviceReset.
  */
 #ifndef FP8BS_H
 #define FP8BS_H
@@ -152,6 +154,12 @@ fp8bs_status fp8bs_grouped_gemm(const uint8_t* xq, const float* sx, int64_t lds,
                                 int64_t N, int64_t K, uint16_t* y, int64_t ldy,
                                 fp8bs_stream_t stream);
 
+/* Scratch bytes fp8bs_grouped_gemm needs for G experts of [N, K]: always 0.
+ * Its per-expert tile table is built inside each CTA's shared memory from
+ * offsets_dev, so the call takes no workspace argument; this size query
+ * exists for callers written against a grouped GEMM that takes one. */
+size_t fp8bs_grouped_gemm_workspace_size(int32_t G, int64_t N, int64_t K);
+
 /* fp8_gemm for callers that cannot allocate device memory -- code running
  * inside an allocator's or memory pool's own callback, plugin hosts that pass
  * a library only its input and output buffers, and latency-critical paths
@@ -167,7 +175,15 @@ fp8bs_status fp8bs_grouped_gemm(const uint8_t* xq, const float* sx, int64_t lds,
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  All
  * calls on a device share the array: calls whose kernels overlap on the GPU
- * race and must be serialised by the caller.  Allocates nothing. */
+ * race and must be serialised by the caller.  Allocates nothing.
+ * On 148 SMs the largest scratch any shape's plan asks for is
+ * num_sms * 128 * 160 * 4 bytes (12.1 MB: split-K runs with 160-column tiles
+ * and at most one (tile, split) piece per SM), so the 32 MiB array serves
+ * every valid shape on devices of up to 409 SMs.
+ * Like the library's other per-device set-up (the status word's address,
+ * kernel attributes), the looked-up address belongs to the device's current
+ * context: after cudaDeviceReset the library must not be called again in
+ * that process. */
 #define FP8BS_NOALLOC_SCRATCH_BYTES (32u << 20)
 fp8bs_status fp8bs_gemm_noalloc(const uint8_t* xq, const float* sx, int64_t lds,
                                 const uint8_t* wq, const float* sw,

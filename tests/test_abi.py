@@ -116,6 +116,15 @@ def test_grouped_swiglu_validation():
     assert f(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                  # sw3 alignment
 
 
+def test_gemm_noalloc_validation():
+    """The no-allocation GEMM rejects bad arguments before any CUDA call."""
+    f = lib.fp8bs_gemm_noalloc
+    assert f(A, A, 4, A, A, 4, 8, 200, A, 8, None) == fp8bs.FP8BS_ERR_UNSUPPORTED   # K % 128
+    assert f(A, A, 4, A, A, -1, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert f(A, A, 4, A, A, 0, 8, 128, A, 8, None) == fp8bs.FP8BS_OK                # empty: a no-op
+    assert f(A, A, 4, None, A, 4, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+
+
 def test_grouped_validation():
     gg = lib.fp8bs_grouped_gemm
     assert gg(A, A, 4, A, A, None, 4, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG
@@ -124,6 +133,8 @@ def test_grouped_validation():
     assert gg(A, A, 4, A, A, A, 2000, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
     assert gg(A, A, 4, A, A, A + 2, 4, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_MISALIGNED
     assert gg(A, A, 4, A, A, A, 4, 16, 8, 136, A, 8, None) == fp8bs.FP8BS_ERR_UNSUPPORTED
+    # the tile table lives in shared memory: no scratch for any shape
+    assert lib.fp8bs_grouped_gemm_workspace_size(256, 2048, 7168) == 0
 
 
 def test_moe_dispatch_validation():

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from fp8_block_scaled_18_b300 import synth
-from gpu_util import assert_gemm_close, dev, dev_bf16, host, sample_rows
+from gpu_util import assert_gemm_close, dev, dev_bf16, host
 from oracle import gemm_tolerance
 
 pytestmark = pytest.mark.gpu
@@ -34,11 +34,6 @@ def _operands(orc, M, N, K, seed):
     xq, sx = orc.act_quant(x, lds=max(4, (K // 128 + 3) // 4 * 4))
     wq, sw = orc.weight_quant(w)
     return xq, sx, wq, sw, bias
-
-
-def _rows(M):
-    edge = sorted({r for t in range(0, M, 128) for r in (t, min(t + 127, M - 1))})
-    return np.union1d(np.array(edge, dtype=np.int64), sample_rows(M, 48, seed=M))
 
 
 def _check_fp8_out(yq, sy, y_ref, L, what):
@@ -67,14 +62,13 @@ WIDTH_SHAPES = [(4000, 1000, 384), (4000, 700, 384), (4000, 1200, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", WIDTH_SHAPES + [(5, 130, 256), (300, 576, 640)])
-def test_fused_bias(F, orc, M, N, K):
+def test_fused_bias(F, orc, orc_mt, M, N, K):
     xq, sx, wq, sw, bias = _operands(orc, M, N, K, seed=M + N)
     y, yq, sy = F.fp8bs_gemm_fused(dev(xq), dev(sx), dev(wq), dev(sw), bias=dev_bf16(bias))
     assert yq is None and sy is None
     assert F.fp8bs_sync_status() == 0
-    rows = _rows(M)
-    y_ref, L = orc.gemm(xq, sx, wq, sw, rows=rows, bias=bias)
-    assert_gemm_close(host(y)[rows], y_ref, L, f"fused bias {M}x{N}x{K}")
+    y_ref, L = orc_mt.gemm(xq, sx, wq, sw, bias=bias)
+    assert_gemm_close(host(y), y_ref, L, f"fused bias {M}x{N}x{K}")
 
 
 def test_fused_without_bias_equals_gemm(F, orc):
@@ -90,7 +84,7 @@ def test_fused_without_bias_equals_gemm(F, orc):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (129, 256, 384), (700, 1536, 1024), (4000, 1024, 256)])
-def test_fused_fp8_out(F, orc, M, N, K):
+def test_fused_fp8_out(F, orc, orc_mt, M, N, K):
     xq, sx, wq, sw, bias = _operands(orc, M, N, K, seed=2 * M + N)
     a = dev(xq), dev(sx), dev(wq), dev(sw)
     y, yq, sy = F.fp8bs_gemm_fused(*a, bias=dev_bf16(bias), want_fp8=True)
@@ -104,17 +98,16 @@ def test_fused_fp8_out(F, orc, M, N, K):
     # without y the fp8 output is the same
     assert np.array_equal(host(yq_only), yq_h)
     assert np.array_equal(host(sy_only).view(np.uint32), sy_h.view(np.uint32))
-    # against the oracle
-    rows = _rows(M)
-    y_ref, L = orc.gemm(xq, sx, wq, sw, rows=rows, bias=bias)
-    assert_gemm_close(host(y)[rows], y_ref, L, f"fused y {M}x{N}x{K}")
-    _check_fp8_out(yq_h[rows], sy_h[rows], y_ref, L, f"fused fp8 {M}x{N}x{K}")
+    # against the oracle, every element
+    y_ref, L = orc_mt.gemm(xq, sx, wq, sw, bias=bias)
+    assert_gemm_close(host(y), y_ref, L, f"fused y {M}x{N}x{K}")
+    _check_fp8_out(yq_h, sy_h, y_ref, L, f"fused fp8 {M}x{N}x{K}")
 
 
-def test_fused_q_down_full(F, orc):
+def test_fused_q_down_full(F, orc, orc_mt):
     """The q down-projection at M = 4096 (N = 1536 = 12 output groups):
     device pipeline (weight_quant, act_quant, fused GEMM with bias and fp8
-    output) against the oracle's pipeline on sampled rows."""
+    output) against the oracle's pipeline on every element."""
     case = synth.q_down(4096)
     M, N, K = case.shape
     rng = np.random.default_rng(31)
@@ -123,9 +116,8 @@ def test_fused_q_down_full(F, orc):
     xq, sx = F.fp8bs_act_quant(dev_bf16(case.x))
     y, yq, sy = F.fp8bs_gemm_fused(xq, sx, wq, sw, bias=dev_bf16(bias), want_fp8=True)
     assert F.fp8bs_sync_status() == 0
-    rows = sample_rows(M, 24, seed=4)
-    xq_o, sx_o = orc.act_quant(case.x[rows])
+    xq_o, sx_o = orc.act_quant(case.x)
     wq_o, sw_o = orc.weight_quant(case.w)
-    y_ref, L = orc.gemm(xq_o, sx_o, wq_o, sw_o, bias=bias)
-    assert_gemm_close(host(y)[rows], y_ref, L, "q_down fused y")
-    _check_fp8_out(host(yq)[rows], host(sy)[rows], y_ref, L, "q_down fused fp8")
+    y_ref, L = orc_mt.gemm(xq_o, sx_o, wq_o, sw_o, bias=bias)
+    assert_gemm_close(host(y), y_ref, L, "q_down fused y")
+    _check_fp8_out(host(yq), host(sy), y_ref, L, "q_down fused fp8")

@@ -55,17 +55,11 @@ def test_noalloc_gemm_matches_workspace_gemm_two_calls(orc):
         assert F.fp8bs_sync_status() == F.FP8BS_OK
 
         y_ref, L = orc.gemm(xq_h, sx_h, wq_h, sw_h)
-        # against the existing entry point, with the bound the GEMM tests use
+        # the same plan and the same in-order split-K reduction as the
+        # existing entry point: identical bits
+        assert torch.equal(y_new.view(torch.int16), y_api.view(torch.int16)), f"noalloc vs fp8bs_gemm M={M}"
+        # and within the bound the GEMM tests use
         assert_gemm_close(host(y_new), bf16_to_f64(host(y_api)), L, f"noalloc vs fp8bs_gemm M={M}")
         # and both against the oracle
         assert_gemm_close(host(y_new), y_ref, L, f"noalloc vs oracle M={M}")
         assert_gemm_close(host(y_api), y_ref, L, f"fp8bs_gemm vs oracle M={M}")
-
-
-def test_noalloc_rejects_bad_arguments():
-    if not torch.cuda.is_available():
-        pytest.skip("no GPU")
-    from fp8_block_scaled_18_b300 import fp8bs as F
-    A = 0x10000
-    assert F.lib.fp8bs_gemm_noalloc(A, A, 4, A, A, 4, 8, 200, A, 8, None) == F.FP8BS_ERR_UNSUPPORTED
-    assert F.lib.fp8bs_gemm_noalloc(A, A, 4, A, A, -1, 8, 128, A, 8, None) == F.FP8BS_ERR_INVALID_ARG
