@@ -1,17 +1,23 @@
 #!/usr/bin/env python3
 """Benchmark of the FP8 (e4m3) block-scaled linear layer on B300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload kv_down]
-                    [--impl ours|reference] [--no-cpu-baseline]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload large_square]
+                    [--impl ours|reference] [--no-cpu-baseline] [--no-configs]
+                    [--profile-steps P]
 
 One step = one pass of the whole path over one batch of synthetic input:
-dense workloads run weight_quant(W), act_quant(X), fp8_gemm and
-weight_dequant(Wq) (q_down_m<M>_fused: the GEMM with bias and FP8 output);
+dense workloads run act_quant(X) and fp8_gemm with W quantised once before
+timing (the large square adds weight_dequant(Wq); q_down_m<M>_fused runs the
+GEMM with bias and FP8 output);
 moe runs act_quant over the expert-grouped token rows and the grouped
 fp8_gemm, moe_swiglu the grouped w1|w3 stage with SwiGLU and FP8 h, and
 moe_layer the whole routed layer with its router (expert weights quantised
-once, before timing).  The default workload is the MLA KV down-projection
-(X [4096,7168] x W [576,7168]).
+once, before timing).  The default workload is the large square
+(X [16384,7168] Student-t(3) x W [7168,7168]: act_quant + fp8_gemm +
+weight_dequant), the largest configuration; the line also carries, under
+"configs", each kernel's roofline row for all five configurations (tiny, the
+KV down-projection, the Q down-projection sweep, the large square and the MoE
+grouped GEMM).
 
 Timing: W warm-up steps, then exactly K steps captured in CUDA graphs and
 replayed between CUDA events, bracketed by a barrier and a synchronize; the
@@ -57,10 +63,14 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="kv_down",
-                    help="kv_down | tiny | q_down_m<M>[_fused] | large_square | moe | moe_swiglu | moe_layer")
+    ap.add_argument("--workload", default="large_square",
+                    help="large_square | kv_down | tiny | q_down_m<M>[_fused] | moe | moe_swiglu | moe_layer | moe_router")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-kernel table of the five configurations")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many eager steps of the workload and exit (for a profiler); nothing is timed")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--soak", type=float, default=1.0,
                     help="seconds of untimed steps before the warm-up, so the clock record sees sustained load")
@@ -194,21 +204,26 @@ class ClockSampler:
 # ---------------------------------------------------------------- workloads
 
 class DenseWork:
-    """weight_quant(W) -> act_quant(X) -> fp8_gemm -> weight_dequant(Wq).
-    fused: the GEMM is fp8bs_gemm_fused with a bias and the output re-quantised
-    to FP8 (1x128 groups, ready for the next FP8 GEMM) instead of bf16."""
+    """act_quant(X) -> fp8_gemm (-> weight_dequant(Wq) for the large square),
+    with W quantised once before timing (weight_quant is timed on its own as
+    a table row).  fused: the GEMM is fp8bs_gemm_fused with a bias and the
+    output re-quantised to FP8 (1x128 groups, ready for the next FP8 GEMM)
+    instead of bf16."""
 
-    def __init__(self, case, device, fused=False):
+    def __init__(self, case, device, fused=False, min_sets=1):
         import torch
         from fp8_block_scaled_18_b300 import fp8bs as F
         self.F = F
         self.case = case
+        self.device = device
         self.M, self.N, self.K = case.shape
         M, N, K = self.M, self.N, self.K
         self.x_host = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16)
         self.w_host = torch.from_numpy(case.w.view(np.int16)).view(torch.bfloat16)
+        self.dequant = case.name == "large_square"  # the configuration's own extra step
         per_set = 2 * M * K + 2 * N * K + M * K + 4 * M * (K // 128) + N * K + 2 * M * N + 2 * N * K
         self.R = max(1, min(8, math.ceil(2 * L2_BYTES / per_set) + 1)) if per_set < 2 * L2_BYTES else 1
+        self.R = max(self.R, min_sets)
         lds = max(4, (K // 128 + 3) // 4 * 4)
         ws_bytes = F.fp8bs_gemm_workspace_size(M, N, K)
         self.fused = fused
@@ -235,89 +250,88 @@ class DenseWork:
         self.gemm_launches = 2 if ws_bytes else 1
         self.flops = 2.0 * M * N * K
         nb, kb = (N + 127) // 128, K // 128
+        # operand bytes of one GEMM: codes of X and W, scales, bf16 output
+        gemm_bytes = 1.0 * M * K + 1.0 * N * K + 4.0 * M * kb + 4.0 * nb * kb + 2.0 * M * N
         self.kernels = {
-            # name: (callable(set), launches, algorithmic bytes or flops, bound)
+            # name: (callable(set), launches, algorithmic units, bound[, bytes for a tensor-bound row])
             "weight_quant": (lambda s: F.fp8bs_weight_quant(s["w"], wq=s["wq"], sw=s["sw"]), 1,
                              3.0 * N * K + 4.0 * nb * kb, "hbm"),
             "act_quant": (lambda s: F.fp8bs_act_quant(s["x"], xq=s["xq"], sx=s["sx"]), 1,
                           3.0 * M * K + 4.0 * M * kb, "hbm"),
             "fp8_gemm": (lambda s: F.fp8bs_gemm(s["xq"], s["sx"], s["wq"], s["sw"], y=s["y"], workspace=s["ws"]),
-                         self.gemm_launches, self.flops, "tensor"),
+                         self.gemm_launches, self.flops, "tensor", gemm_bytes),
             "weight_dequant": (lambda s: F.fp8bs_weight_dequant(s["wq"], s["sw"], w=s["wd"]), 1,
                                3.0 * N * K + 4.0 * nb * kb, "hbm"),
         }
         self.order = ["weight_quant", "act_quant", "fp8_gemm", "weight_dequant"]
         if fused:
             # the fused GEMM, and what it replaces: the plain GEMM plus act_quant over its output
+            fused_bytes = gemm_bytes - 2.0 * M * N + 1.0 * M * N + 4.0 * M * (N // 128) + 2.0 * N
             self.kernels["fp8_gemm_fused"] = (
                 lambda s: F.fp8bs_gemm_fused(s["xq"], s["sx"], s["wq"], s["sw"], bias=self.bias, want_y=False,
-                                             want_fp8=True, yq=s["yq"], sy=s["sy"]), 1, self.flops, "tensor")
+                                             want_fp8=True, yq=s["yq"], sy=s["sy"]), 1, self.flops, "tensor",
+                fused_bytes)
             self.kernels["act_quant_of_y"] = (lambda s: F.fp8bs_act_quant(s["y"], xq=s["yq2"], sx=s["sy2"]), 1,
                                               3.0 * M * N + 4.0 * M * (N // 128), "hbm")
             self.order = ["weight_quant", "act_quant", "fp8_gemm_fused", "weight_dequant", "fp8_gemm",
                           "act_quant_of_y"]
-        self.step_kernels = ["weight_quant", "act_quant", "fp8_gemm_fused" if fused else "fp8_gemm",
-                             "weight_dequant"]
-        # weight_quant and weight_dequant run on a second stream: they need
-        # nothing from act_quant, and the GEMM only needs weight_quant's output
-        self.side = torch.cuda.Stream(device=device)
-        self.wq_done = torch.cuda.Event()
+        self.step_kernels = ["act_quant", "fp8_gemm_fused" if fused else "fp8_gemm"]
+        if self.dequant:
+            self.step_kernels.append("weight_dequant")
+
+    def prepare(self):
+        """The weight as a checkpoint holds it: quantised once, before timing."""
+        for s in self.sets:
+            self.F.fp8bs_weight_quant(s["w"], wq=s["wq"], sw=s["sw"])
 
     def step(self, i):
-        import torch
         s = self.sets[i % self.R]
         F = self.F
-        main = torch.cuda.current_stream()
-        self.side.wait_stream(main)
-        F.fp8bs_weight_quant(s["w"], wq=s["wq"], sw=s["sw"], stream=self.side)
-        self.wq_done.record(self.side)
-        F.fp8bs_weight_dequant(s["wq"], s["sw"], w=s["wd"], stream=self.side)
-        F.fp8bs_act_quant(s["x"], xq=s["xq"], sx=s["sx"], stream=main)
-        main.wait_event(self.wq_done)
+        F.fp8bs_act_quant(s["x"], xq=s["xq"], sx=s["sx"])
         if self.fused:
             F.fp8bs_gemm_fused(s["xq"], s["sx"], s["wq"], s["sw"], bias=self.bias, want_y=False, want_fp8=True,
-                               yq=s["yq"], sy=s["sy"], stream=main)
+                               yq=s["yq"], sy=s["sy"])
         else:
-            F.fp8bs_gemm(s["xq"], s["sx"], s["wq"], s["sw"], y=s["y"], workspace=s["ws"], stream=main)
-        main.wait_stream(self.side)
+            F.fp8bs_gemm(s["xq"], s["sx"], s["wq"], s["sw"], y=s["y"], workspace=s["ws"])
+        if self.dequant:
+            F.fp8bs_weight_dequant(s["wq"], s["sw"], w=s["wd"])
 
     def launches_per_step(self):
         return sum(self.kernels[k][1] for k in self.step_kernels)
 
-    # e2e: host (pinned) bf16 X and W in, the output (bf16 Y, or FP8 Yq and
-    # its scales for the fused workload) out, through the public calls
-    def e2e_setup(self):
-        self.xp = self.x_host.pin_memory()
-        self.wp = self.w_host.pin_memory()
+    # e2e: per step the bf16 X comes in from pinned host memory and the
+    # result (bf16 Y, or FP8 Yq and its scales for the fused workload) goes
+    # back; the weight stays resident in its quantised form
+    def e2e_slots(self):
         import torch
-        self.h2d = self.xp.numel() * 2 + self.wp.numel() * 2
-        if self.fused:
-            self.yp = torch.empty((self.M, self.N), dtype=torch.uint8).pin_memory()
-            self.syp = torch.empty(self.sets[0]["sy"].shape, dtype=torch.float32).pin_memory()
-            self.d2h = self.yp.numel() + self.syp.numel() * 4
-        else:
-            self.yp = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
-            self.d2h = self.yp.numel() * 2
-
-    def e2e_step(self, i):
-        s = self.sets[i % self.R]
-        s["w"].copy_(self.wp, non_blocking=True)
-        s["x"].copy_(self.xp, non_blocking=True)
-        self.step(i)
-        if self.fused:
-            self.yp.copy_(s["yq"], non_blocking=True)
-            self.syp.copy_(s["sy"], non_blocking=True)
-        else:
-            self.yp.copy_(s["y"], non_blocking=True)
+        if len(self.sets) < 2:  # a second buffer set so copies overlap compute
+            s0 = self.sets[0]
+            s1 = {k: (torch.empty_like(v) if isinstance(v, torch.Tensor) else v) for k, v in s0.items()}
+            s1["y"] = torch.empty((self.M, (self.N + 7) // 8 * 8), dtype=torch.bfloat16,
+                                  device=self.device)[:, :self.N]
+            s1["wq"], s1["sw"] = s0["wq"], s0["sw"]
+            self.sets.append(s1)
+        xp = self.x_host.pin_memory()
+        slots = []
+        for j in range(2):
+            s = self.sets[j]
+            if self.fused:
+                outs = [(torch.empty(s["yq"].shape, dtype=torch.uint8).pin_memory(), s["yq"]),
+                        (torch.empty(s["sy"].shape, dtype=torch.float32).pin_memory(), s["sy"])]
+            else:
+                outs = [(torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory(), s["y"])]
+            slots.append({"h2d": [(s["x"], xp)], "d2h": outs, "run": (lambda j=j: self.step(j))})
+        self.R = max(self.R, 2) if len(self.sets) >= 2 else self.R
+        return slots
 
     def config(self):
+        step = "act_quant+" + ("fp8_gemm_fused(bias, fp8 out)" if self.fused else "fp8_gemm")
+        if self.dequant:
+            step += "+weight_dequant"
         return {"workload": self.case.name + ("_fused" if self.fused else ""), "M": self.M, "N": self.N, "K": self.K,
-                "step": "weight_quant+act_quant+" + ("fp8_gemm_fused(bias, fp8 out)" if self.fused
-                                                      else "fp8_gemm") + "+weight_dequant",
-                "streams": "weight_quant then weight_dequant on a second stream (joined before the GEMM "
-                           "and at the end of each step); act_quant then fp8_gemm on the main stream",
+                "step": step + " (W quantised once before timing, as a checkpoint stores it)",
                 "l2": f"inputs rotate over {self.R} buffer sets of {self.set_bytes / 1e6:.0f} MB (> 126 MB L2)"
-                      if self.R > 1 else "working set larger than the 126 MB L2"}
+                      if self.R > 1 else f"working set {self.set_bytes / 1e6:.0f} MB, larger than the 126 MB L2"}
 
 
 class MoEWork:
@@ -353,6 +367,7 @@ class MoEWork:
         self.xq = torch.empty((self.T, K), dtype=torch.uint8, device=device)
         self.sx = torch.empty((self.T, lds), dtype=torch.float32, device=device)
         self.y = torch.empty((self.T, N), dtype=torch.bfloat16, device=device)
+        self.bufs = [{"x": self.x, "xq": self.xq, "sx": self.sx, "y": self.y}]
         self.R = 1
         counts = np.diff(case.offsets)
         self.flops = 2.0 * self.T * N * K
@@ -372,6 +387,8 @@ class MoEWork:
             # h leaves as FP8 (1x128 groups): the operand of the w2 GEMM
             self.hq = torch.empty((self.T, N), dtype=torch.uint8, device=device)
             self.sh = torch.empty((self.T, max(4, (N // 128 + 3) // 4 * 4)), dtype=torch.float32, device=device)
+            self.bufs[0].update(hq=self.hq, sh=self.sh)
+            del self.bufs[0]["y"]
             gbytes3 -= self.T * N  # one byte per h element instead of two
             self.kernels["grouped_gemm_swiglu"] = (
                 lambda s: F.fp8bs_grouped_gemm_swiglu(self.xq, self.sx, self.wq, self.sw, self.w3q, self.sw3,
@@ -381,36 +398,44 @@ class MoEWork:
             self.order = ["act_quant", "grouped_gemm_swiglu"]
         self.grouped_flops = self.flops
         self.experts_nonempty = int((counts > 0).sum())
+        self.step_kernels = list(self.order)
+
+    def prepare(self):
+        pass
 
     def step(self, i):
-        for k in self.order:
-            self.kernels[k][0](None)
+        b = self.bufs[i % len(self.bufs)]
+        F = self.F
+        F.fp8bs_act_quant(b["x"], xq=b["xq"], sx=b["sx"])
+        if self.swiglu:
+            F.fp8bs_grouped_gemm_swiglu(b["xq"], b["sx"], self.wq, self.sw, self.w3q, self.sw3, self.off,
+                                        want_h=False, want_fp8=True, hq=b["hq"], sh=b["sh"])
+        else:
+            F.fp8bs_grouped_gemm(b["xq"], b["sx"], self.wq, self.sw, self.off, y=b["y"])
 
     def launches_per_step(self):
         return 2
 
-    def e2e_setup(self):
+    # e2e: per step the expert-grouped bf16 rows and the offsets come in, the
+    # output (bf16 y, or FP8 h and its scales) goes back
+    def e2e_slots(self):
         import torch
-        self.xp = self.x_host.pin_memory()
-        self.offp = torch.from_numpy(self.case.offsets).pin_memory()
-        self.h2d = self.xp.numel() * 2 + self.offp.numel() * 4
-        if self.swiglu:  # FP8 h and its scales come back
-            self.yp = torch.empty((self.T, self.N), dtype=torch.uint8).pin_memory()
-            self.shp = torch.empty(self.sh.shape, dtype=torch.float32).pin_memory()
-            self.d2h = self.yp.numel() + self.shp.numel() * 4
-        else:
-            self.yp = torch.empty((self.T, self.N), dtype=torch.bfloat16).pin_memory()
-            self.d2h = self.yp.numel() * 2
-
-    def e2e_step(self, i):
-        self.x.copy_(self.xp, non_blocking=True)
-        self.off.copy_(self.offp, non_blocking=True)
-        self.step(i)
-        if self.swiglu:
-            self.yp.copy_(self.hq, non_blocking=True)
-            self.shp.copy_(self.sh, non_blocking=True)
-        else:
-            self.yp.copy_(self.y, non_blocking=True)
+        if len(self.bufs) < 2:
+            self.bufs.append({k: torch.empty_like(v) for k, v in self.bufs[0].items()})
+        xp = self.x_host.pin_memory()
+        offp = torch.from_numpy(self.case.offsets).pin_memory()
+        slots = []
+        for j in range(2):
+            b = self.bufs[j]
+            if self.swiglu:
+                outs = [(torch.empty(b["hq"].shape, dtype=torch.uint8).pin_memory(), b["hq"]),
+                        (torch.empty(b["sh"].shape, dtype=torch.float32).pin_memory(), b["sh"])]
+            else:
+                outs = [(torch.empty(b["y"].shape, dtype=torch.bfloat16).pin_memory(), b["y"])]
+            # the offsets buffer is shared: every step carries the same routing
+            slots.append({"h2d": [(b["x"], xp)] + ([(self.off, offp)] if j == 0 else []), "d2h": outs,
+                          "run": (lambda j=j: self.step(j))})
+        return slots
 
     def config(self):
         if self.swiglu:
@@ -523,6 +548,10 @@ class MoELayerWork:
         self.flops = T * (4.0 * I * D + 2.0 * D * I) + tokens * (4.0 * I * D + 2.0 * D * I) + 2.0 * tokens * G * D
         self.grouped_flops = T * (4.0 * I * D + 2.0 * D * I)
         self.experts_nonempty = int((np.diff(case.offsets) > 0).sum())
+        self.step_kernels = list(self.order)
+
+    def prepare(self):
+        pass
 
     def step(self, i):
         for k in self.order:
@@ -531,19 +560,20 @@ class MoELayerWork:
     def launches_per_step(self):
         return len(self.order)
 
-    def e2e_setup(self):
+    # e2e: per step the tokens come in (the router runs on the device) and the
+    # layer output goes back; the kernels read self.x and write self.y, which
+    # each slot points at its own pair of buffers before it runs
+    def e2e_slots(self):
         import torch
-        # per step: the tokens and this batch's routing come in, the layer output goes back
-        # per step the tokens come in (the router runs on the device) and the layer output goes back
-        self.xp = self.x_host.pin_memory()
-        self.yp = torch.empty(self.y.shape, dtype=torch.bfloat16).pin_memory()
-        self.h2d = self.xp.numel() * 2
-        self.d2h = self.yp.numel() * 2
+        xs = [self.x, torch.empty_like(self.x)]
+        ys = [self.y, torch.empty_like(self.y)]
+        xp = self.x_host.pin_memory()
 
-    def e2e_step(self, i):
-        self.x.copy_(self.xp, non_blocking=True)
-        self.step(i)
-        self.yp.copy_(self.y, non_blocking=True)
+        def run(j):
+            self.x, self.y = xs[j], ys[j]
+            self.step(j)
+        return [{"h2d": [(xs[j], xp)], "d2h": [(torch.empty(self.y.shape, dtype=torch.bfloat16).pin_memory(),
+                                                ys[j])], "run": (lambda j=j: run(j))} for j in range(2)]
 
     def config(self):
         return {"workload": "moe_layer", "tokens": self.tokens, "experts": self.G, "top_k": self.topk,
@@ -554,6 +584,71 @@ class MoELayerWork:
                 "l2": "working set (11.3 GB of expert weights) larger than the 126 MB L2"}
 
 
+class RouterWork:
+    """The MoE router alone on 4096 tokens: the gate (bf16 gate logits,
+    sigmoid, group-limited top-8, gate values) and its routing tables."""
+
+    def __init__(self, device):
+        import torch
+        from fp8_block_scaled_18_b300 import fp8bs as F
+        from fp8_block_scaled_18_b300 import synth
+        self.F = F
+        case = synth.moe()
+        self.case = case
+        G, D = case.n_experts, case.k
+        tokens = case.x_tokens.shape[0]
+        self.G, self.D, self.tokens = G, D, tokens
+        self.topk = case.rows_of_token.shape[1]
+        T = tokens * self.topk
+        self.x_host = torch.from_numpy(case.x_tokens.view(np.int16)).view(torch.bfloat16)
+        self.x = self.x_host.to(device)
+        self.gw = torch.from_numpy(case.gate_w.view(np.int16)).view(torch.bfloat16).to(device)
+        self.gbias = torch.from_numpy(case.gate_bias).to(device)
+        e = lambda *shape, dt=torch.int32: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+        self.ids, self.gates = e(tokens, self.topk), e(tokens, self.topk, dt=torch.float32)
+        self.off, self.tor, self.rot, self.wrow = e(G + 1), e(T), e(tokens, self.topk), e(T, dt=torch.float32)
+        self.R = 1
+        self.kernels = {
+            "moe_gate": (lambda s: F.fp8bs_moe_gate(self.x, self.gw, self.gbias, ids=self.ids, weights=self.gates), 1,
+                         2.0 * tokens * G * D, "tensor_bf16"),
+            "moe_route": (lambda s: F.fp8bs_moe_route(self.ids, self.gates, G, offsets=self.off, token_of_row=self.tor,
+                                                      rows_of_token=self.rot, weight_of_row=self.wrow), 1,
+                          8.0 * tokens * self.topk + 12.0 * T, "hbm"),
+        }
+        self.order = ["moe_gate", "moe_route"]
+        self.step_kernels = list(self.order)
+        self.flops = 2.0 * tokens * G * D
+
+    def prepare(self):
+        pass
+
+    def step(self, i):
+        for k in self.order:
+            self.kernels[k][0](None)
+
+    def launches_per_step(self):
+        return 2
+
+    def e2e_slots(self):
+        import torch
+        xs = [self.x, torch.empty_like(self.x)]
+        xp = self.x_host.pin_memory()
+
+        def run(j):
+            self.x = xs[j]
+            self.step(j)
+        return [{"h2d": [(xs[j], xp)],
+                 "d2h": [(torch.empty(self.ids.shape, dtype=torch.int32).pin_memory(), self.ids),
+                         (torch.empty(self.gates.shape, dtype=torch.float32).pin_memory(), self.gates)],
+                 "run": (lambda j=j: run(j))} for j in range(2)]
+
+    def config(self):
+        return {"workload": "moe_router", "tokens": self.tokens, "experts": self.G, "top_k": self.topk,
+                "dim": self.D, "step": "moe_gate (bf16 gate GEMM, sigmoid, group-limited top-8, gate values) + "
+                                       "moe_route (routing tables)",
+                "l2": "inputs (59 MB) re-read each step from L2: the router is latency-bound, not HBM-bound"}
+
+
 def make_work(name: str, device):
     from fp8_block_scaled_18_b300 import synth
     if name == "moe":
@@ -562,6 +657,8 @@ def make_work(name: str, device):
         return MoEWork(device, swiglu=True)
     if name == "moe_layer":
         return MoELayerWork(device)
+    if name == "moe_router":
+        return RouterWork(device)
     if name == "kv_down":
         return DenseWork(synth.kv_down(), device)
     if name == "tiny":
@@ -614,6 +711,129 @@ def chunked_graphs(fn, total: int, chunk: int = 200):
     return graphs
 
 
+def kernel_row(work, k, per_call_s, peaks):
+    """Per-kernel roofline row.  A tensor-bound kernel's roofline time is
+    max(FLOP / FP8 peak, bytes / HBM peak) (SURVEY's per-GEMM roofline), so
+    small-M GEMMs are held to the weight read; HBM-bound kernels to their
+    algorithmic bytes.  frac = roofline time / measured time, against the
+    burst peaks; frac_sustained against the sustained tensor peak."""
+    entry = work.kernels[k]
+    _, launches, units, bound = entry[:4]
+    nbytes = entry[4] if len(entry) > 4 else None
+    hbm = float(peaks["hbm_gbs"])
+    row = {"us_per_call": round(per_call_s * 1e6, 3), "launches_per_call": launches, "bound": bound}
+    if bound in ("tensor", "tensor_bf16"):
+        peak = float(peaks["bf16_tflops"]) * (FP8_OVER_BF16 if bound == "tensor" else 1.0)
+        peak_s = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * (
+            FP8_OVER_BF16 if bound == "tensor" else 1.0)
+        t_tensor = units / (peak * 1e12)
+        t_hbm = nbytes / (hbm * 1e9) if nbytes else 0.0
+        row.update(achieved=round(units / per_call_s / 1e12, 2), unit="TFLOP/s")
+        row["roof_bound"] = "tensor" if t_tensor >= t_hbm else "hbm"
+        row["frac"] = round(max(t_tensor, t_hbm) / per_call_s, 4)
+        row["frac_sustained"] = round(max(units / (peak_s * 1e12), t_hbm) / per_call_s, 4)
+        if nbytes:
+            row["gbs"] = round(nbytes / per_call_s / 1e9, 1)
+    else:
+        row.update(achieved=round(units / per_call_s / 1e9, 2), unit="GB/s", roof_bound="hbm",
+                   frac=round(units / per_call_s / 1e9 / hbm, 4))
+    return row
+
+
+def time_kernels(work, K, world, device):
+    """ms for K launches of each kernel of work.order, alone, from graphs."""
+    kernel_graphs = {k: chunked_graphs(lambda i, k=k: work.kernels[k][0](work.sets[i % work.R]
+                                                                         if hasattr(work, "sets") else None), K)
+                     for k in work.order}
+    return {k: replay_timed(kernel_graphs[k], world, device) for k in work.order}
+
+
+CONFIG_TABLE = ["tiny", "kv_down"] + [f"q_down_m{m}" for m in (1, 16, 64, 512, 4096, 16384)] + \
+    ["large_square", "moe"]
+
+
+def config_table(args, world, device, peaks, done=None):
+    """The five configurations (tiny, KV down-projection, the Q sweep, the
+    large square, the MoE grouped GEMM): each kernel timed alone (graphs of K
+    launches) with its roofline row, and the configuration's step."""
+    import gc
+    import torch
+    K = args.steps
+    out = {}
+    for name in CONFIG_TABLE:
+        if done is not None and name == done[0]:
+            out[name] = done[1]
+            continue
+        work = make_work(name, device)
+        work.prepare()
+        for i in range(max(3, work.R)):
+            work.step(i)
+        kernel_ms = time_kernels(work, K, world, device)
+        step_ms = replay_timed(chunked_graphs(work.step, K), world, device)
+        rows = {k: kernel_row(work, k, kernel_ms[k] / K * 1e-3, peaks) for k in work.order}
+        out[name] = {"step": work.config()["step"], "us_per_step": round(step_ms / K * 1e3, 3),
+                     "kernels": rows}
+        del work
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
+
+
+def e2e_overlapped(work, K, W, world, device):
+    """The same steps end to end through the public calls: each step's inputs
+    copied in from pinned host memory and its result copied back, on two copy
+    streams, double-buffered so that step i+1's upload and step i-1's
+    download run while step i computes.  Returns (ms, h2d bytes, d2h bytes)
+    per K steps."""
+    import torch
+    slots = work.e2e_slots()
+    main = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    h2d_done = [torch.cuda.Event() for _ in slots]
+    computed = [torch.cuda.Event() for _ in slots]
+    d2h_done = [torch.cuda.Event() for _ in slots]
+    h2d_bytes = sum(src.numel() * src.element_size() for dst, src in slots[0]["h2d"])
+    d2h_bytes = sum(dst.numel() * dst.element_size() for dst, src in slots[0]["d2h"])
+    for ev in computed + d2h_done:
+        ev.record(main)
+
+    def upload(i):
+        j = i % 2
+        up.wait_event(computed[j])           # step i-2 no longer reads this slot's inputs
+        with torch.cuda.stream(up):
+            for dst, src in slots[j]["h2d"]:
+                dst.copy_(src, non_blocking=True)
+        h2d_done[j].record(up)
+
+    def run(n):
+        upload(0)
+        for i in range(n):
+            j = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            main.wait_event(h2d_done[j])
+            main.wait_event(d2h_done[j])     # step i-2's result has left this slot
+            slots[j]["run"]()
+            computed[j].record(main)
+            down.wait_event(computed[j])
+            with torch.cuda.stream(down):
+                for dst, src in slots[j]["d2h"]:
+                    dst.copy_(src, non_blocking=True)
+            d2h_done[j].record(down)
+        main.wait_stream(down)
+
+    run(W)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    run(K)
+    e1.record(main)
+    torch.cuda.synchronize()
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1), world, device), h2d_bytes, d2h_bytes
+
+
 def run_ours(args, rank, local, world):
     import torch
     device = f"cuda:{local}"
@@ -623,19 +843,26 @@ def run_ours(args, rank, local, world):
 
     peaks, peaks_src = load_peaks()
     work = make_work(args.workload, device)
+    work.prepare()
     # eager warm-up (also loads modules and sets kernel attributes before capture)
     for i in range(max(3, work.R)):
         work.step(i)
     st = F.fp8bs_sync_status()
     if st != 0:
         raise SystemExit(f"device status after warm-up: {F.fp8bs_status_string(st)}")
+    if args.profile_steps:
+        # a fixed number of eager steps for a profiler, nothing timed or printed
+        for i in range(args.profile_steps):
+            work.step(i)
+        torch.cuda.synchronize()
+        st = F.fp8bs_sync_status()
+        if st != 0:
+            raise SystemExit(f"device status: {F.fp8bs_status_string(st)}")
+        return
 
     K, W = args.steps, max(3, args.warmup)
     step_graphs = chunked_graphs(work.step, K)
     warm_graphs = chunked_graphs(work.step, W)
-    kernel_graphs = {k: chunked_graphs(lambda i, k=k: work.kernels[k][0](work.sets[i % work.R]
-                                                                         if hasattr(work, "sets") else None), K)
-                     for k in work.order}
 
     with ClockSampler(local) as clocks:
         # soak: ~1 s of steps so the clock record covers sustained load
@@ -647,7 +874,7 @@ def run_ours(args, rank, local, world):
         for g in warm_graphs:  # W untimed warm-up steps
             g.replay()
         step_ms = replay_timed(step_graphs, world, device)
-        kernel_ms = {k: replay_timed(kernel_graphs[k], world, device) for k in work.order}
+        kernel_ms = time_kernels(work, K, world, device)
     clock = clocks.summary()
     st = F.fp8bs_sync_status()
     if st != 0:
@@ -657,41 +884,31 @@ def run_ours(args, rank, local, world):
     total_flops = sum_over_ranks(work.flops * K, world, device)
     value = total_flops / (step_ms * 1e-3) / 1e12
 
-    # per-kernel roofline rows
-    hbm_peak = float(peaks["hbm_gbs"])
-    fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
-    kernels = {}
-    # shares and the roofline kernel over the step's own kernels; other
-    # kernels (comparisons) are timed alone and reported without a share
-    step_kernels = getattr(work, "step_kernels", work.order)
+    # per-kernel roofline rows; shares and the roofline kernel over the
+    # step's own kernels (other kernels are timed alone, without a share)
+    step_kernels = work.step_kernels
     step_ms_sum = sum(kernel_ms[k] for k in step_kernels)
+    kernels = {}
     for k in work.order:
-        _, launches, units, bound = work.kernels[k]
-        per_call_s = kernel_ms[k] / K * 1e-3
-        if bound == "tensor":
-            ach, peak, unit = units / per_call_s / 1e12, fp8_peak, "TFLOP/s"
-        elif bound == "tensor_bf16":
-            ach, peak, unit = units / per_call_s / 1e12, float(peaks["bf16_tflops"]), "TFLOP/s"
-        else:
-            ach, peak, unit = units / per_call_s / 1e9, hbm_peak, "GB/s"
-        kernels[k] = {"us_per_call": round(per_call_s * 1e6, 3), "launches_per_call": launches,
-                      "achieved": round(ach, 2), "unit": unit, "bound": bound,
-                      "frac": round(ach / peak, 4),
-                      "share": round(kernel_ms[k] / step_ms_sum, 4) if k in step_kernels else None}
-    if "fp8_gemm" in kernels:
-        kernels["fp8_gemm"]["tflops"] = kernels["fp8_gemm"]["achieved"]
+        kernels[k] = kernel_row(work, k, kernel_ms[k] / K * 1e-3, peaks)
+        kernels[k]["share"] = round(kernel_ms[k] / step_ms_sum, 4) if k in step_kernels else None
     dom = max(step_kernels, key=lambda k: kernel_ms[k])
-    _, launches, units, bound = work.kernels[dom]
+    entry = work.kernels[dom]
+    units, bound = entry[2], entry[3]
     dom_s = kernel_ms[dom] / K * 1e-3
     if bound == "tensor":
-        roof = {"bound": "tensor", "achieved": units / dom_s / 1e12, "peak": fp8_peak, "unit": "TFLOP/s"}
-        peak_note = f"{peaks_src} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio)"
+        roof = {"bound": "tensor", "achieved": units / dom_s / 1e12, "peak": float(peaks["bf16_tflops"]) *
+                FP8_OVER_BF16, "unit": "TFLOP/s"}
+        peak_note = (f"{peaks_src} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio); "
+                     f"frac_sustained uses the {peaks_src} sustained bf16 x {FP8_OVER_BF16:g}")
+        roof["frac_sustained"] = round(roof["achieved"] / (float(peaks["bf16_tflops_sustained"]) * FP8_OVER_BF16),
+                                       4)
     elif bound == "tensor_bf16":
         roof = {"bound": "tensor", "achieved": units / dom_s / 1e12, "peak": float(peaks["bf16_tflops"]),
                 "unit": "TFLOP/s"}
         peak_note = f"{peaks_src} bf16 burst"
     else:
-        roof = {"bound": "hbm", "achieved": units / dom_s / 1e9, "peak": hbm_peak, "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": units / dom_s / 1e9, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s"}
         peak_note = f"{peaks_src} HBM copy bandwidth"
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = ncu_traffic(dom, work.config()["workload"])
@@ -702,34 +919,32 @@ def run_ours(args, rank, local, world):
         roof[key] = round(roof[key], 4)
 
     # end to end through the public calls with pinned host buffers
-    work.e2e_setup()
-    for i in range(W):
-        work.e2e_step(i)
-    barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(K):
-        work.e2e_step(i)
-    e1.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    e2e_ms, h2d, d2h = e2e_overlapped(work, K, W, world, device)
     e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
+    main_row = {"step": work.config()["step"], "us_per_step": round(ms_per_step * 1e3, 3), "kernels": kernels}
+    main_name = args.workload
+    cfg = work.config()
+    launches = work.launches_per_step()
+    del work
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 MMA, fp32 promote, bf16 out", "data": "synthetic (seeded numpy / torch RNG)",
-        "config": {**work.config(), "parallelism": f"replicas{world}", "timing": "CUDA graphs of K steps"},
+        "config": {**cfg, "parallelism": f"replicas{world}",
+                   "timing": "CUDA graphs of K steps"},
         "roofline": roof, "kernels": kernels,
         "act_quant_gbs": kernels.get("act_quant", {}).get("achieved"),
         "act_quant_hbm_frac": kernels.get("act_quant", {}).get("frac"),
         "clocks": clock,
-        "e2e": {"value": round(e2e_value, 4), "unit": "TFLOP/s", "h2d_bytes_per_step": work.h2d,
-                "d2h_bytes_per_step": work.d2h, "api": "fp8bs_* C ABI via the Python binding, eager, pinned host"},
-        "gpu_launches": K * work.launches_per_step(),
+        "e2e": {"value": round(e2e_value, 4), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "api": "fp8bs_* C ABI via the Python binding, eager, pinned host buffers, uploads and downloads "
+                       "on two copy streams double-buffered against the compute"},
+        "gpu_launches": K * launches,
     }
+    if not args.no_configs:
+        line["configs"] = config_table(args, world, device, peaks, done=(main_name, main_row))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     if rank == 0:
@@ -738,13 +953,14 @@ def run_ours(args, rank, local, world):
 
 # ---------------------------------------------------------------- oracle legs
 
-def oracle_sample_step(orc, case, rows):
-    """One bounded oracle pass: weight_quant + act_quant(rows) + gemm(rows) +
-    weight_dequant for a dense case; returns the GEMM flops done."""
-    wq, sw = orc.weight_quant(case.w)
+def oracle_sample_step(orc, case, rows, wq, sw):
+    """One bounded oracle pass over a dense case's step: act_quant(rows) +
+    gemm(rows) against the quantised W (+ weight_dequant of W for the large
+    square); returns the GEMM flops done."""
     xq, sx = orc.act_quant(case.x[rows])
     orc.gemm(xq, sx, wq, sw)
-    orc.weight_dequant(wq, sw)
+    if case.name == "large_square":
+        orc.weight_dequant(wq, sw)
     return 2.0 * len(rows) * case.w.shape[0] * case.x.shape[1]
 
 
@@ -811,15 +1027,15 @@ def make_case(workload: str):
     raise SystemExit(f"unknown workload {workload}")
 
 
-def oracle_rows_for(orc, case, seconds: float) -> int:
+def oracle_rows_for(orc, case, seconds: float, wq, sw) -> int:
     """Rows of a dense case whose oracle pass takes about `seconds`
     (fixed weight-side cost + per-row GEMM cost, measured on 1 and 5 rows)."""
     M = case.x.shape[0]
     t0 = time.perf_counter()
-    oracle_sample_step(orc, case, np.array([0]))
+    oracle_sample_step(orc, case, np.array([0]), wq, sw)
     t1 = time.perf_counter() - t0
     t0 = time.perf_counter()
-    oracle_sample_step(orc, case, np.arange(5) % M)
+    oracle_sample_step(orc, case, np.arange(5) % M, wq, sw)
     t5 = time.perf_counter() - t0
     per_row = max((t5 - t1) / 4, 1e-4)
     fixed = max(t1 - per_row, 0.0)
@@ -838,6 +1054,19 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
     from fp8_block_scaled_18_b300 import synth
     from oracle import Oracle
     orc = Oracle()
+    if workload == "moe_router":
+        case = synth.moe()
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < seconds and n < case.x_tokens.shape[0]:
+            ids, w = orc.moe_gate(case.x_tokens[n:n + 16], case.gate_w, case.gate_bias)
+            orc.moe_route(ids, w, case.n_experts)
+            n += 16
+        dt = time.perf_counter() - t0
+        flops = 2.0 * n * case.n_experts * case.k
+        sample = f"{n} of {case.x_tokens.shape[0]} tokens: router (gate GEMM, sigmoid, top-k) + routing tables"
+        return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "host_cores_available": cpu_cores(),
+                "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
     if workload == "moe_layer":
         case = synth.moe()
         counts = np.diff(case.offsets)
@@ -870,13 +1099,15 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
     else:
         case = make_case(workload)
         M = case.x.shape[0]
-        rows = oracle_rows_for(orc, case, seconds)
+        wq, sw = orc.weight_quant(case.w)  # untimed, as the GPU arm quantises W before timing
+        rows = oracle_rows_for(orc, case, seconds, wq, sw)
         sel = np.linspace(0, M - 1, rows).astype(np.int64)
         t0 = time.perf_counter()
-        flops = oracle_sample_step(orc, case, sel)
+        flops = oracle_sample_step(orc, case, sel, wq, sw)
         dt = time.perf_counter() - t0
-        sample = (f"{rows} of {M} rows: weight_quant(W) + act_quant(rows) + gemm(rows) + weight_dequant(W), "
-                  f"TFLOP/s over the sampled GEMM work")
+        sample = (f"{rows} of {M} rows: act_quant(rows) + gemm(rows)"
+                  + (" + weight_dequant(W)" if case.name == "large_square" else "")
+                  + ", W quantised before timing; TFLOP/s over the sampled GEMM work")
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "host_cores_available": cpu_cores(),
             "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
 
@@ -891,7 +1122,22 @@ def run_reference(args, rank, local, world):
     orc = Oracle()
     K, W = args.steps, max(3, args.warmup)
     budget = 150.0  # seconds for the whole run
-    if args.workload == "moe_layer":
+    if args.workload == "moe_router":
+        case = synth.moe()
+        ntok = case.x_tokens.shape[0]
+        t0 = time.perf_counter()
+        orc.moe_gate(case.x_tokens[:8], case.gate_w, case.gate_bias)
+        per_tok = max((time.perf_counter() - t0) / 8, 1e-5)
+        rows = int(max(1, min(ntok, budget / (K + W) / per_tok)))
+
+        def step(i):
+            sel = (np.arange(rows) + i * rows) % ntok
+            ids, w = orc.moe_gate(case.x_tokens[sel], case.gate_w, case.gate_bias)
+            orc.moe_route(ids, w, case.n_experts)
+            return 2.0 * rows * case.n_experts * case.k
+        sample = f"{rows} of {ntok} tokens per step: router (gate GEMM, sigmoid, top-k) + routing tables"
+        cfg = {"workload": "moe_router"}
+    elif args.workload == "moe_layer":
         case = synth.moe()
         counts = np.diff(case.offsets)
         g = int(np.argmax(counts))  # the busiest expert
@@ -969,12 +1215,15 @@ def run_reference(args, rank, local, world):
         # set-up, untimed: the quantised weight the sampled GEMM rows use
         wq_all, sw_all = orc.weight_quant(case.w)
 
+        dequant = case.name == "large_square"
+
         def step(i, rows):
-            # one 128-row weight block quantised and dequantised (rotating),
-            # act_quant + gemm of `rows` activation rows against the whole W
-            b = i % nblk
-            wq_b, sw_b = orc.weight_quant(case.w[128 * b:128 * (b + 1)])
-            orc.weight_dequant(wq_b, sw_b)
+            # act_quant + gemm of `rows` activation rows against the whole
+            # quantised W; for the large square also weight_dequant of one
+            # 128-row block of W (rotating)
+            if dequant:
+                b = i % nblk
+                orc.weight_dequant(wq_all[128 * b:128 * (b + 1)], sw_all[b:b + 1])
             rs = (np.arange(rows) + i * rows) % M
             xq, sx = orc.act_quant(case.x[rs])
             orc.gemm(xq, sx, wq_all, sw_all)
@@ -992,8 +1241,8 @@ def run_reference(args, rank, local, world):
         rows = int(max(1, min(M, (budget / (K + W) - fixed) / per_row)))
         step_fn = step
         step = lambda i: step_fn(i, rows)  # noqa: E731
-        sample = (f"{rows} of {M} rows per step: weight_quant + weight_dequant of one 128-row block of W "
-                  f"(rotating), act_quant(rows), gemm(rows) against the whole quantised W")
+        sample = (f"{rows} of {M} rows per step: act_quant(rows), gemm(rows) against the whole quantised W"
+                  + (", weight_dequant of one 128-row block of W (rotating)" if dequant else ""))
         M_, N_, K_ = case.shape
         cfg = {"workload": case.name, "M": M_, "N": N_, "K": K_}
     for i in range(W):
