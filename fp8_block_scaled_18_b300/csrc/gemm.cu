@@ -125,11 +125,17 @@ struct Layout {
     // SwiGLU FP8 output: per tile parity, per warpgroup, the amax of each row's 64 values
     static constexpr int OFF_HAMAX = OFF_BIAS + BIAS_BYTES;
     static constexpr int HAMAX_BYTES = 2 * 2 * BM * 4;
-    static constexpr int BYTES = OFF_HAMAX + HAMAX_BYTES;
+    // bf16 output staging of 256-column tiles: per promotion warp two 1 KB
+    // boxes (32 rows x 16 columns, 32-byte swizzle) that TMA stores drain
+    static constexpr int EPI_WARPS = BN == 256 ? 8 : 0;
+    static constexpr int OFF_EPI = (OFF_HAMAX + HAMAX_BYTES + 1023) & ~1023;
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * 1024;
+    static constexpr int BYTES = OFF_EPI + EPI_BYTES;
     static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;                  // allocation: a power of two
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
     static_assert(NBUF >= 2 && NBUF * BUF_COLS <= 512, "two or more chunk buffers must fit in TMEM");
+    static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
 };
 
 struct Params {
@@ -308,7 +314,7 @@ template <int BN, int STAGES, int MODE>
 __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmS,
-                    const __grid_constant__ Params p) {
+                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ Params p) {
     using L = Layout<BN, STAGES>;
     using R = Roles<nwg_for(BN)>;
     constexpr int kEpiWarps = R::kEpiWarps;
@@ -339,6 +345,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
         tma_prefetch_desc(&tmB);
         if (MODE == kGroupedSwiglu) tma_prefetch_desc(&tmB3);
         tma_prefetch_desc(&tmS);
+        if (BN == 256 && (MODE == kDense || MODE == kGrouped) && p.y != nullptr) tma_prefetch_desc(&tmY);
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -366,6 +373,10 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
     if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
     constexpr bool GROUPED = is_grouped(MODE);
     constexpr bool SWIGLU = MODE == kGroupedSwiglu;
+    // bf16 output of 256-column dense / grouped tiles leaves through shared
+    // memory and TMA stores (whole 32-row boxes; rows past M are dropped by
+    // the tensor map, rows past a grouped expert's end take the direct path)
+    constexpr bool TMA_EPI = BN == 256 && (MODE == kDense || MODE == kGrouped);
     static_assert(!SWIGLU || BN == 256, "SwiGLU tiles are 128 gate + 128 up columns");
     if (GROUPED && warp == kEpiWarp0) build_tile_table<tile_cols<BN, MODE>()>(p, prefix, lane);
     tc_fence_before();
@@ -386,12 +397,15 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
         WorkCursor<BN, MODE> wc;
         wc.begin(p);
         Tile tl;
-        while (ok && wc.next(p, prefix, num_tiles, tl)) {
-            for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
-                const int s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1u;
-                if (!warp_wait(empty_bar(s), ph ^ 1u, ctl)) { ok = false; break; }
-                if (lane == 0) {
+        // One lane runs the loop: its waits and the TMA issues are single-
+        // thread operations, and a lone lane polls a barrier with less
+        // overhead than a warp-wide vote.
+        if (lane == 0) {
+            while (ok && wc.next(p, prefix, num_tiles, tl)) {
+                for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!bounded_wait(empty_bar(s), ph ^ 1u, ctl)) { ok = false; break; }
                     mbar_arrive_expect_tx(full_bar(s), L::STAGE_BYTES);
                     tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * BK, tl.m0);
                     if constexpr (SWIGLU) {  // gate rows, then the same rows of w3
@@ -402,9 +416,10 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                         tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * BK, tl.b_row);
                     }
                 }
-                __syncwarp();
             }
         }
+        __syncwarp();
+        it = __shfl_sync(0xffffffffu, it, 0);
         // Every issued load must land before the CTA's shared memory goes away.
         const uint32_t first = it > STAGES ? it - STAGES : 0;
         for (uint32_t j = first; j < it; ++j) drain_wait(full_bar(j % STAGES), (j / STAGES) & 1u, ctl);
@@ -417,17 +432,17 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
         WorkCursor<BN, MODE> wc;
         wc.begin(p);
         Tile tl;
-        while (ok && wc.next(p, prefix, num_tiles, tl)) {
-            for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
-                if ((it % kMmaWarps) != mw) continue;
-                const int s = it % STAGES;
-                const uint32_t sph = (it / STAGES) & 1u;
-                const int b = it % NBUF;
-                const uint32_t bph = (it / NBUF) & 1u;
-                if (!warp_wait(tempty_bar(b), bph ^ 1u, ctl)) { ok = false; break; }
-                if (!warp_wait(full_bar(s), sph, ctl)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
+        if (lane == 0) {  // one lane runs the loop (single-thread waits, MMAs and commits)
+            while (ok && wc.next(p, prefix, num_tiles, tl)) {
+                for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++it) {
+                    if ((it % kMmaWarps) != mw) continue;
+                    const int s = it % STAGES;
+                    const uint32_t sph = (it / STAGES) & 1u;
+                    const int b = it % NBUF;
+                    const uint32_t bph = (it / NBUF) & 1u;
+                    if (!bounded_wait(tempty_bar(b), bph ^ 1u, ctl)) { ok = false; break; }
+                    if (!bounded_wait(full_bar(s), sph, ctl)) { ok = false; break; }
+                    tc_fence_after();
                     const uint64_t adesc = sdesc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
                     const uint64_t bdesc = sdesc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
                     const uint32_t d = tmem + static_cast<uint32_t>(b * L::BUF_COLS);
@@ -436,17 +451,14 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                         umma_e4m3(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
                     umma_commit(empty_bar(s));
                     umma_commit(tfull_bar(b));
+                    issued = true;
                 }
-                issued = true;
-                __syncwarp();
             }
+            // All of this warp's MMAs must finish before TMEM is released.
+            if (issued) umma_commit(done_bar(mw));
         }
-        // All of this warp's MMAs must finish before TMEM is released.
-        if (issued) {
-            if (lane == 0) umma_commit(done_bar(mw));
-            __syncwarp();
-            drain_wait(done_bar(mw), 0, ctl);
-        }
+        __syncwarp();
+        if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) drain_wait(done_bar(mw), 0, ctl);
       } else if (warp == kScaleWarp) {
         // ------------------------------------------------------------ scale loader
         // Per block of kScaleChunks chunks: sx of the tile's rows by TMA (one
@@ -552,6 +564,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
         const float* sw_slots = reinterpret_cast<const float*>(smem + L::OFF_SWS);
         uint32_t ss = 0;                    // scale blocks consumed
         uint32_t h_tiles = 0;               // SwiGLU FP8 output: tiles exchanged (barrier parity, phase)
+        uint32_t epi_n = 0;                 // TMA-store epilogue: boxes this warp has stored
         uint32_t it = 0;
         bool ok = true;
         WorkCursor<BN, MODE> wc;
@@ -717,8 +730,8 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                 }
                 continue;
             }
-            if (!row_ok) continue;
             if (MODE == kSplitK) {
+                if (!row_ok) continue;
                 float* pr = p.partial + (static_cast<int64_t>(tl.tile) * p.M + m) * p.N;
 #pragma unroll
                 for (int v = 0; v < COLS / 4; ++v) {
@@ -737,7 +750,45 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                 uint32_t yb[COLS / 2];  // bf16 pairs (column 2v in the low half)
 #pragma unroll
                 for (int v = 0; v < COLS / 2; ++v) yb[v] = pack_bf16x2(lo_f32(acc[v]), hi_f32(acc[v]));
-                if (p.y != nullptr) {
+                // Whole 32-row boxes go out through shared memory: the warp's
+                // 32 rows x 16 columns at a time, alternating between its two
+                // 1 KB boxes (32-byte swizzle: the 16-byte half c of row r sits
+                // at r * 32 + 16 * (c ^ ((r >> 2) & 1)), so the warp's stores
+                // hit distinct banks), one TMA store per box.
+                bool direct = p.y != nullptr;
+                if constexpr (TMA_EPI) {
+                    const int r0 = tl.m0 + quarter * 32;
+                    if (p.y != nullptr && (MODE == kDense || r0 + 32 <= tl.m_end)) {
+                        direct = false;
+                        const uint32_t stage = sbase + L::OFF_EPI + static_cast<uint32_t>(ew) * 2048u;
+                        const bool rows_in = r0 < p.M;
+#pragma unroll
+                        for (int pc = 0; pc < COLS / 16; ++pc, ++epi_n) {
+                            const uint32_t box = stage + (epi_n & 1u) * 1024u;
+                            if (lane == 0) bulk_wait_group_read<1>();  // the store two boxes back has read it
+                            __syncwarp();
+#pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                const uint32_t dst = box + lane * 32 + 16 * (c ^ ((lane >> 2) & 1));
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                             "r"(yb[8 * pc + 4 * c]), "r"(yb[8 * pc + 4 * c + 1]),
+                                             "r"(yb[8 * pc + 4 * c + 2]), "r"(yb[8 * pc + 4 * c + 3])
+                                             : "memory");
+                            }
+                            fence_proxy_async_shared();
+                            __syncwarp();
+                            if (lane == 0) {
+                                // a box wholly outside y is not stored, but its
+                                // (empty) group is still committed: the buffer
+                                // reuse above counts one group per box
+                                if (rows_in && nbase + 16 * pc < p.N) tma_store_2d(&tmY, box, nbase + 16 * pc, r0);
+                                bulk_commit_group();
+                            }
+                        }
+                    }
+                }
+                if (!row_ok) continue;
+                if (direct) {
                     uint16_t* yr = p.y + static_cast<int64_t>(m) * p.ldy;
 #pragma unroll
                     for (int v = 0; v < COLS / 8; ++v) {
@@ -777,6 +828,10 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                     }
                 }
             }
+        }
+        if constexpr (TMA_EPI) {  // the output boxes must be written before the CTA exits
+            if (lane == 0) bulk_wait_group<0>();
+            __syncwarp();
         }
     }
 
@@ -840,7 +895,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 // box_rows x 128 bytes, 128-byte swizzle, zero fill outside the tensor.
 cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
                      uint32_t box_rows) {
-    return make_tmap_2d(map, base, 1, inner, rows, stride_bytes, BK, box_rows, true);
+    return make_tmap_2d(map, base, 1, inner, rows, stride_bytes, BK, box_rows, 128);
 }
 
 // Tile widths 256, 192 or 160 columns.  A CTA's time per 128-K chunk is set
@@ -939,7 +994,7 @@ cudaError_t ensure_kernel_ready(int device) {
 template <int BN, int STAGES, int MODE>
 cudaError_t launch_mode(const GemmArgs& a, Params& p, int grid, const DeviceInfo& dev, cudaStream_t stream) {
     const int64_t b_rows = is_grouped(MODE) ? static_cast<int64_t>(a.G) * a.N : a.N;
-    CUtensorMap tmA, tmB, tmB3, tmS;
+    CUtensorMap tmA, tmB, tmB3, tmS, tmY;
     cudaError_t e;
     if ((e = make_map(&tmA, a.xq, a.K, a.M, a.K, BM)) != cudaSuccess) return e;
     if constexpr (MODE == kGroupedSwiglu) {  // two boxes of 128 rows per stage, one from each weight
@@ -950,11 +1005,18 @@ cudaError_t launch_mode(const GemmArgs& a, Params& p, int grid, const DeviceInfo
         tmB3 = tmB;  // unused
     }
     // sx [M, lds] fp32: boxes of kScaleChunks chunks x BM rows
-    if ((e = make_tmap_2d(&tmS, a.sx, 4, a.lds, a.M, a.lds * 4, kScaleChunks, BM, false)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&tmS, a.sx, 4, a.lds, a.M, a.lds * 4, kScaleChunks, BM, 0)) != cudaSuccess) return e;
+    // y [M, N] bf16 with row stride ldy: boxes of 32 rows x 16 columns for
+    // the TMA-store epilogue of 256-column dense / grouped tiles
+    if (BN == 256 && (MODE == kDense || MODE == kGrouped) && a.y != nullptr) {
+        if ((e = make_tmap_2d(&tmY, a.y, 2, a.N, a.M, a.ldy * 2, 16, 32, 32)) != cudaSuccess) return e;
+    } else {
+        tmY = tmA;  // unused
+    }
     if ((e = ensure_kernel_ready<BN, STAGES, MODE>(dev.device)) != cudaSuccess) return e;
     return launch_pdl(fp8_gemm_kernel<BN, STAGES, MODE>, dim3(grid), dim3(Roles<nwg_for(BN)>::kThreads),
                       Layout<BN, STAGES>::ALLOC,
-                      stream, tmA, tmB, tmB3, tmS, p);
+                      stream, tmA, tmB, tmB3, tmS, tmY, p);
 }
 
 template <int MODE>

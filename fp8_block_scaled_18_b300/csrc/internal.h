@@ -30,11 +30,12 @@ uint64_t wait_timeout_ns();
 
 // Encode a 2-D TMA descriptor over a row-major tensor [rows, inner] of
 // elem_bytes-sized elements (1, 2 or 4; 4 = fp32) with the given row stride in bytes;
-// boxes of box_rows x box_inner elements; swizzle128 selects the 128-byte
-// swizzle (the MMA operand layout), else no swizzle.  Reads outside the
-// tensor fill with zeros.  (tmap.cu)
+// boxes of box_rows x box_inner elements; swizzle_bytes 128, 64 or 32 selects
+// that shared-memory swizzle (128: the MMA operand layout), 0 none.  Loads
+// outside the tensor fill with zeros; stores outside it are dropped.
+// (tmap.cu)
 cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
-                         uint64_t stride_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+                         uint64_t stride_bytes, uint32_t box_inner, uint32_t box_rows, int swizzle_bytes);
 
 // Launch `kernel` with programmatic stream serialisation: it may begin while
 // the previous kernel in `stream` finishes; the kernel itself waits

@@ -488,8 +488,8 @@ cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, 
                             int32_t* ids, float* w, const DeviceInfo& dev, cudaStream_t stream) {
     CUtensorMap tmX, tmW;
     cudaError_t e;
-    if ((e = make_tmap_2d(&tmX, x, 2, dim, T, ldx * 2, kGateK, kGateM, true)) != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&tmW, wg, 2, dim, E, dim * 2, kGateK, E, true)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&tmX, x, 2, dim, T, ldx * 2, kGateK, kGateM, 128)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&tmW, wg, 2, dim, E, dim * 2, kGateK, E, 128)) != cudaSuccess) return e;
     {
         static bool ready[64];
         if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
