@@ -58,6 +58,7 @@ def load(mutant: int = 0, omp: bool = False) -> ctypes.CDLL:
             "orc_act_quant_pow2": [_P, _I64, _I64, _I64, _P, _I64, _P, _I64],
             "orc_gemm_dgrad_rows": [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P],
             "orc_gemm_wgrad": [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _P, _P],
+            "orc_gemm_wgrad_rows": [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P],
         }.items():
             fn = getattr(lib, name)
             fn.restype = None
@@ -290,9 +291,10 @@ class Oracle:
                                      rows.size, _ptr(dx), _ptr(L))
         return dx, L
 
-    def gemm_wgrad(self, dyq, sdy, xq, sx):
+    def gemm_wgrad(self, dyq, sdy, xq, sx, rows=None):
         """dW = dY^T X from 128x1-grouped dyq [M, N] / sdy and xq [M, K] / sx
-        (act_quant_cols): (dw, L) fp64 [N, K]."""
+        (act_quant_cols): (dw, L) fp64 [N, K], or [len(rows), K] for the
+        listed rows n of dW."""
         dyq = np.ascontiguousarray(dyq, dtype=np.uint8)
         sdy = np.ascontiguousarray(sdy, dtype=np.float32)
         xq = np.ascontiguousarray(xq, dtype=np.uint8)
@@ -301,9 +303,16 @@ class Oracle:
         M2, K = xq.shape
         MB = (M + 127) // 128
         assert M2 == M and sdy.shape == (MB, N) and sx.shape == (MB, K)
-        dw = np.empty((N, K), dtype=np.float64)
-        L = np.empty((N, K), dtype=np.float64)
-        self.lib.orc_gemm_wgrad(_ptr(dyq), N, _ptr(sdy), _ptr(xq), K, _ptr(sx), M, N, K, _ptr(dw), _ptr(L))
+        if rows is None:
+            dw = np.empty((N, K), dtype=np.float64)
+            L = np.empty((N, K), dtype=np.float64)
+            self.lib.orc_gemm_wgrad(_ptr(dyq), N, _ptr(sdy), _ptr(xq), K, _ptr(sx), M, N, K, _ptr(dw), _ptr(L))
+            return dw, L
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        dw = np.empty((rows.size, K), dtype=np.float64)
+        L = np.empty((rows.size, K), dtype=np.float64)
+        self.lib.orc_gemm_wgrad_rows(_ptr(dyq), N, _ptr(sdy), _ptr(xq), K, _ptr(sx), M, N, K, _ptr(rows), rows.size,
+                                     _ptr(dw), _ptr(L))
         return dw, L
 
 

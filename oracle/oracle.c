@@ -663,32 +663,72 @@ void orc_gemm_dgrad_rows(const uint8_t* dyq, int64_t ldq, const float* sdy, int6
  * exact fp64 per block (a block holds at most 128 products).  dyq [M, N]
  * row stride ldd, sdy [ceil(M/128), N]; xq [M, K] row stride ldx,
  * sx [ceil(M/128), K] (both from orc_act_quant_cols); the last block of
- * tokens may be ragged.  dw and L are [N, K]. */
-void orc_gemm_wgrad(const uint8_t* dyq, int64_t ldd, const float* sdy, const uint8_t* xq, int64_t ldx,
-                    const float* sx, int64_t M, int64_t N, int64_t K, double* dw, double* L) {
+ * tokens may be ragged.  Only the listed rows n of dW are computed; dw and
+ * L are [nrows, K].  Each element's sums run over m in ascending order as
+ * written; the loop over k is innermost only so that xq is read along its
+ * rows (the order of the terms of any one element is unchanged).  Built
+ * with -fopenmp the listed rows are shared out between threads. */
+void orc_gemm_wgrad_rows(const uint8_t* dyq, int64_t ldd, const float* sdy, const uint8_t* xq, int64_t ldx,
+                         const float* sx, int64_t M, int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
+                         double* dw, double* L) {
     int64_t MB = (M + ORC_BLOCK - 1) / ORC_BLOCK;
 #if ORC_MUTANT == 15
     if (M % ORC_BLOCK) MB -= 1; /* mutant: a ragged last block of tokens dropped */
 #endif
-    for (int64_t n = 0; n < N; n++) {
-        for (int64_t k = 0; k < K; k++) {
-            double acc = 0.0, lsum = 0.0;
+    double dec[256];
+    for (int c = 0; c < 256; c++)
+        dec[c] = orc_e4m3_decode((uint8_t)c);
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        double* b = (double*)malloc(sizeof(double) * (size_t)K * 2);
+        double* babs = b + K;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t r = 0; r < nrows; r++) {
+            int64_t n = rows[r];
+            double* acc = dw + r * K;
+            double* lsum = L + r * K;
+            for (int64_t k = 0; k < K; k++) {
+                acc[k] = 0.0;
+                lsum[k] = 0.0;
+            }
             for (int64_t mb = 0; mb < MB; mb++) {
                 int64_t m0 = mb * ORC_BLOCK, m1 = m0 + ORC_BLOCK < M ? m0 + ORC_BLOCK : M;
-                double b = 0.0, babs = 0.0;
-                for (int64_t m = m0; m < m1; m++) {
-                    double p = orc_e4m3_decode(dyq[m * ldd + n]) * orc_e4m3_decode(xq[m * ldx + k]);
-                    b += p;
-                    babs += fabs(p);
+                for (int64_t k = 0; k < K; k++) {
+                    b[k] = 0.0;
+                    babs[k] = 0.0;
                 }
-                double scale = (double)sdy[mb * N + n] * (double)sx[mb * K + k];
-                acc += scale * b;
-                lsum += fabs(scale) * babs;
+                for (int64_t m = m0; m < m1; m++) {
+                    double dy = dec[dyq[m * ldd + n]];
+                    const uint8_t* xr = xq + m * ldx;
+                    for (int64_t k = 0; k < K; k++) {
+                        double p = dy * dec[xr[k]];
+                        b[k] += p;
+                        babs[k] += fabs(p);
+                    }
+                }
+                for (int64_t k = 0; k < K; k++) {
+                    double scale = (double)sdy[mb * N + n] * (double)sx[mb * K + k];
+                    acc[k] += scale * b[k];
+                    lsum[k] += fabs(scale) * babs[k];
+                }
             }
-            dw[n * K + k] = acc;
-            L[n * K + k] = lsum;
         }
+        free(b);
     }
+}
+
+/* wgrad over every row n: dw and L are [N, K]. */
+void orc_gemm_wgrad(const uint8_t* dyq, int64_t ldd, const float* sdy, const uint8_t* xq, int64_t ldx,
+                    const float* sx, int64_t M, int64_t N, int64_t K, double* dw, double* L) {
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+    for (int64_t n = 0; n < N; n++)
+        rows[n] = n;
+    orc_gemm_wgrad_rows(dyq, ldd, sdy, xq, ldx, sx, M, N, K, rows, N, dw, L);
+    free(rows);
 }
 
 int orc_mutant_id(void) { return ORC_MUTANT; }

@@ -43,3 +43,17 @@ def test_threaded_grouped_equals_single_threaded(orc, orc_mt):
             yd, _ = orc.gemm(xq[r0:r1], sx[r0:r1], wq[g], sw[g])
             pos = np.nonzero((rows >= r0) & (rows < r1))[0]
             assert np.array_equal(y1[pos], yd[rows[pos] - r0])
+
+
+def test_threaded_wgrad_equals_single_threaded(orc, orc_mt):
+    rng = np.random.default_rng(13)
+    M, N, K = 300, 136, 256   # a ragged last block of tokens
+    dy = synth.activations(rng, M, N, n_outlier=3, outlier_scale=10.0)
+    x = synth.activations(rng, M, K)
+    dyq, sdy = orc.act_quant_cols(dy)
+    xq, sx = orc.act_quant_cols(x)
+    dw1, L1 = orc.gemm_wgrad(dyq, sdy, xq, sx)
+    rows = np.array([5, 0, 135, 64], dtype=np.int64)
+    dw2, L2 = orc_mt.gemm_wgrad(dyq, sdy, xq, sx, rows=rows)
+    assert np.array_equal(dw2.view(np.uint64), dw1[rows].view(np.uint64))
+    assert np.array_equal(L2.view(np.uint64), L1[rows].view(np.uint64))
