@@ -279,6 +279,39 @@ fp8bs_status fp8bs_moe_route(const int32_t* ids, const float* weights, int64_t T
                                       d, cs(stream)));
 }
 
+fp8bs_status fp8bs_act_quant_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt, int64_t ldt,
+                                  float* sc, int64_t ldsc, fp8bs_stream_t stream) {
+    if (M < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+    if (K % 64) return FP8BS_ERR_UNSUPPORTED;
+    if (M == 0 || K == 0) return FP8BS_OK;
+    if (M > kMaxRows || K > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
+    if (!x || !xqt || !sc) return FP8BS_ERR_INVALID_ARG;
+    if (ldx < K || ldt < M || ldsc < K) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xqt) || ldx % 8 || ldt % 16 || (reinterpret_cast<uintptr_t>(sc) & 3u))
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_act_quant_cols(x, M, K, ldx, xqt, ldt, sc, ldsc, d, cs(stream)));
+}
+
+fp8bs_status fp8bs_gemm_wgrad(const uint8_t* dyqt, int64_t lddyt, const float* sdy, int64_t ldsdy, const uint8_t* xqt,
+                              int64_t ldxt, const float* sx, int64_t ldsx, int64_t T, int64_t N, int64_t K, float* dw,
+                              int64_t lddw, fp8bs_stream_t stream) {
+    if (T < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return FP8BS_OK;
+    if (T == 0) return FP8BS_ERR_INVALID_ARG;  // an empty sum: no tokens to contract over
+    if (T > kMaxRows || N > kMaxRows || K > kMaxRows) return FP8BS_ERR_UNSUPPORTED;
+    if (!dyqt || !sdy || !xqt || !sx || !dw) return FP8BS_ERR_INVALID_ARG;
+    if (lddyt < T || ldxt < T || ldsdy < N || ldsx < K || lddw < K) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(dyqt) || !aligned16(xqt) || !aligned16(sdy) || !aligned16(sx) || !aligned16(dw) || lddyt % 16 ||
+        ldxt % 16 || ldsdy % 4 || ldsx % 4 || lddw % 4)
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    WgradArgs a{dyqt, lddyt, sdy, ldsdy, xqt, ldxt, sx, ldsx, T, N, K, dw, lddw};
+    return from_cuda(launch_wgrad(a, d, cs(stream)));
+}
+
 fp8bs_status fp8bs_sync_status(fp8bs_stream_t stream) {
     if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
     DeviceInfo d;

@@ -130,7 +130,11 @@ struct Layout {
     static constexpr int EPI_WARPS = BN == 256 ? 8 : 0;
     static constexpr int OFF_EPI = (OFF_HAMAX + HAMAX_BYTES + 1023) & ~1023;
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * 1024;
-    static constexpr int BYTES = OFF_EPI + EPI_BYTES;
+    // weight gradient (160-column tiles): per scale slot the column factors
+    // of the tile's BN columns for kScaleChunks token chunks ([chunk][column])
+    static constexpr int CF_SLOT = BN == 160 ? kScaleChunks * BN * 4 : 0;
+    static constexpr int OFF_CF = (OFF_EPI + EPI_BYTES + 127) & ~127;
+    static constexpr int BYTES = OFF_CF + kScaleSlots * CF_SLOT;
     static constexpr int ALLOC = BYTES + 1024;                    // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;                  // allocation: a power of two
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
@@ -162,6 +166,10 @@ struct Params {
     // chunks; split s writes fp32 partial sums to partial[s][M][N]
     int splits, kps;
     float* partial;
+    // weight gradient: dW [M, ldyf] fp32 (M = output rows, N = output columns,
+    // KB = token chunks)
+    float* yf;
+    int64_t ldyf;
     unsigned* err;
     uint64_t timeout_ns;
 };
@@ -273,7 +281,11 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, const 
 // MODE: how tiles map to work.
 // kGroupedSwiglu: grouped, each tile = 128 columns of w1 (gate) next to the
 // same 128 columns of w3 (up), output h = silu(gate) * up.
-enum : int { kDense = 0, kSplitK = 1, kGrouped = 2, kGroupedSwiglu = 3 };
+// kWgrad: the weight gradient dW = dY^T X contracting over tokens; the
+// operands are the column-quantised dY^T and X^T (token-contiguous rows), and
+// the promotion factor of chunk kb (128 tokens) for output (n, k) is
+// RN(sdy[kb][n] * sx[kb][k]), a row factor times a column factor.
+enum : int { kDense = 0, kSplitK = 1, kGrouped = 2, kGroupedSwiglu = 3, kWgrad = 4 };
 __host__ __device__ constexpr bool is_grouped(int mode) { return mode == kGrouped || mode == kGroupedSwiglu; }
 // output columns one tile covers: BN, or 128 h columns for SwiGLU tiles
 template <int BN, int MODE>
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
     if (threadIdx.x == 32) {  // the descriptors are kernel parameters: fetch them while the set-up runs
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (MODE == kGroupedSwiglu) tma_prefetch_desc(&tmB3);
+        if (MODE == kGroupedSwiglu || MODE == kWgrad) tma_prefetch_desc(&tmB3);
         tma_prefetch_desc(&tmS);
         if (BN == 256 && (MODE == kDense || MODE == kGrouped) && p.y != nullptr) tma_prefetch_desc(&tmY);
     }
@@ -479,7 +491,10 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
             const int bi = lane / kScaleChunks;
             bool sw_lane;
             const float* swr;
-            if constexpr (SWIGLU) {  // slot rows 0 and 1: the tile's w1 and w3 blocks
+            if constexpr (MODE == kWgrad) {  // no weight scales: both factors come by TMA
+                sw_lane = false;
+                swr = nullptr;
+            } else if constexpr (SWIGLU) {  // slot rows 0 and 1: the tile's w1 and w3 blocks
                 sw_lane = lane < 2 * kScaleChunks && fb < nblk;
                 swr = (bi == 0 ? p.sw : p.sw3) + static_cast<int64_t>(tl.sw_base + fb) * p.KB;
             } else {
@@ -509,8 +524,17 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                 const uint32_t ph = (sb / kScaleSlots) & 1u;
                 if (!warp_wait(sempty_bar(s), ph ^ 1u, ctl)) { ok = false; break; }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(sfull_bar(s), L::SX_SLOT);
-                    tma_load_2d(sbase + L::OFF_SX + s * L::SX_SLOT, &tmS, sfull_bar(s), q * kScaleChunks, tl.m0);
+                    if constexpr (MODE == kWgrad) {
+                        // row factors sdy[chunk][n] of the tile's 128 rows and
+                        // column factors sx[chunk][k] of its BN columns, for
+                        // kScaleChunks token chunks each
+                        mbar_arrive_expect_tx(sfull_bar(s), L::SX_SLOT + L::CF_SLOT);
+                        tma_load_2d(sbase + L::OFF_SX + s * L::SX_SLOT, &tmS, sfull_bar(s), tl.m0, q * kScaleChunks);
+                        tma_load_2d(sbase + L::OFF_CF + s * L::CF_SLOT, &tmB3, sfull_bar(s), tl.n0, q * kScaleChunks);
+                    } else {
+                        mbar_arrive_expect_tx(sfull_bar(s), L::SX_SLOT);
+                        tma_load_2d(sbase + L::OFF_SX + s * L::SX_SLOT, &tmS, sfull_bar(s), q * kScaleChunks, tl.m0);
+                    }
                 }
                 if (lane < kSwBlocks * kScaleChunks) sw_slots[s * (kSwBlocks * kScaleChunks) + lane] = v;
                 if (p.bias != nullptr && q == tl.kb0 / kScaleChunks) {
@@ -620,6 +644,39 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                             acc[4 * v + t] = pack_f32x2(__uint_as_float(bw[t] << 16), __uint_as_float(bw[t] & 0xFFFF0000u));
                     }
                 }
+                if constexpr (MODE == kWgrad) {
+                    // acc += RN(a * b_col) * P per element: a = sdy[chunk][n] of this
+                    // thread's row, b_col = sx[chunk][k] of each column (slot layout
+                    // [chunk][row] and [chunk][column]).  The column factors are
+                    // read after the TMEM load, so the slot is freed afterwards.
+                    const float a = sx_slots[sl * (BM * kScaleChunks) + c4 * BM + row];
+                    if (!warp_wait(tfull_bar(b), bph, ctl)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t taddr = tmem + t_lane + static_cast<uint32_t>(b * L::BUF_COLS + col0);
+                    static_assert(MODE != kWgrad || WHOLE, "weight-gradient tiles load a whole chunk at once");
+                    uint64_t pr[COLS / 2];
+                    tmem_ld_cols_pairs(taddr, pr);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(b));
+                    const uint4* cf = reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const float*>(smem + L::OFF_CF + sl * L::CF_SLOT) + c4 * BN + col0);
+                    const uint64_t a2 = pack_f32x2(a, a);
+#pragma unroll
+                    for (int v = 0; v < COLS / 4; ++v) {
+                        const uint4 b4 = cf[v];
+                        const uint64_t b01 = (static_cast<uint64_t>(b4.y) << 32) | b4.x;
+                        const uint64_t b23 = (static_cast<uint64_t>(b4.w) << 32) | b4.z;
+                        acc[2 * v] = f2_fma(f2_mul(a2, b01), pr[2 * v], acc[2 * v]);
+                        acc[2 * v + 1] = f2_fma(f2_mul(a2, b23), pr[2 * v + 1], acc[2 * v + 1]);
+                    }
+                    if (c4 == kScaleChunks - 1 || j == nk - 1) {  // the block's last chunk here: free the slot
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(sempty_bar(sl));
+                        ++ss;
+                    }
+                    continue;
+                }
                 const float* swv = sw_slots + sl * (kSwBlocks * kScaleChunks) + c4;
                 const float sxv = sx_slots[sl * (BM * kScaleChunks) + row * kScaleChunks + c4];
                 const float f_lo = __fmul_rn(sxv, swv[i0 * kScaleChunks]);
@@ -727,6 +784,24 @@ __global__ void __launch_bounds__(Roles<nwg_for(BN)>::kThreads, 1)
                     for (int v = 0; v < 8; ++v)
                         *reinterpret_cast<uint4*>(hr + 8 * v) =
                             make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
+                }
+                continue;
+            }
+            if constexpr (MODE == kWgrad) {
+                if (!row_ok) continue;
+                float* yr = p.yf + static_cast<int64_t>(m) * p.ldyf;
+#pragma unroll
+                for (int v = 0; v < COLS / 4; ++v) {
+                    const int n = nbase + 4 * v;
+                    const float q[4] = {lo_f32(acc[2 * v]), hi_f32(acc[2 * v]), lo_f32(acc[2 * v + 1]),
+                                        hi_f32(acc[2 * v + 1])};
+                    if (n + 4 <= p.N) {
+                        *reinterpret_cast<float4*>(yr + n) = make_float4(q[0], q[1], q[2], q[3]);
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            if (n + jj < p.N) yr[n + jj] = q[jj];
+                    }
                 }
                 continue;
             }
@@ -1091,6 +1166,35 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
                           static_cast<const float*>(p.partial), pl.splits, p.M, p.N, a.y, a.ldy);
     }
     return launch_bn<kDense>(pl.bn, a, p, pl.grid, dev, stream);
+}
+
+cudaError_t launch_wgrad(const WgradArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+    constexpr int BN = 160;
+    const int64_t TB = (a.T + 127) / 128;
+    Params p{};
+    p.M = static_cast<int>(a.N);
+    p.N = static_cast<int>(a.K);
+    p.KB = static_cast<int>(TB);
+    p.MT = static_cast<int>((a.N + BM - 1) / BM);
+    p.NT = static_cast<int>((a.K + BN - 1) / BN);
+    p.num_tiles = p.MT * p.NT;
+    p.yf = a.dw;
+    p.ldyf = a.lddw;
+    p.err = dev.err;
+    p.timeout_ns = wait_timeout_ns();
+    CUtensorMap tmA, tmB, tmS, tmC;
+    cudaError_t e;
+    // operands: rows of dY^T and X^T, tokens contiguous (128-token K chunks)
+    if ((e = make_map(&tmA, a.dyqt, a.T, a.N, a.lddyt, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&tmB, a.xqt, a.T, a.K, a.ldxt, BN)) != cudaSuccess) return e;
+    // row factors sdy [TB, N] and column factors sx [TB, K]: boxes of one
+    // tile's rows (columns) for kScaleChunks token chunks
+    if ((e = make_tmap_2d(&tmS, a.sdy, 4, a.N, TB, a.ldsdy * 4, BM, kScaleChunks, 0)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&tmC, a.sx, 4, a.K, TB, a.ldsx * 4, BN, kScaleChunks, 0)) != cudaSuccess) return e;
+    if ((e = ensure_kernel_ready<BN, kStages160, kWgrad>(dev.device)) != cudaSuccess) return e;
+    const int grid = std::min(p.num_tiles, dev.num_sms);
+    return launch_pdl(fp8_gemm_kernel<BN, kStages160, kWgrad>, dim3(grid), dim3(Roles<nwg_for(BN)>::kThreads),
+                      Layout<BN, kStages160>::ALLOC, stream, tmA, tmB, tmC, tmS, tmA, p);
 }
 
 }  // namespace fp8bs

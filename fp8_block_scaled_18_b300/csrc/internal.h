@@ -115,4 +115,28 @@ struct GemmArgs {
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
+// Weight gradient dW [N, K] fp32 = dY^T X over T tokens from the column-
+// quantised (128x1 groups along the tokens) operands, stored transposed:
+// dyqt [N, lddyt] and xqt [K, ldxt] e4m3 (row = one channel's T tokens),
+// sdy [ceil(T/128), ldsdy] and sx [ceil(T/128), ldsx] fp32 (gemm.cu).
+struct WgradArgs {
+    const uint8_t* dyqt;
+    int64_t lddyt;
+    const float* sdy;
+    int64_t ldsdy;
+    const uint8_t* xqt;
+    int64_t ldxt;
+    const float* sx;
+    int64_t ldsx;
+    int64_t T, N, K;
+    float* dw;
+    int64_t lddw;
+};
+cudaError_t launch_wgrad(const WgradArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// 128x1 column quantisation: per column k and per block of 128 rows, amax,
+// s = amax / 448 and the codes, written transposed: xqt[k, m] (quant.cu).
+cudaError_t launch_act_quant_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt, int64_t ldt,
+                                  float* sc, int64_t ldsc, const DeviceInfo& dev, cudaStream_t stream);
+
 }  // namespace fp8bs

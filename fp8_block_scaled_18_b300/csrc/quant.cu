@@ -197,6 +197,85 @@ __global__ void wait_selftest_kernel(unsigned* err, uint64_t timeout_ns) {
     if (!ok && threadIdx.x == 0) atomicOr(err, DEVERR_SELFTEST);
 }
 
+// ---------------------------------------------------------------- act_quant_cols
+//
+// 128x1 groups (the weight gradient's operands, quantised along the tokens):
+// for each column k and each block of 128 rows, amax over the block's valid
+// rows, s = amax / 448, and the codes written transposed, xqt[k, m], so that
+// each output row holds one channel's tokens contiguously (the layout the
+// weight-gradient GEMM contracts over).  A CTA takes tiles of 128 rows x 64
+// columns: the tile is read with 16-byte loads into shared memory, then
+// thread (c, g) takes column c and rows 32g .. 32g+31, reduces their amax,
+// combines the four partial amaxes of its column through shared memory,
+// encodes its 32 values with the act_quant arithmetic and stores its 32
+// codes -- contiguous in the transposed output -- as two 16-byte stores.
+constexpr int kCqRows = 128;
+constexpr int kCqCols = 64;
+
+__global__ void __launch_bounds__(256) act_quant_cols_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                            int64_t ldx, uint8_t* __restrict__ xqt, int64_t ldt,
+                                                            float* __restrict__ sc, int64_t ldsc) {
+    __shared__ __align__(16) uint16_t tile[kCqRows][kCqCols];
+    __shared__ uint32_t pam[4][kCqCols];
+    grid_dependency_wait();  // the previous kernel may still read xqt / sc
+    allow_dependents();
+    const int t = threadIdx.x;
+    const int c = t % kCqCols;   // column within the tile
+    const int g = t / kCqCols;   // row group of 32
+    const int64_t MB = (M + kCqRows - 1) / kCqRows;
+    const int64_t CB = K / kCqCols;
+    for (int64_t tt = blockIdx.x; tt < MB * CB; tt += gridDim.x) {
+        const int64_t mb = tt / CB;
+        const int64_t k0 = (tt - mb * CB) * kCqCols;
+        const int64_t m0 = mb * kCqRows;
+        __syncthreads();  // the previous tile's reads of `tile` and `pam` are done
+        // 128 rows x 128 bytes: four 16-byte chunks per thread, eight threads per row
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int q = t + 256 * i;
+            const int r = q / 8, ch = q % 8;
+            uint4 v = make_uint4(0, 0, 0, 0);  // rows past M are zeros (they never raise the amax)
+            if (m0 + r < M) v = ld_stream(x + (m0 + r) * ldx + k0 + ch * 8);
+            *reinterpret_cast<uint4*>(&tile[r][ch * 8]) = v;
+        }
+        __syncthreads();
+        uint4 v[4];  // rows 32g + 8j .. +7 of column c, as 8 bf16 values each
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int r = 32 * g + 8 * j + 2 * h;
+                w[h] = static_cast<uint32_t>(tile[r][c]) | (static_cast<uint32_t>(tile[r + 1][c]) << 16);
+            }
+            v[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        uint32_t amax2 = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) amax2 = absmax_bits8(v[j], amax2);
+        pam[g][c] = amax2;
+        __syncthreads();
+        amax2 = __vmaxu2(__vmaxu2(pam[0][c], pam[1][c]), __vmaxu2(pam[2][c], pam[3][c]));
+        const float amax = bits_to_amax(amax2);
+        const GroupScale gs = group_scale(amax);
+        const bool zero = amax == 0.0f;
+        uint2 codes[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) codes[j] = encode8(v[j], gs, zero);
+        const int64_t mrow = m0 + 32 * g;  // first token of this thread's 32 codes
+        uint8_t* out = xqt + (k0 + c) * ldt + mrow;
+        if (mrow + 32 <= M) {
+            *reinterpret_cast<uint4*>(out) = make_uint4(codes[0].x, codes[0].y, codes[1].x, codes[1].y);
+            *reinterpret_cast<uint4*>(out + 16) = make_uint4(codes[2].x, codes[2].y, codes[3].x, codes[3].y);
+        } else if (mrow < M) {  // the ragged last block: only the tokens that exist
+            const uint32_t wds[8] = {codes[0].x, codes[0].y, codes[1].x, codes[1].y,
+                                     codes[2].x, codes[2].y, codes[3].x, codes[3].y};
+            for (int b = 0; b < static_cast<int>(M - mrow); ++b) out[b] = static_cast<uint8_t>(wds[b / 4] >> (8 * (b % 4)));
+        }
+        if (g == 0) sc[mb * ldsc + k0 + c] = gs.s;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq,
@@ -238,6 +317,14 @@ cudaError_t launch_e4m3_encode(const float* v, int64_t n, uint8_t* q, const Devi
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, const DeviceInfo& dev, cudaStream_t stream) {
     wait_selftest_kernel<<<1, 32, 0, stream>>>(dev.err, timeout_ns);
     return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt, int64_t ldt,
+                                  float* sc, int64_t ldsc, const DeviceInfo& dev, cudaStream_t stream) {
+    const int64_t tiles = ((M + kCqRows - 1) / kCqRows) * (K / kCqCols);
+    const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 4;
+    const int blocks = static_cast<int>(tiles < max_blocks ? tiles : max_blocks);
+    return launch_pdl(act_quant_cols_kernel, dim3(blocks), dim3(256), 0, stream, x, M, K, ldx, xqt, ldt, sc, ldsc);
 }
 
 }  // namespace fp8bs

@@ -37,6 +37,8 @@ _SIGS = {
     "fp8bs_gemm_noalloc": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm": (_ST, [_P, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm_workspace_size": (_SZ, [_I32, _I64, _I64]),
+    "fp8bs_act_quant_cols": (_ST, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
+    "fp8bs_gemm_wgrad": (_ST, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8bs_grouped_gemm_swiglu": (_ST, [_P, _P, _I64, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P,
                                         _I64, _P, _I64, _P]),
     "fp8bs_moe_dispatch": (_ST, [_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
@@ -228,6 +230,37 @@ def fp8bs_gemm_noalloc(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw:
                                   _dev(sw, torch.float32, "sw"), M, N, K, _bf16_ptr(y, "y"),
                                   _rows_stride(y, "y"), _stream(stream)), "fp8bs_gemm_noalloc")
     return y
+
+
+def fp8bs_act_quant_cols(x: torch.Tensor, xqt: Optional[torch.Tensor] = None, sc: Optional[torch.Tensor] = None,
+                         stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """x [M, K] bf16 -> (xqt [K, ldt] e4m3, the codes transposed, ldt = M
+    rounded up to 16; sc [ceil(M/128), K] fp32): 128x1 groups along the rows."""
+    M, K = x.shape
+    if xqt is None:
+        xqt = torch.empty((K, (M + 15) // 16 * 16), dtype=torch.uint8, device=x.device)
+    if sc is None:
+        sc = torch.empty(((M + 127) // 128, K), dtype=torch.float32, device=x.device)
+    _check(lib.fp8bs_act_quant_cols(_bf16_ptr(x, "x"), M, K, _rows_stride(x, "x"), _dev(xqt, torch.uint8, "xqt"),
+                                    _rows_stride(xqt, "xqt"), _dev(sc, torch.float32, "sc"), _rows_stride(sc, "sc"),
+                                    _stream(stream)), "fp8bs_act_quant_cols")
+    return xqt, sc
+
+
+def fp8bs_gemm_wgrad(dyqt: torch.Tensor, sdy: torch.Tensor, xqt: torch.Tensor, sx: torch.Tensor, T: int,
+                     dw: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """dW [N, K] fp32 = dY^T X over T tokens from fp8bs_act_quant_cols of dY
+    (dyqt [N, >=T], sdy) and of X (xqt [K, >=T], sx)."""
+    N, K = dyqt.shape[0], xqt.shape[0]
+    if dw is None:
+        dw = torch.empty((N, (K + 3) // 4 * 4), dtype=torch.float32, device=dyqt.device)[:, :K]
+    _check(lib.fp8bs_gemm_wgrad(_dev(dyqt, torch.uint8, "dyqt"), _rows_stride(dyqt, "dyqt"),
+                                _dev(sdy, torch.float32, "sdy"), _rows_stride(sdy, "sdy"),
+                                _dev(xqt, torch.uint8, "xqt"), _rows_stride(xqt, "xqt"),
+                                _dev(sx, torch.float32, "sx"), _rows_stride(sx, "sx"), T, N, K,
+                                _dev(dw, torch.float32, "dw"), _rows_stride(dw, "dw"), _stream(stream)),
+           "fp8bs_gemm_wgrad")
+    return dw
 
 
 def fp8bs_grouped_gemm_workspace_size(G: int, N: int, K: int) -> int:

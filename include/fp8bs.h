@@ -190,6 +190,41 @@ fp8bs_status fp8bs_gemm_noalloc(const uint8_t* xq, const float* sx, int64_t lds,
                                 int64_t M, int64_t N, int64_t K,
                                 uint16_t* y, int64_t ldy, fp8bs_stream_t stream);
 
+/* Backward pass, weight gradient (E4M3 in the backward pass as well as the
+ * forward: the Float8 paragraph of the 88811315.cn post on DeepSeek v3).
+ * dW = dY^T X contracts over the tokens, so both operands are quantised in
+ * 128x1 groups along the tokens -- the contraction dimension of this GEMM,
+ * as the forward groups its operands along K.
+ *
+ * act_quant_cols: per column k and per block of 128 rows (the last block may
+ * be ragged: its amax is over the rows that exist), amax = max |x|,
+ * s = amax / 448, codes e4m3(x / s) exactly as fp8bs_act_quant computes them,
+ * written TRANSPOSED so that each channel's tokens are contiguous:
+ *   x   [M, K] bf16, row stride ldx (ldx % 8 == 0, 16-byte aligned)
+ *   xqt [K, ldt] e4m3: xqt[k*ldt + m] = code of x[m, k] (ldt >= M,
+ *       ldt % 16 == 0, 16-byte aligned); bytes m >= M of a row are untouched
+ *   sc  [ceil(M/128), ldsc] fp32: sc[mb*ldsc + k] = s of column k, block mb
+ *       (ldsc >= K, 4-byte aligned)
+ * K % 64 == 0 (else FP8BS_ERR_UNSUPPORTED); M == 0 or K == 0 is a no-op. */
+fp8bs_status fp8bs_act_quant_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                  uint8_t* xqt, int64_t ldt, float* sc, int64_t ldsc,
+                                  fp8bs_stream_t stream);
+
+/* gemm_wgrad: dW[n, k] = sum_tb fp32(sdy[tb, n] * sx[tb, k]) * P_tb[n, k],
+ * P_tb the sum over the 128 tokens of block tb of dec(dy code) * dec(x code),
+ * accumulated in fp32 and promoted once per token block (as fp8bs_gemm
+ * promotes once per 128-wide K chunk); dW in fp32.
+ *   dyqt [N, lddyt], sdy [ceil(T/128), ldsdy]: fp8bs_act_quant_cols of dY [T, N]
+ *   xqt  [K, ldxt],  sx  [ceil(T/128), ldsx]:  fp8bs_act_quant_cols of X  [T, K]
+ *   dw   [N, lddw] fp32 (lddw >= K, lddw % 4 == 0, 16-byte aligned)
+ * T >= 1 tokens (T == 0: FP8BS_ERR_INVALID_ARG); N or K == 0 is a no-op.
+ * Code row strides % 16 == 0 and >= T, scale row strides % 4 == 0, all base
+ * pointers 16-byte aligned.  Tokens past T read as zero codes. */
+fp8bs_status fp8bs_gemm_wgrad(const uint8_t* dyqt, int64_t lddyt, const float* sdy, int64_t ldsdy,
+                              const uint8_t* xqt, int64_t ldxt, const float* sx, int64_t ldsx,
+                              int64_t T, int64_t N, int64_t K, float* dw, int64_t lddw,
+                              fp8bs_stream_t stream);
+
 /* MoE expert first stage with the SwiGLU activation fused (the pages' Expert
  * forward, "DeepSeek-V3" repository overview, MoE section: w2(silu(w1(x)) *
  * w3(x)); this call computes the part before w2).  For each expert g and

@@ -125,6 +125,34 @@ def test_gemm_noalloc_validation():
     assert f(A, A, 4, None, A, 4, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG
 
 
+def test_backward_calls_validation():
+    """The column quantiser and the weight-gradient GEMM reject bad arguments
+    before any CUDA call."""
+    q = lib.fp8bs_act_quant_cols
+    assert q(A, 4, 100, 128, A, 16, A, 128, None) == fp8bs.FP8BS_ERR_UNSUPPORTED     # K % 64
+    assert q(A, -1, 64, 64, A, 16, A, 64, None) == fp8bs.FP8BS_ERR_INVALID_ARG
+    assert q(A, 0, 64, 64, A, 16, A, 64, None) == fp8bs.FP8BS_OK                     # empty: a no-op
+    assert q(A, 40, 64, 64, A, 32, A, 64, None) == fp8bs.FP8BS_ERR_INVALID_ARG       # ldt < M
+    assert q(A, 40, 64, 64, A, 40, A, 64, None) == fp8bs.FP8BS_ERR_MISALIGNED        # ldt % 16
+    assert q(A, 40, 64, 60, A, 48, A, 64, None) == fp8bs.FP8BS_ERR_INVALID_ARG       # ldx < K
+    g = lib.fp8bs_gemm_wgrad
+    ok = [A, 32, A, 64, A, 32, A, 128, 32, 64, 128, A, 128, None]
+    bad = list(ok); bad[8] = 0
+    assert g(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                      # T == 0
+    bad = list(ok); bad[9] = 0
+    assert g(*bad) == fp8bs.FP8BS_OK                                                   # N == 0: a no-op
+    bad = list(ok); bad[1] = 24
+    assert g(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG                                      # lddyt < T
+    bad = list(ok); bad[1] = 40
+    assert g(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                       # lddyt % 16
+    bad = list(ok); bad[7] = 130
+    assert g(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                       # ldsx % 4
+    bad = list(ok); bad[11] = A + 4
+    assert g(*bad) == fp8bs.FP8BS_ERR_MISALIGNED                                       # dw alignment
+    bad = list(ok); bad[2] = None
+    assert g(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG
+
+
 def test_grouped_validation():
     gg = lib.fp8bs_grouped_gemm
     assert gg(A, A, 4, A, A, None, 4, 16, 8, 128, A, 8, None) == fp8bs.FP8BS_ERR_INVALID_ARG
