@@ -56,6 +56,7 @@ def load(mutant: int = 0, omp: bool = False) -> ctypes.CDLL:
             "orc_moe_route": [_P, _P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P],
             "orc_act_quant_cols": [_P, _I64, _I64, _I64, _P, _I64, _P],
             "orc_act_quant_pow2": [_P, _I64, _I64, _I64, _P, _I64, _P, _I64],
+            "orc_weight_quant_pow2": [_P, _I64, _I64, _P, _P],
             "orc_gemm_dgrad_rows": [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P],
             "orc_gemm_wgrad": [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _P, _P],
             "orc_gemm_wgrad_rows": [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P],
@@ -263,6 +264,15 @@ class Oracle:
         sx = np.zeros((M, lds), dtype=np.float32)
         self.lib.orc_act_quant_pow2(_ptr(x), M, K, K, _ptr(xq), K, _ptr(sx), lds)
         return xq, sx
+
+    def weight_quant_pow2(self, w_bits):
+        """weight_quant with power-of-two (UE8M0-style) scales, rounded up."""
+        w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+        N, K = w.shape
+        wq = np.zeros((N, K), dtype=np.uint8)
+        sw = np.zeros(((N + 127) // 128, K // 128), dtype=np.float32)
+        self.lib.orc_weight_quant_pow2(_ptr(w), N, K, _ptr(wq), _ptr(sw))
+        return wq, sw
 
     def act_quant_cols(self, x_bits):
         """x [M, K] bf16 bits -> (xq [M, K] u8, sx [ceil(M/128), K] fp32):

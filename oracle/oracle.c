@@ -547,13 +547,26 @@ void orc_moe_route(const int32_t* ids, const float* w, int64_t T, int32_t top_k,
     free(next);
 }
 
-/* act_quant with power-of-two scales: the pages pass a scale format
- * (scale_fmt) to act_quant without defining it ("DeepSeek-V3" repository
- * overview, the linear() excerpt).  Reading: a UE8M0-style scale, an
- * unsigned power of two with no mantissa, rounded up so that nothing
- * saturates -- s = 2^e with e the smallest integer such that
- * amax <= 448 * 2^e; then x / s is exact and q = e4m3(x / s) only rounds.
- * An all-zero group has s = 0 (R4).  Layout as orc_act_quant. */
+/* Power-of-two scales: the pages pass a scale format (scale_fmt) to
+ * act_quant without defining it ("DeepSeek-V3" repository overview, the
+ * linear() excerpt).  Reading: a UE8M0-style scale, an unsigned power of two
+ * with no mantissa, rounded up so that nothing saturates -- s = 2^e with e
+ * the smallest integer such that amax <= 448 * 2^e; then x / s is exact and
+ * q = e4m3(x / s) only rounds.  An all-zero group or block has s = 0 (R4). */
+static float orc_pow2_scale(float amax) {
+    if (amax == 0.0f)
+        return 0.0f;
+    int e;
+    frexp((double)amax / 448.0, &e);        /* 2^(e-1) <= amax/448 < 2^e, up to rounding */
+    e -= 2;                                 /* step up from below with exact comparisons */
+    while (ldexp(448.0, e) < (double)amax) e++;
+#if ORC_MUTANT == 16
+    e -= 1;                                 /* mutant: rounded down (the top codes saturate) */
+#endif
+    return (float)ldexp(1.0, e);
+}
+
+/* act_quant with power-of-two scales; layout as orc_act_quant. */
 void orc_act_quant_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq, float* sx,
                         int64_t lds) {
     int64_t G = K / ORC_BLOCK;
@@ -562,22 +575,35 @@ void orc_act_quant_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, ui
             const uint16_t* xg = x + m * ldx + g * ORC_BLOCK;
             float amax = 0.0f;
             for (int k = 0; k < ORC_BLOCK; k++) amax = fmaxf(amax, fabsf(orc_bf16_to_f32(xg[k])));
-            float s = 0.0f;
-            if (amax > 0.0f) {
-                int e;
-                frexp((double)amax / 448.0, &e);        /* 2^(e-1) <= amax/448 < 2^e, up to rounding */
-                e -= 2;                                 /* step up from below with exact comparisons */
-                while (ldexp(448.0, e) < (double)amax) e++;
-#if ORC_MUTANT == 16
-                e -= 1;                                 /* mutant: rounded down (the top codes saturate) */
-#endif
-                s = (float)ldexp(1.0, e);
-            }
+            float s = orc_pow2_scale(amax);
             for (int k = 0; k < ORC_BLOCK; k++) {
                 float v = orc_bf16_to_f32(xg[k]);
                 xq[m * ldq + g * ORC_BLOCK + k] = amax == 0.0f ? (signbit(v) ? 0x80 : 0x00) : orc_e4m3_encode(v / s);
             }
             sx[m * lds + g] = s;
+        }
+    }
+}
+
+/* weight_quant with power-of-two scales: per 128x128 block (the ragged last
+ * row block over its valid rows, R6) s = 2^e as above, q = e4m3(w / s).
+ * Layout as orc_weight_quant. */
+void orc_weight_quant_pow2(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw) {
+    int64_t NB = (N + ORC_BLOCK - 1) / ORC_BLOCK, KB = K / ORC_BLOCK;
+    for (int64_t nb = 0; nb < NB; nb++) {
+        int64_t n_end = (nb + 1) * ORC_BLOCK < N ? (nb + 1) * ORC_BLOCK : N;
+        for (int64_t kb = 0; kb < KB; kb++) {
+            float amax = 0.0f;
+            for (int64_t n = nb * ORC_BLOCK; n < n_end; n++)
+                for (int64_t k = kb * ORC_BLOCK; k < (kb + 1) * ORC_BLOCK; k++)
+                    amax = fmaxf(amax, fabsf(orc_bf16_to_f32(w[n * K + k])));
+            float s = orc_pow2_scale(amax);
+            for (int64_t n = nb * ORC_BLOCK; n < n_end; n++)
+                for (int64_t k = kb * ORC_BLOCK; k < (kb + 1) * ORC_BLOCK; k++) {
+                    float v = orc_bf16_to_f32(w[n * K + k]);
+                    wq[n * K + k] = amax == 0.0f ? (signbit(v) ? 0x80 : 0x00) : orc_e4m3_encode(v / s);
+                }
+            sw[nb * KB + kb] = s;
         }
     }
 }

@@ -702,6 +702,43 @@ def pin_act_quant_pow2(o):
     assert s1[0, 0] == s2[0, 0] == np.float32(2.0 ** -5) and np.array_equal(q1, q2)
 
 
+def pin_weight_quant_pow2(o):
+    """Power-of-two weight scales per 128x128 block: against exact rationals
+    (s a power of two with s/2 < amax/448 <= s over the block's valid rows),
+    the codes ml_dtypes' round-to-nearest-even e4m3 of the exact quotient; a
+    ragged last row block equals the zero-padded one; a block whose amax is
+    448 * 2^a matches the fp32-scale path; an all-zero block has s = 0."""
+    rng = np.random.default_rng(31)
+    w = synth.normal_bf16(rng, (200, 384), 0.02)
+    w[0:128, 128:256] = 0
+    w[150, 300] = bf16_bits(np.array([[7.5]], dtype=np.float32))[0, 0]   # an outlier in the ragged block
+    wq, sw = o.weight_quant_pow2(w)
+    wf = f32_of_bf16(w).astype(np.float64)
+    for nb in range(2):
+        for kb in range(3):
+            blk = wf[128 * nb:min(200, 128 * (nb + 1)), 128 * kb:128 * (kb + 1)]
+            qb = wq[128 * nb:min(200, 128 * (nb + 1)), 128 * kb:128 * (kb + 1)]
+            amax = np.abs(blk).max()
+            s = float(sw[nb, kb])
+            if amax == 0:
+                assert s == 0.0 and not (qb & 0x7F).any()
+                continue
+            mant, _ = np.frexp(s)
+            assert mant == 0.5, "scale is not a power of two"
+            assert Fraction(s) / 2 < Fraction(amax) / 448 <= Fraction(s)
+            assert np.array_equal(qb, e4m3_code_lib(blk / s))
+    wp = np.zeros((256, 384), dtype=np.uint16)
+    wp[:200] = w
+    wq_p, sw_p = o.weight_quant_pow2(wp)
+    assert np.array_equal(wq_p[:200], wq) and np.array_equal(sw_p.view(np.uint32), sw.view(np.uint32))
+    v = e4m3_values()
+    codes = np.stack([_pos_codes_with_max(rng, 128) for _ in range(128)])
+    blk = bf16_bits((v[codes] * 2.0 ** -3).astype(np.float32))
+    q1, s1 = o.weight_quant_pow2(blk)
+    q2, s2 = o.weight_quant(blk)
+    assert s1[0, 0] == s2[0, 0] == np.float32(2.0 ** -3) and np.array_equal(q1, q2)
+
+
 ALL_PINS = [
     pin_codec_midpoints,
     pin_act_quant_rank1,
@@ -726,4 +763,5 @@ ALL_PINS = [
     pin_gemm_dgrad,
     pin_gemm_wgrad,
     pin_act_quant_pow2,
+    pin_weight_quant_pow2,
 ]
