@@ -62,6 +62,33 @@ fp8bs_status fp8bs_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t
     return from_cuda(launch_weight_quant(w, N, K, wq, sw, d, cs(stream)));
 }
 
+fp8bs_status fp8bs_act_quant_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq,
+                                  float* sx, int64_t lds, fp8bs_stream_t stream) {
+    if (M < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (M == 0) return FP8BS_OK;
+    if (!x || !xq || !sx) return FP8BS_ERR_INVALID_ARG;
+    if (ldx < K || ldq < K || lds < K / 128) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(sx) || ldx % 8 || ldq % 16 || lds % 4)
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_act_quant(x, M, K, ldx, xq, ldq, sx, lds, d, cs(stream), true));
+}
+
+fp8bs_status fp8bs_weight_quant_pow2(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
+                                     fp8bs_stream_t stream) {
+    if (N < 0) return FP8BS_ERR_INVALID_ARG;
+    if (fp8bs_status st = check_k(K)) return st;
+    if (N == 0) return FP8BS_OK;
+    if (!w || !wq || !sw) return FP8BS_ERR_INVALID_ARG;
+    if ((N + 127) / 128 > kMaxGridY) return FP8BS_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return FP8BS_ERR_MISALIGNED;
+    DeviceInfo d;
+    if (fp8bs_status st = device(&d)) return st;
+    return from_cuda(launch_weight_quant(w, N, K, wq, sw, d, cs(stream), true));
+}
+
 fp8bs_status fp8bs_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
                                   fp8bs_stream_t stream) {
     if (N < 0) return FP8BS_ERR_INVALID_ARG;

@@ -67,6 +67,39 @@ __device__ __forceinline__ GroupScale group_scale(float amax) {
     return g;
 }
 
+// Power-of-two (UE8M0-style) scale of a group or block, rounded up so that
+// nothing saturates: s = 2^e with e the smallest integer such that
+// amax <= 448 * 2^e (the scale_fmt reading of the linear() excerpt, "DeepSeek-V3"
+// repository overview).  With amax = (1 + f) 2^E (f the 23-bit fraction) and
+// 448 = 1.75 * 2^8, e = E - 8 when 1 + f <= 1.75 and E - 7 otherwise; a
+// subnormal amax is first scaled by 2^64 (exactly).  x / s is then exact and
+// r = 2^-e is its exact reciprocal, so encode8's quotient steps return x * r;
+// where 2^-e is not a normal float (e < -126) the codes use IEEE division.
+// amax == 0 gives s = 0 (the caller encodes +-0 codes).
+__device__ __forceinline__ GroupScale group_scale_pow2(float amax) {
+    GroupScale g;
+    if (!(amax > 0.0f)) {
+        g.s = 0.0f;
+        g.r = 0.0f;
+        g.exact_div = true;
+        return g;
+    }
+    uint32_t u = __float_as_uint(amax);
+    int adj = 0;
+    if ((u >> 23) == 0) {  // subnormal amax
+        u = __float_as_uint(amax * 18446744073709551616.0f);  // x 2^64, exact
+        adj = -64;
+    }
+    const int ex = static_cast<int>(u >> 23) - 127;
+    // (a bf16 amax is at least 2^-133, so e >= -141; the clamp only keeps
+    // the shift below defined for any fp32 input)
+    const int e = max(ex - 8 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0) + adj, -149);
+    g.s = e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+    g.exact_div = e < -126 || e > 126;
+    g.r = g.exact_div ? 0.0f : __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    return g;
+}
+
 // Largest |x| over 8 bf16 values held as bit patterns: for non-negative
 // IEEE patterns integer order equals value order, so the maximum of
 // (bits & 0x7fff) per 16-bit half is the amax's bit pattern.

@@ -56,10 +56,11 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
+// pow2: power-of-two (UE8M0-style) scales rounded up instead of amax / 448.
 cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq,
-                             float* sx, int64_t lds, const DeviceInfo& dev, cudaStream_t stream);
+                             float* sx, int64_t lds, const DeviceInfo& dev, cudaStream_t stream, bool pow2 = false);
 cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
-                                const DeviceInfo& dev, cudaStream_t stream);
+                                const DeviceInfo& dev, cudaStream_t stream, bool pow2 = false);
 cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
                                   const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_e4m3_encode(const float* v, int64_t n, uint8_t* q, const DeviceInfo& dev,

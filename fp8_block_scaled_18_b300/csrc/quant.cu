@@ -34,6 +34,7 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 constexpr int kAqTeam = 4;
 constexpr int kAqGroupsPerWarp = 32 / kAqTeam;
 
+template <bool POW2>
 __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, int64_t KB,
                                                        int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
                                                        float* __restrict__ sx, int64_t lds,
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
         amax2 = __vmaxu2(amax2, __shfl_xor_sync(0xffffffffu, amax2, 2));
         if (valid) {
             const float amax = bits_to_amax(amax2);
-            const GroupScale gs = group_scale(amax);
+            const GroupScale gs = POW2 ? group_scale_pow2(amax) : group_scale(amax);
             const bool zero = (amax == 0.0f);
             uint8_t* q = xq + m * ldq + kb * 128;
 #pragma unroll
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
 // One CTA per 128x128 block.  Thread t reads the 16-byte chunk (t % 16) of
 // rows (t / 16) + kWqRowStep j (each warp load covers two full
 // 256-byte row segments), block amax via warp shuffles and shared memory.
-template <int kWqThreads>
+template <int kWqThreads, bool POW2>
 __global__ void __launch_bounds__(kWqThreads) weight_quant_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                           uint8_t* __restrict__ wq, float* __restrict__ sw) {
     constexpr int kWqRowStep = kWqThreads / 16;  // rows between a thread's loads
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kWqThreads) weight_quant_kernel(const uint16_t
     float amax = warp_max[0];
 #pragma unroll
     for (int i = 1; i < kWqThreads / 32; ++i) amax = fmaxf(amax, warp_max[i]);
-    const GroupScale gs = group_scale(amax);
+    const GroupScale gs = POW2 ? group_scale_pow2(amax) : group_scale(amax);
     const bool zero = (amax == 0.0f);
 #pragma unroll
     for (int j = 0; j < kWqRowsPerThread; ++j) {
@@ -279,22 +280,29 @@ __global__ void __launch_bounds__(256) act_quant_cols_kernel(const uint16_t* __r
 }  // namespace
 
 cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq,
-                             float* sx, int64_t lds, const DeviceInfo& dev, cudaStream_t stream) {
+                             float* sx, int64_t lds, const DeviceInfo& dev, cudaStream_t stream, bool pow2) {
     const int64_t KB = K / 128;
     const int64_t groups = M * KB;
     const int64_t warps_needed = (groups + kAqGroupsPerWarp - 1) / kAqGroupsPerWarp;
     const int64_t blocks_needed = (warps_needed + 7) / 8;
     const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 8;  // 8 x 256 threads per SM
     const int blocks = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
-    return launch_pdl(act_quant_kernel, dim3(blocks), dim3(256), 0, stream, x, KB, ldx, xq, ldq, sx, lds, groups);
+    if (pow2)
+        return launch_pdl(act_quant_kernel<true>, dim3(blocks), dim3(256), 0, stream, x, KB, ldx, xq, ldq, sx, lds,
+                          groups);
+    return launch_pdl(act_quant_kernel<false>, dim3(blocks), dim3(256), 0, stream, x, KB, ldx, xq, ldq, sx, lds,
+                      groups);
 }
 
 cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t* wq, float* sw,
-                                const DeviceInfo& dev, cudaStream_t stream) {
+                                const DeviceInfo& dev, cudaStream_t stream, bool pow2) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
-    if (static_cast<int64_t>(grid.x) * grid.y < 2 * static_cast<int64_t>(dev.num_sms))
-        return launch_pdl(weight_quant_kernel<512>, grid, dim3(512), 0, stream, w, N, K, wq, sw);
-    return launch_pdl(weight_quant_kernel<256>, grid, dim3(256), 0, stream, w, N, K, wq, sw);
+    const bool small = static_cast<int64_t>(grid.x) * grid.y < 2 * static_cast<int64_t>(dev.num_sms);
+    if (pow2)
+        return small ? launch_pdl(weight_quant_kernel<512, true>, grid, dim3(512), 0, stream, w, N, K, wq, sw)
+                     : launch_pdl(weight_quant_kernel<256, true>, grid, dim3(256), 0, stream, w, N, K, wq, sw);
+    return small ? launch_pdl(weight_quant_kernel<512, false>, grid, dim3(512), 0, stream, w, N, K, wq, sw)
+                 : launch_pdl(weight_quant_kernel<256, false>, grid, dim3(256), 0, stream, w, N, K, wq, sw);
 }
 
 cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,

@@ -30,6 +30,8 @@ _ST = ctypes.c_int
 _SIGS = {
     "fp8bs_act_quant": (_ST, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
     "fp8bs_weight_quant": (_ST, [_P, _I64, _I64, _P, _P, _P]),
+    "fp8bs_act_quant_pow2": (_ST, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
+    "fp8bs_weight_quant_pow2": (_ST, [_P, _I64, _I64, _P, _P, _P]),
     "fp8bs_weight_dequant": (_ST, [_P, _P, _I64, _I64, _P, _P]),
     "fp8bs_gemm": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P]),
     "fp8bs_gemm_fused": (_ST, [_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
@@ -146,6 +148,36 @@ def fp8bs_weight_quant(w: torch.Tensor, wq: Optional[torch.Tensor] = None, sw: O
         sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device)
     _check(lib.fp8bs_weight_quant(_bf16_ptr(w, "w"), N, K, _dev(wq, torch.uint8, "wq"),
                                   _dev(sw, torch.float32, "sw"), _stream(stream)), "fp8bs_weight_quant")
+    return wq, sw
+
+
+def fp8bs_act_quant_pow2(x: torch.Tensor, xq: Optional[torch.Tensor] = None, sx: Optional[torch.Tensor] = None,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """x [M, K] bf16 -> (xq [M, K] uint8 e4m3, sx [M, lds] fp32)."""
+    M, K = x.shape
+    ldx = _rows_stride(x, "x")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((M, max(4, ((K // 128) + 3) // 4 * 4)), dtype=torch.float32, device=x.device)
+    _check(lib.fp8bs_act_quant_pow2(_bf16_ptr(x, "x"), M, K, ldx, _dev(xq, torch.uint8, "xq"),
+                               _rows_stride(xq, "xq"), _dev(sx, torch.float32, "sx"),
+                               _rows_stride(sx, "sx"), _stream(stream)), "fp8bs_act_quant_pow2")
+    return xq, sx
+
+
+def fp8bs_weight_quant_pow2(w: torch.Tensor, wq: Optional[torch.Tensor] = None, sw: Optional[torch.Tensor] = None,
+                       stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """w [N, K] bf16 (dense) -> (wq [N, K] uint8, sw [ceil(N/128), K/128] fp32)."""
+    N, K = w.shape
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if sw is None:
+        sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device)
+    _check(lib.fp8bs_weight_quant_pow2(_bf16_ptr(w, "w"), N, K, _dev(wq, torch.uint8, "wq"),
+                                  _dev(sw, torch.float32, "sw"), _stream(stream)), "fp8bs_weight_quant_pow2")
     return wq, sw
 
 

@@ -83,6 +83,22 @@ fp8bs_status fp8bs_act_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ld
 fp8bs_status fp8bs_weight_quant(const uint16_t* w, int64_t N, int64_t K,
                                 uint8_t* wq, float* sw, fp8bs_stream_t stream);
 
+/* act_quant / weight_quant with power-of-two scales: the pages' act_quant
+ * takes a scale format (scale_fmt, the linear() excerpt of the "DeepSeek-V3"
+ * repository overview) that they do not define.  These calls read it as a
+ * UE8M0-style scale -- an unsigned power of two, no mantissa -- rounded up so
+ * that nothing saturates: s = 2^e with e the smallest integer such that
+ * amax <= 448 * 2^e, codes e4m3(x / s) (x / s is exact; only the encode
+ * rounds); an all-zero group or block has s = 0 and +-0 codes.  Arguments,
+ * layouts and errors exactly as fp8bs_act_quant / fp8bs_weight_quant; the
+ * scales are written as fp32 (exact powers of two), so the outputs feed
+ * fp8bs_gemm and fp8bs_weight_dequant unchanged. */
+fp8bs_status fp8bs_act_quant_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                  uint8_t* xq, int64_t ldq, float* sx, int64_t lds,
+                                  fp8bs_stream_t stream);
+fp8bs_status fp8bs_weight_quant_pow2(const uint16_t* w, int64_t N, int64_t K,
+                                     uint8_t* wq, float* sw, fp8bs_stream_t stream);
+
 /* weight_dequant (the bf16 branch of linear(); also the FP8->BF16 checkpoint
  * cast): w[n,k] = bf16_rne(fp32(dec(wq[n,k])) * sw[n/128, k/128]).
  *   wq [N, K] e4m3 dense, sw [ceil(N/128), K/128] fp32 dense, w [N, K] bf16 dense;
