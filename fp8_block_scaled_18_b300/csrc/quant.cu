@@ -132,42 +132,74 @@ __global__ void __launch_bounds__(kWqThreads) weight_quant_kernel(const uint16_t
 
 // ---------------------------------------------------------------- weight_dequant
 //
-// One CTA per 128x128 block: thread t decodes the 16-byte chunk (t % 8) of
-// rows (t / 8) + kDqRowStep j: w = bf16_rne(fp32(dec(q)) * s).
-template <int kDqThreads>
-__global__ void __launch_bounds__(kDqThreads) weight_dequant_kernel(const uint8_t* __restrict__ wq,
-                                                            const float* __restrict__ sw, int64_t N,
-                                                            int64_t K, uint16_t* __restrict__ w) {
-    constexpr int kDqRowStep = kDqThreads / 8;
+// w = bf16_rne(fp32(dec(q)) * s) per 128x128 block.  Work items are 16 rows x
+// 128 columns of one block (2 KB of codes): thread t of a 128-thread group
+// takes row (t / 8) and the 16-byte chunk (t % 8), so a warp reads four whole
+// 128-byte rows and writes 256 contiguous bytes per row.  Each 128-thread
+// group strides over the items kDqBatch at a time, the next batch's codes
+// and scales loading while the current batch converts and stores
+// (2 x kDqBatch loads in flight per thread).
+constexpr int kDqItemRows = 16;
+constexpr int kDqBatch = 2;
+
+__global__ void __launch_bounds__(256) weight_dequant_kernel(const uint8_t* __restrict__ wq,
+                                                            const float* __restrict__ sw, int64_t N, int64_t K,
+                                                            uint16_t* __restrict__ w) {
     grid_dependency_wait();  // wq / sw may come from the kernel just before
     allow_dependents();
-    constexpr int kDqRowsPerThread = 128 / kDqRowStep;
-    const int kb = blockIdx.x, nb = blockIdx.y;
     const int64_t KB = K / 128;
-    const int t = threadIdx.x;
-    const int chunk = t & 7;
-    const int r0 = t >> 3;
-    const float s = sw[static_cast<int64_t>(nb) * KB + kb];
+    const int64_t NB = (N + 127) / 128;
+    const int64_t items = NB * KB * (128 / kDqItemRows);
+    const int t = threadIdx.x & 127;
+    const int row = t >> 3, chunk = t & 7;
+    const int64_t groups = 2 * static_cast<int64_t>(gridDim.x);  // two 128-thread groups per CTA
+    const int64_t g0 = 2 * static_cast<int64_t>(blockIdx.x) + (threadIdx.x >> 7);
+    struct Item {
+        int64_t off;  // element offset of the chunk, or -1 when there is none
+        uint4 q;
+        float s;
+    };
+    auto fetch = [&](int64_t it, Item& x) {
+        x.off = -1;
+        if (it >= items) return;
+        const int64_t blk = it / (128 / kDqItemRows);
+        const int64_t part = it - blk * (128 / kDqItemRows);
+        const int64_t nb = blk / KB, kb = blk - nb * KB;
+        const int64_t n = nb * 128 + part * kDqItemRows + row;
+        if (n >= N) return;
+        x.off = n * K + kb * 128 + chunk * 16;
+        x.s = __ldg(sw + nb * KB + kb);
+        x.q = ld_stream(wq + x.off);
+    };
+    Item cur[kDqBatch], nxt[kDqBatch];
+    // batch b of this group holds items g0 + (b * kDqBatch + i) * groups
 #pragma unroll
-    for (int j = 0; j < kDqRowsPerThread; ++j) {
-        const int64_t n = static_cast<int64_t>(nb) * 128 + r0 + kDqRowStep * j;
-        if (n >= N) continue;
-        const int64_t off = n * K + static_cast<int64_t>(kb) * 128 + chunk * 16;
-        const uint4 q = ld_stream(wq + off);
-        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-        uint32_t out[8];
+    for (int i = 0; i < kDqBatch; ++i) fetch(g0 + i * groups, cur[i]);
+    for (int64_t base = g0; base < items; base += kDqBatch * groups) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f01 = cvt_e4m3x2_to_f32(static_cast<uint16_t>(words[i] & 0xFFFFu));
-            const float2 f23 = cvt_e4m3x2_to_f32(static_cast<uint16_t>(words[i] >> 16));
-            const __nv_bfloat162 b01 = __floats2bfloat162_rn(__fmul_rn(f01.x, s), __fmul_rn(f01.y, s));
-            const __nv_bfloat162 b23 = __floats2bfloat162_rn(__fmul_rn(f23.x, s), __fmul_rn(f23.y, s));
-            out[2 * i] = *reinterpret_cast<const uint32_t*>(&b01);
-            out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&b23);
+        for (int i = 0; i < kDqBatch; ++i) fetch(base + (kDqBatch + i) * groups, nxt[i]);
+#pragma unroll
+        for (int i = 0; i < kDqBatch; ++i) {
+            const Item& x = cur[i];
+            if (x.off < 0) continue;
+            const uint32_t words[4] = {x.q.x, x.q.y, x.q.z, x.q.w};
+            uint32_t out[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f01 = cvt_e4m3x2_to_f32(static_cast<uint16_t>(words[j] & 0xFFFFu));
+                const float2 f23 = cvt_e4m3x2_to_f32(static_cast<uint16_t>(words[j] >> 16));
+                const __nv_bfloat162 b01 = __floats2bfloat162_rn(__fmul_rn(f01.x, x.s), __fmul_rn(f01.y, x.s));
+                const __nv_bfloat162 b23 = __floats2bfloat162_rn(__fmul_rn(f23.x, x.s), __fmul_rn(f23.y, x.s));
+                out[2 * j] = *reinterpret_cast<const uint32_t*>(&b01);
+                out[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&b23);
+            }
+            // one 32-byte store: a warp writes four whole 256-byte row segments
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(w + x.off), "r"(out[0]),
+                         "r"(out[1]), "r"(out[2]), "r"(out[3]), "r"(out[4]), "r"(out[5]), "r"(out[6]), "r"(out[7])
+                         : "memory");
         }
-        uint4* dst = reinterpret_cast<uint4*>(w + off);
-        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+#pragma unroll
+        for (int i = 0; i < kDqBatch; ++i) cur[i] = nxt[i];
     }
 }
 
@@ -225,20 +257,32 @@ __global__ void __launch_bounds__(256) act_quant_cols_kernel(const uint16_t* __r
     const int g = t / kCqCols;   // row group of 32
     const int64_t MB = (M + kCqRows - 1) / kCqRows;
     const int64_t CB = K / kCqCols;
+    // the tile's 128 rows x 128 bytes: four 16-byte chunks per thread, eight
+    // threads per row; rows past M read as zeros (they never raise the amax)
+    auto load_tile = [&](int64_t tt, uint4 (&v)[4]) {
+        const int64_t mb = tt / CB;
+        const int64_t k0 = (tt - mb * CB) * kCqCols;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int q = t + 256 * i;
+            const int r = q / 8, ch = q % 8;
+            v[i] = make_uint4(0, 0, 0, 0);
+            if (tt < MB * CB && mb * kCqRows + r < M) v[i] = ld_stream(x + (mb * kCqRows + r) * ldx + k0 + ch * 8);
+        }
+    };
+    uint4 pre[4];
+    load_tile(blockIdx.x, pre);
     for (int64_t tt = blockIdx.x; tt < MB * CB; tt += gridDim.x) {
         const int64_t mb = tt / CB;
         const int64_t k0 = (tt - mb * CB) * kCqCols;
         const int64_t m0 = mb * kCqRows;
         __syncthreads();  // the previous tile's reads of `tile` and `pam` are done
-        // 128 rows x 128 bytes: four 16-byte chunks per thread, eight threads per row
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int q = t + 256 * i;
-            const int r = q / 8, ch = q % 8;
-            uint4 v = make_uint4(0, 0, 0, 0);  // rows past M are zeros (they never raise the amax)
-            if (m0 + r < M) v = ld_stream(x + (m0 + r) * ldx + k0 + ch * 8);
-            *reinterpret_cast<uint4*>(&tile[r][ch * 8]) = v;
+            *reinterpret_cast<uint4*>(&tile[q / 8][(q % 8) * 8]) = pre[i];
         }
+        load_tile(tt + gridDim.x, pre);  // the next tile's loads run during this tile's work
         __syncthreads();
         uint4 v[4];  // rows 32g + 8j .. +7 of column c, as 8 bf16 values each
 #pragma unroll
@@ -307,10 +351,11 @@ cudaError_t launch_weight_quant(const uint16_t* w, int64_t N, int64_t K, uint8_t
 
 cudaError_t launch_weight_dequant(const uint8_t* wq, const float* sw, int64_t N, int64_t K, uint16_t* w,
                                   const DeviceInfo& dev, cudaStream_t stream) {
-    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>((N + 127) / 128));
-    if (static_cast<int64_t>(grid.x) * grid.y < 2 * static_cast<int64_t>(dev.num_sms))
-        return launch_pdl(weight_dequant_kernel<512>, grid, dim3(512), 0, stream, wq, sw, N, K, w);
-    return launch_pdl(weight_dequant_kernel<256>, grid, dim3(256), 0, stream, wq, sw, N, K, w);
+    const int64_t items = ((N + 127) / 128) * (K / 128) * (128 / kDqItemRows);
+    const int64_t want = (items + 2 * kDqBatch - 1) / (2 * kDqBatch);  // CTAs that each get a batch per group
+    const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;       // 8 x 256 threads per SM
+    const int blocks = static_cast<int>(want < cap ? want : cap);
+    return launch_pdl(weight_dequant_kernel, dim3(blocks), dim3(256), 0, stream, wq, sw, N, K, w);
 }
 
 cudaError_t launch_e4m3_encode(const float* v, int64_t n, uint8_t* q, const DeviceInfo& dev,
