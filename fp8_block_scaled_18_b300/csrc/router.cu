@@ -25,57 +25,71 @@ namespace {
 
 // ------------------------------------------------------------------ gate
 //
-// One CTA per 128 tokens, 576 threads: warp 0 TMA producer (x tile 128 x 64
-// bf16 and the gate weight E x 64 bf16 per 128-byte K chunk, 128-byte
-// swizzle, kGateStages-deep ring), warp 1 MMA issuer (four
-// tcgen05.mma.kind::f16, M 128, N E, K 16, per chunk, all accumulating in one
-// TMEM region of E fp32 columns; owns the TMEM allocation), warps 2-17 the
-// epilogue: four warps per TMEM lane quarter, each taking a quarter of the
-// experts (columns) of its 32 tokens.  Once the sums are complete the
-// pipeline's shared memory is reused:
-//   1. each thread turns its columns' logits into affinities s = sigmoid(l)
-//      and stores them, expert-major, in shared memory;
-//   2. each thread forms the scores (largest s + bias) of the groups
-//      g = its quarter index mod 4 for its token;
-//   3. each thread picks its token's kept groups (all four threads of a token
-//      pick the same ones) and keeps a sorted top-k of its columns inside
-//      them by biased affinity, ties to the lower expert;
-//   4. one thread per token merges the four partial lists (in expert
-//      order, so ties still go to the lower expert), normalises the chosen
-//      affinities and writes ids and gate values.
-// The phases are separated by mbarriers with bounded waits.
+// A 128-token tile is taken by CS CTAs of 576 threads (a thread-block
+// cluster when CS > 1), each computing the logits of E / CS experts: warp 0
+// TMA producer (x tile 128 x 64 bf16 and E / CS gate-weight rows x 64 bf16
+// per 128-byte K chunk, 128-byte swizzle, a ring of GateLayout::ST stages),
+// warp 1 MMA issuer (four tcgen05.mma.kind::f16, M 128, N E / CS, K 16, per
+// chunk, accumulating in TMEM; owns the TMEM allocation), warps 2-17 the
+// epilogue (four warps per TMEM lane quarter):
+//   1. each warp turns 16-column units of its 32 tokens' logits into
+//      affinities s = sigmoid(l) and writes them, token-major, into the
+//      selection table of the CTA that selects for those tokens (the CTA
+//      itself when CS == 1; cluster rank q takes tokens 32q .. 32q + 31 of
+//      the tile, so a lane quarter's rows go to one CTA of the cluster);
+//   2. one warp per token, lane l holding experts l, l + 32, ...: group
+//      scores (largest s + bias of each group) by warp max-reductions, the
+//      topk_groups best groups (lower index on ties), then top_k rounds of
+//      a warp arg-max over the kept experts' biased affinities (lower expert
+//      on ties), and the gate values from the chosen s.
+// Values are compared through an order-preserving map of their fp32 bits
+// to unsigned integers, so the hardware warp reductions give exact fp32
+// comparisons.  The two steps meet at an mbarrier with a bounded wait.
 constexpr int kGateM = 128;
 constexpr int kGateK = 64;            // bf16 elements per 128-byte chunk
-constexpr int kGateStages = 4;
 constexpr int kGateMaxE = 256;
 constexpr int kGateMaxGroups = 32;
 constexpr int kGateMaxTopK = 16;
 constexpr int kGateEpiWarp0 = 2;
 constexpr int kGateEpiWarps = 16;
 constexpr int kGateThreads = 32 * (kGateEpiWarp0 + kGateEpiWarps);
+constexpr int kGateSelStride = 260;  // floats per token row of the selection table
+static_assert(kGateMaxGroups <= 32 && kGateMaxTopK <= 32, "one lane per group and per chosen expert");
+static_assert(kGateMaxE <= 8 * 32, "eight experts per lane");
 
+// Shared memory of one CTA.  When CS == 1 the selection table lies over the
+// pipeline stages (written once this CTA's sums are complete); in a cluster
+// the peers write into it while this CTA may still be in its K loop, so it
+// has its own space, and the smaller stages (E / CS weight rows) still leave
+// room for a deeper ring.
+template <int CS>
 struct GateLayout {
+    static constexpr int ST = CS == 1 ? 4 : 7;  // pipeline stages
     static constexpr int A_BYTES = kGateM * 128;
-    static constexpr int B_BYTES = kGateMaxE * 128;
+    static constexpr int B_BYTES = (kGateMaxE / CS) * 128;
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = kGateStages * A_BYTES;
-    // full[S], empty[S], done, then the epilogue's three phase barriers
-    static constexpr int OFF_BAR = OFF_B + kGateStages * B_BYTES;
-    static constexpr int NUM_BARS = 2 * kGateStages + 1 + 3;
+    static constexpr int OFF_B = ST * A_BYTES;
+    static constexpr int STAGES_END = OFF_B + ST * B_BYTES;
+    // selection table: affinities [NT tokens][kGateSelStride] fp32 (the
+    // stride keeps both the per-token-row writes and the per-expert reads
+    // free of bank conflicts and rows 16-byte aligned), then per-warp group
+    // keys [16][32] u32
+    static constexpr int NT = kGateM / CS;
+    static constexpr int OFF_SEL = CS == 1 ? 0 : STAGES_END;
+    static constexpr int OFF_GK = OFF_SEL + NT * kGateSelStride * 4;
+    static constexpr int SEL_END = OFF_GK + kGateEpiWarps * kGateMaxGroups * 4;
+    static_assert(CS > 1 || SEL_END <= STAGES_END, "the selection table fits in the pipeline stages");
+    // full[ST], empty[ST], done, the epilogue's step barrier, recv (the
+    // selection table is complete)
+    static constexpr int OFF_BAR = CS == 1 ? STAGES_END : SEL_END;
+    static constexpr int NUM_BARS = 2 * ST + 3;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_BIAS = (OFF_ABORT + 4 + 15) & ~15;
     static constexpr int BYTES = OFF_BIAS + kGateMaxE * 4;
     static constexpr int ALLOC = BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 256;
-    // epilogue tables, over the pipeline stages once the sums are complete:
-    // affinities [E][128 tokens] fp32, group scores [32][128] fp32, partial
-    // top-k lists [4 quarters][16][128] expert ids (int16)
-    static constexpr int OFF_S = 0;
-    static constexpr int OFF_G = OFF_S + kGateMaxE * kGateM * 4;
-    static constexpr int OFF_P = OFF_G + kGateMaxGroups * kGateM * 4;
-    static constexpr int EPI_END = OFF_P + 4 * kGateMaxTopK * kGateM * 2;
-    static_assert(EPI_END <= OFF_BAR, "the epilogue tables fit in the pipeline stages");
+    static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
 };
 
 struct GateParams {
@@ -114,31 +128,80 @@ __device__ __forceinline__ bool drain_wait_g(uint32_t bar, uint32_t parity, cons
     return ok;
 }
 
-__device__ __forceinline__ float sigmoid_f32(float v) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-v))); }
-
-// Sorted insertion of (v, e) into a descending list of n <= kGateMaxTopK
-// entries (static indices, so the list stays in registers): an entry moves
-// down only past strictly smaller values, so equal values keep the order in
-// which they arrived.
-__device__ __forceinline__ void topk_insert(float (&lb)[kGateMaxTopK], int (&le)[kGateMaxTopK], int n, float v,
-                                            int e) {
-#pragma unroll
-    for (int i = 0; i < kGateMaxTopK; ++i) {
-        if (i < n && v > lb[i]) {
-            const float tb = lb[i];
-            const int te = le[i];
-            lb[i] = v;
-            le[i] = e;
-            v = tb;
-            e = te;
+// ---- thread-block cluster helpers (distributed shared memory, remote mbarriers)
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of `addr` (a shared::cta address of this CTA)
+// in the CTA of the cluster with the given rank.
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+    return d;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+// All threads of every CTA of the cluster: after barrier initialisation
+// (before any CTA touches another's shared memory) and before exit (no CTA
+// leaves while a peer may still write into it).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded_wait for a barrier that other CTAs of the cluster arrive on
+// (acquire at cluster scope, so their shared-memory writes are visible).
+__device__ __forceinline__ bool bounded_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 31u) == 0) {
+            if (*ctl.abort) return false;
+            if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+                *ctl.abort = 1;
+                atomicOr(ctl.err, DEVERR_WAIT_TIMEOUT);
+                return false;
+            }
         }
     }
 }
 
+__device__ __forceinline__ float sigmoid_f32(float v) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-v))); }
+
+// Order-preserving map of fp32 bit patterns to unsigned integers: for
+// non-NaN a, b, a > b exactly when key(a) > key(b) (with +0 above -0).
+// Selection keys are at least 1, so 0 marks an expert that is not (or no
+// longer) a candidate.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return max((u & 0x80000000u) ? ~u : (u | 0x80000000u), 1u);
+}
+
+// CS: CTAs per 128-token tile (a thread-block cluster when CS > 1).  Each
+// takes E / CS experts through the K loop and selects for 128 / CS tokens.
+template <int CS>
 __global__ void __launch_bounds__(kGateThreads, 1)
     moe_gate_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ GateParams p) {
-    using L = GateLayout;
+    using L = GateLayout<CS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
@@ -147,9 +210,13 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t bar0 = sbase + L::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kGateStages + s); };
-    const uint32_t done_bar = bar0 + 8u * (2 * kGateStages);
-    auto phase_bar = [&](int i) { return bar0 + 8u * (2 * kGateStages + 1 + i); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (L::ST + s); };
+    const uint32_t done_bar = bar0 + 8u * (2 * L::ST);
+    const uint32_t step_bar = bar0 + 8u * (2 * L::ST + 1);
+    const uint32_t recv_bar = bar0 + 8u * (2 * L::ST + 2);
+    const uint32_t crank = CS > 1 ? cluster_rank() : 0u;
+    const int EN = p.E / CS;                 // this CTA's experts: e0 .. e0 + EN - 1
+    const int e0 = static_cast<int>(crank) * EN;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
     float* bias_s = reinterpret_cast<float*>(smem + L::OFF_BIAS);
 
@@ -158,15 +225,17 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         tma_prefetch_desc(&tmW);
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kGateStages; ++s) {
+        for (int s = 0; s < L::ST; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
         mbar_init(done_bar, 1);
-        for (int i = 0; i < 3; ++i) mbar_init(phase_bar(i), kGateEpiWarps);
+        mbar_init(step_bar, kGateEpiWarps);
+        mbar_init(recv_bar, CS * 4);  // the four warps of one lane quarter in every CTA
         *abort_flag = 0;
         fence_barrier_init();
     }
+    if constexpr (CS > 1) cluster_sync_all();  // every CTA's barriers exist before any remote access
     grid_dependency_wait();
     allow_dependents();
     if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
@@ -176,33 +245,33 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_TMEM);
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
-    const int m0 = blockIdx.x * kGateM;
+    const int m0 = (blockIdx.x / CS) * kGateM;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + p.E * 128);
+        const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + EN * 128);
         int kb = 0;
         for (; kb < p.KB; ++kb) {
-            const int s = kb % kGateStages;
-            const uint32_t ph = (kb / kGateStages) & 1u;
+            const int s = kb % L::ST;
+            const uint32_t ph = (kb / L::ST) & 1u;
             if (!warp_wait(empty_bar(s), ph ^ 1u, ctl)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(full_bar(s), tx);
                 tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmX, full_bar(s), kb * kGateK, m0);
-                tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmW, full_bar(s), kb * kGateK, 0);
+                tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmW, full_bar(s), kb * kGateK, e0);
             }
             __syncwarp();
         }
         // every issued load must land before the CTA's shared memory goes away
-        const int first = kb > kGateStages ? kb - kGateStages : 0;
-        for (int j = first; j < kb; ++j) drain_wait_g(full_bar(j % kGateStages), (j / kGateStages) & 1u, ctl);
+        const int first = kb > L::ST ? kb - L::ST : 0;
+        for (int j = first; j < kb; ++j) drain_wait_g(full_bar(j % L::ST), (j / L::ST) & 1u, ctl);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        const uint32_t idesc = idesc_bf16_f32(kGateM, p.E);
+        const uint32_t idesc = idesc_bf16_f32(kGateM, EN);
         bool issued = false;
         for (int kb = 0; kb < p.KB; ++kb) {
-            const int s = kb % kGateStages;
-            if (!warp_wait(full_bar(s), (kb / kGateStages) & 1u, ctl)) break;
+            const int s = kb % L::ST;
+            if (!warp_wait(full_bar(s), (kb / L::ST) & 1u, ctl)) break;
             tc_fence_after();
             if (lane == 0) {
                 const uint64_t adesc = sdesc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
@@ -222,114 +291,132 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         if (issued) drain_wait_g(done_bar, 0, ctl);
     } else {
         // ------------------------------------------------------------ epilogue
-        const int quarter = warp & 3;              // TMEM lane quarter this warp may read
-        const int tok = quarter * 32 + lane;       // the token (TMEM lane) of this thread
-        const int sl = (warp - kGateEpiWarp0) >> 2;  // which quarter of the experts
-        const int m = m0 + tok;
+        const int ew = warp - kGateEpiWarp0;
+        const int quarter = warp & 3;         // TMEM lane quarter this warp may read
+        const int sl = ew >> 2;               // which of the four warps of the quarter
         const uint32_t taddr0 = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        // this thread's columns: 16-column units [u0, u1) of the E / 16
-        const int units = p.E / 16;
-        const int u0 = sl * units / 4, u1 = (sl + 1) * units / 4;
-        const int per = p.E / p.n_groups;
-        float* S = reinterpret_cast<float*>(smem + L::OFF_S);      // [e][tok]
-        float* Gs = reinterpret_cast<float*>(smem + L::OFF_G);     // [g][tok]
-        int16_t* P = reinterpret_cast<int16_t*>(smem + L::OFF_P);  // [sl][k][tok]
-        auto phase = [&](int i) {  // all epilogue warps reach phase i
-            __syncwarp();
-            if (lane == 0) mbar_arrive(phase_bar(i));
-            return warp_wait(phase_bar(i), 0, ctl);
-        };
+        float* S = reinterpret_cast<float*>(smem + L::OFF_SEL);  // [NT][kGateSelStride]
         bool ok = warp_wait(done_bar, 0, ctl);
         tc_fence_after();
-        // the stages were last written by TMA (async proxy); the tables below
-        // overwrite them with ordinary stores
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        // 1. affinities of this thread's columns
+        if constexpr (CS == 1) {
+            // the stages were last written by TMA (async proxy); the table
+            // overwrites them with ordinary stores
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        // 1. affinities, token-major, into the selecting CTA's table: this
+        //    warp's 16-column units sl, sl + 4, ... of the EN columns
         if (ok) {
-            for (int u = u0; u < u1; ++u) {
+            const int row = CS == 1 ? quarter * 32 + lane : lane;
+            const uint32_t dst = CS == 1 ? sbase + L::OFF_SEL : mapa_rank(sbase + L::OFF_SEL, quarter);
+            for (int u = sl; u < EN / 16; u += 4) {
                 uint64_t pr[8];
                 tmem_ld_x16_pairs(taddr0 + 16 * u, pr);
+                float sv[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float l = (i & 1) ? hi_f32(pr[i >> 1]) : lo_f32(pr[i >> 1]);
-                    S[(16 * u + i) * kGateM + tok] = sigmoid_f32(l);
+                for (int i = 0; i < 16; ++i) sv[i] = sigmoid_f32((i & 1) ? hi_f32(pr[i >> 1]) : lo_f32(pr[i >> 1]));
+                const uint32_t at = dst + static_cast<uint32_t>((row * kGateSelStride + e0 + 16 * u) * 4);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if constexpr (CS == 1)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(at + 16u * c),
+                                     "f"(sv[4 * c]), "f"(sv[4 * c + 1]), "f"(sv[4 * c + 2]), "f"(sv[4 * c + 3])
+                                     : "memory");
+                    else
+                        st_cluster_v4(at + 16u * c, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
                 }
             }
         }
-        ok = phase(0) && ok;
-        // 2. group scores: the largest biased affinity of each group g = sl (mod 4)
-        if (ok) {
-            for (int g = sl; g < p.n_groups; g += 4) {
-                float gm = -INFINITY;
-                for (int e = g * per; e < (g + 1) * per; ++e) gm = fmaxf(gm, __fadd_rn(S[e * kGateM + tok], bias_s[e]));
-                Gs[g * kGateM + tok] = gm;
-            }
+        __syncwarp();
+        if constexpr (CS == 1) {
+            if (lane == 0) mbar_arrive(step_bar);
+            ok = warp_wait(step_bar, 0, ctl) && ok;
+        } else {
+            if (lane == 0) mbar_arrive_cluster(mapa_rank(recv_bar, quarter));
+            ok = __all_sync(0xffffffffu, bounded_wait_cluster(recv_bar, 0, ctl)) && ok;
         }
-        ok = phase(1) && ok;
-        // 3. the kept groups (the topk_groups best, lower index on ties), then
-        //    a sorted top-k of this thread's columns inside them
+        // 2. selection, one warp per token; lane l holds experts l + 32 j
         if (ok) {
-            uint32_t keep = 0;
-            for (int r = 0; r < p.topk_groups; ++r) {
-                int best = -1;
-                float bv = 0.0f;
-                for (int g = 0; g < p.n_groups; ++g) {
-                    const float v = Gs[g * kGateM + tok];
-                    if (!((keep >> g) & 1u) && (best < 0 || v > bv)) {
-                        best = g;
-                        bv = v;
+            const int J = (p.E + 31) / 32;
+            const int per = p.E / p.n_groups;
+            uint32_t* gk = reinterpret_cast<uint32_t*>(smem + L::OFF_GK) + 32 * ew;
+            float bias_r[8];
+            int grp[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = 32 * j + lane;
+                bias_r[j] = e < p.E ? bias_s[e] : 0.0f;
+                grp[j] = e < p.E ? e / per : -1;
+            }
+            const int tok0 = m0 + static_cast<int>(crank) * L::NT;
+            for (int t = ew; t < L::NT && tok0 + t < p.T; t += kGateEpiWarps) {
+                const float* St = S + t * kGateSelStride;
+                uint32_t ck[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ck[j] = (j < J && grp[j] >= 0) ? order_key(__fadd_rn(St[32 * j + lane], bias_r[j])) : 0u;
+                // group scores: one per lane g < n_groups
+                uint32_t mine = 0;
+                if (per == 32) {  // group j is slot j
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (j < J) {
+                            const uint32_t g = __reduce_max_sync(0xffffffffu, ck[j]);
+                            if (lane == j) mine = g;
+                        }
+                    }
+                } else {
+                    for (int g = 0; g < p.n_groups; ++g) {
+                        uint32_t m = 0;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (grp[j] == g) m = max(m, ck[j]);
+                        m = __reduce_max_sync(0xffffffffu, m);
+                        if (lane == g) mine = m;
                     }
                 }
-                keep |= 1u << best;
-            }
-            float lb[kGateMaxTopK];
-            int le[kGateMaxTopK];
-#pragma unroll
-            for (int i = 0; i < kGateMaxTopK; ++i) {
-                lb[i] = -INFINITY;
-                le[i] = -1;
-            }
-            for (int e = 16 * u0; e < 16 * u1; ++e) {
-                if (!((keep >> (e / per)) & 1u)) continue;
-                topk_insert(lb, le, p.top_k, __fadd_rn(S[e * kGateM + tok], bias_s[e]), e);
-            }
-#pragma unroll
-            for (int i = 0; i < kGateMaxTopK; ++i)
-                if (i < p.top_k) P[(sl * kGateMaxTopK + i) * kGateM + tok] = static_cast<int16_t>(le[i]);
-        }
-        ok = phase(2) && ok;
-        // 4. merge the four lists (in expert order), gate values, outputs
-        if (ok && sl == 0 && m < p.T) {
-            float lb[kGateMaxTopK];
-            int le[kGateMaxTopK];
-#pragma unroll
-            for (int i = 0; i < kGateMaxTopK; ++i) {
-                lb[i] = -INFINITY;
-                le[i] = -1;
-            }
-            for (int q = 0; q < 4; ++q) {
-                for (int i = 0; i < p.top_k; ++i) {
-                    const int e = P[(q * kGateMaxTopK + i) * kGateM + tok];
-                    if (e < 0) break;  // a shorter list (fewer kept columns than top_k)
-                    topk_insert(lb, le, p.top_k, __fadd_rn(S[e * kGateM + tok], bias_s[e]), e);
+                gk[lane] = mine;
+                __syncwarp();
+                // group lane is kept when fewer than topk_groups groups beat it
+                int better = 0;
+                for (int h = 0; h < p.n_groups; ++h) {
+                    const uint32_t o = gk[h];
+                    better += (o > mine || (o == mine && h < lane)) ? 1 : 0;
                 }
-            }
-            float ls[kGateMaxTopK];
-            float ssum = 0.0f;
+                const uint32_t keep = __ballot_sync(0xffffffffu, lane < p.n_groups && better < p.topk_groups);
+                __syncwarp();
 #pragma unroll
-            for (int r = 0; r < kGateMaxTopK; ++r) {
-                if (r < p.top_k) {
-                    ls[r] = S[le[r] * kGateM + tok];
-                    ssum = __fadd_rn(ssum, ls[r]);
+                for (int j = 0; j < 8; ++j)
+                    if (grp[j] < 0 || !((keep >> grp[j]) & 1u)) ck[j] = 0u;
+                // top_k rounds of arg-max (largest key, then lowest expert)
+                int my_id = -1;
+                for (int r = 0; r < p.top_k; ++r) {
+                    uint32_t bk = 0;
+                    int bj = 0;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (ck[j] > bk) {
+                            bk = ck[j];
+                            bj = j;
+                        }
+                    }
+                    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+                    const uint32_t cand = (bk == mk && bk != 0u) ? static_cast<uint32_t>(32 * bj + lane) : 0xffffffffu;
+                    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+                    if (win == static_cast<uint32_t>(32 * bj + lane)) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (j == bj) ck[j] = 0u;
+                    }
+                    if (lane == r) my_id = static_cast<int>(win);
                 }
-            }
-            int32_t* idr = p.ids + static_cast<int64_t>(m) * p.top_k;
-            float* wr = p.w + static_cast<int64_t>(m) * p.top_k;
-#pragma unroll
-            for (int r = 0; r < kGateMaxTopK; ++r) {
-                if (r < p.top_k) {
-                    idr[r] = le[r];
-                    wr[r] = __fmul_rn(__fdiv_rn(ls[r], ssum), p.route_scale);
+                // gate values: the chosen affinities normalised in rank order
+                const float sr = (lane < p.top_k && my_id >= 0 && my_id < p.E) ? St[my_id] : 0.0f;
+                float ssum = 0.0f;
+                for (int r = 0; r < p.top_k; ++r) ssum = __fadd_rn(ssum, __shfl_sync(0xffffffffu, sr, r));
+                if (lane < p.top_k) {
+                    const int64_t o = static_cast<int64_t>(tok0 + t) * p.top_k + lane;
+                    p.ids[o] = my_id;
+                    p.w[o] = __fmul_rn(__fdiv_rn(sr, ssum), p.route_scale);
                 }
             }
         }
@@ -340,6 +427,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, L::TMEM_COLS);
     }
+    if constexpr (CS > 1) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ routing tables
@@ -486,15 +574,22 @@ __global__ void __launch_bounds__(kRouteThreads)
 cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, const float* bias, int64_t T,
                             int64_t dim, int E, int n_groups, int topk_groups, int top_k, float route_scale,
                             int32_t* ids, float* w, const DeviceInfo& dev, cudaStream_t stream) {
+    // Clusters of four CTAs per 128-token tile (a quarter of the experts
+    // each, a multiple of 16 columns) when E allows, else one CTA per tile.
+    const int cs = (E % 64 == 0) ? 4 : 1;
     CUtensorMap tmX, tmW;
     cudaError_t e;
     if ((e = make_tmap_2d(&tmX, x, 2, dim, T, ldx * 2, kGateK, kGateM, 128)) != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&tmW, wg, 2, dim, E, dim * 2, kGateK, E, 128)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&tmW, wg, 2, dim, E, dim * 2, kGateK, E / cs, 128)) != cudaSuccess) return e;
     {
         static bool ready[64];
         if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
         if (!ready[dev.device]) {
-            e = cudaFuncSetAttribute(moe_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GateLayout::ALLOC);
+            e = cudaFuncSetAttribute(moe_gate_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GateLayout<1>::ALLOC);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(moe_gate_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GateLayout<4>::ALLOC);
             if (e != cudaSuccess) return e;
             ready[dev.device] = true;
         }
@@ -512,8 +607,22 @@ cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, 
     p.route_scale = route_scale;
     p.err = dev.err;
     p.timeout_ns = wait_timeout_ns();
-    const int grid = static_cast<int>((T + kGateM - 1) / kGateM);
-    return launch_pdl(moe_gate_kernel, dim3(grid), dim3(kGateThreads), GateLayout::ALLOC, stream, tmX, tmW, p);
+    const int tiles = static_cast<int>((T + kGateM - 1) / kGateM);
+    if (cs == 1)
+        return launch_pdl(moe_gate_kernel<1>, dim3(tiles), dim3(kGateThreads), GateLayout<1>::ALLOC, stream, tmX, tmW, p);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 4;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(4 * tiles);
+    cfg.blockDim = dim3(kGateThreads);
+    cfg.dynamicSmemBytes = GateLayout<4>::ALLOC;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_gate_kernel<4>, tmX, tmW, p);
 }
 
 cudaError_t launch_moe_route(const int32_t* ids, const float* w, int64_t T, int top_k, int E, int32_t* offsets,

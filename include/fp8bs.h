@@ -333,7 +333,10 @@ fp8bs_status fp8bs_moe_combine(const uint16_t* yk, int64_t ldyk, int64_t R, cons
  * n_groups divides E, n_groups <= 32, 1 <= topk_groups <= n_groups,
  * 1 <= top_k <= 16 and top_k <= topk_groups * E / n_groups (else
  * FP8BS_ERR_INVALID_ARG).  Near-ties may resolve differently from an exact
- * (fp64) router: the logits carry fp32 rounding. */
+ * (fp64) router: the logits carry fp32 rounding.  A token whose biased
+ * affinities include NaN or -inf (non-finite x or bias) may get id -1 in a
+ * slot, with gate value computed as if that affinity were 0; fp8bs_moe_route
+ * then reports FP8BS_ERR_INDEX. */
 fp8bs_status fp8bs_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, const float* bias, int64_t T,
                             int64_t dim, int32_t E, int32_t n_groups, int32_t topk_groups, int32_t top_k,
                             float route_scale, int32_t* ids, float* weights, fp8bs_stream_t stream);

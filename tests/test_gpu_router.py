@@ -87,6 +87,8 @@ def _check_gate(ids_g, w_g, x, wg, bias, s_o, ids_o, n_groups, topk_groups, top_
     (300, 512, 256, 8, 4, 8, 0.075),     # DeepSeek-V3's routing shape at a reduced width, ragged tokens
     (130, 128, 64, 16, 3, 5, 0.15),      # groups of 4 experts: a 16-column slice spans several groups
     (5, 64, 16, 1, 1, 1, 0.2),           # one group, top-1, one K chunk
+    (200, 192, 96, 3, 2, 4, 0.15),       # one CTA per tile (E not a multiple of 64), groups of 32
+    (77, 128, 80, 5, 3, 7, 0.15),        # one CTA per tile, groups of 16
 ])
 def test_gate_vs_oracle(F, orc, T, dim, E, n_groups, topk_groups, top_k, std):
     rng = np.random.default_rng(T + E)
@@ -116,6 +118,35 @@ def test_gate_full_width(F, orc):
     assert F.fp8bs_sync_status() == 0
     ids_o, _, s_o = orc.moe_gate(x, gw, bias, want_scores=True)
     _check_gate(host(ids), host(w).astype(np.float64), x, gw, bias, s_o, ids_o, 8, 4, 8, min_decided=0.0)
+
+
+@pytest.mark.parametrize("E,n_groups", [(256, 8), (96, 3)])
+def test_gate_exact_ties_go_to_lower_index(F, orc, E, n_groups):
+    """Group 1 is an exact copy of group 0 (weight rows and bias), so those
+    experts' logits, and the two groups' scores, tie exactly; the selection
+    must then prefer the lower group and the lower expert: wherever expert
+    e + per is chosen, e is chosen too and ranks before it."""
+    rng = np.random.default_rng(E)
+    T, dim, per = 256, 256, E // n_groups
+    x = synth.normal_bf16(rng, (T, dim), 1.0)
+    wg = synth.normal_bf16(rng, (E, dim), 0.1)
+    wg[per:2 * per] = wg[:per]
+    bias = rng.uniform(-0.1, 0.1, size=E).astype(np.float32)
+    bias[per:2 * per] = bias[:per]
+    ids, w = F.fp8bs_moe_gate(dev_bf16(x), dev_bf16(wg), dev(bias), n_groups=n_groups, topk_groups=2, top_k=6)
+    assert F.fp8bs_sync_status() == 0
+    ids, w = host(ids), host(w)
+    ids_o, _ = orc.moe_gate(x, wg, bias, n_groups=n_groups, topk_groups=2, top_k=6)
+    twins = 0
+    for t in range(T):
+        pos = {int(e): i for i, e in enumerate(ids[t])}
+        for e, i in pos.items():
+            if per <= e < 2 * per:
+                twins += 1
+                assert e - per in pos and pos[e - per] < i, f"token {t}: {ids[t]}"
+                assert w[t, i] == w[t, pos[e - per]]
+    assert twins > 0.2 * T
+    assert (ids == ids_o).all(axis=1).mean() >= 0.95
 
 
 def test_gate_without_bias_and_strided_x(F, orc):
