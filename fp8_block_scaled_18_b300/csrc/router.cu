@@ -17,6 +17,7 @@
 
 #include <algorithm>
 
+#include "codec.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -25,13 +26,17 @@ namespace {
 
 // ------------------------------------------------------------------ gate
 //
-// A 128-token tile is taken by CS CTAs of 576 threads (a thread-block
+// A 128-token tile is taken by CS CTAs of 608 threads (a thread-block
 // cluster when CS > 1), each computing the logits of E / CS experts: warp 0
 // TMA producer (x tile 128 x 64 bf16 and E / CS gate-weight rows x 64 bf16
 // per 128-byte K chunk, 128-byte swizzle, a ring of GateLayout::ST stages),
-// warp 1 MMA issuer (four tcgen05.mma.kind::f16, M 128, N E / CS, K 16, per
-// chunk, accumulating in TMEM; owns the TMEM allocation), warps 2-17 the
-// epilogue (four warps per TMEM lane quarter):
+// warps 1 and 2 MMA issuers (four tcgen05.mma.kind::f16, M 128, N E / CS,
+// K 16, per chunk; warp 1 the even chunks, warp 2 the odd ones, each into its
+// own TMEM accumulator; warp 1 owns the TMEM allocation), warps 3-18 the
+// epilogue (four warps per TMEM lane quarter), which adds the two sums.  In a cluster each CTA loads
+// 128 / CS rows of the x tile and multicasts them to all CTAs (each stage
+// is then released by the MMAs of every CTA), so the tile leaves L2 once.
+// Epilogue:
 //   1. each warp turns 16-column units of its 32 tokens' logits into
 //      affinities s = sigmoid(l) and writes them, token-major, into the
 //      selection table of the CTA that selects for those tokens (the CTA
@@ -50,7 +55,7 @@ constexpr int kGateK = 64;            // bf16 elements per 128-byte chunk
 constexpr int kGateMaxE = 256;
 constexpr int kGateMaxGroups = 32;
 constexpr int kGateMaxTopK = 16;
-constexpr int kGateEpiWarp0 = 2;
+constexpr int kGateEpiWarp0 = 3;
 constexpr int kGateEpiWarps = 16;
 constexpr int kGateThreads = 32 * (kGateEpiWarp0 + kGateEpiWarps);
 constexpr int kGateSelStride = 260;  // floats per token row of the selection table
@@ -88,7 +93,10 @@ struct GateLayout {
     static constexpr int OFF_BIAS = (OFF_ABORT + 4 + 15) & ~15;
     static constexpr int BYTES = OFF_BIAS + kGateMaxE * 4;
     static constexpr int ALLOC = BYTES + 1024;
-    static constexpr uint32_t TMEM_COLS = 256;
+    // two accumulators (even and odd K chunks) of up to E / CS columns
+    static constexpr uint32_t ACC_COLS = kGateMaxE / CS;
+    static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
     static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -148,6 +156,25 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, fl
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c),
                  "f"(d)
                  : "memory");
+}
+// TMA 2D load written to the same shared-memory offset in every CTA of the
+// cluster named by `mask`, completing its bytes on the mbarrier at offset
+// `bar` in each of them.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0, int32_t c1,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+        : "memory");
+}
+// Arrive (once the MMAs issued so far complete) on the mbarrier at offset
+// `bar` in every CTA of the cluster named by `mask`.
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
 }
 // All threads of every CTA of the cluster: after barrier initialisation
 // (before any CTA touches another's shared memory) and before exit (no CTA
@@ -227,9 +254,9 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::ST; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), CS);  // every CTA's MMAs read the stage
         }
-        mbar_init(done_bar, 1);
+        mbar_init(done_bar, 2);  // one commit from each MMA warp
         mbar_init(step_bar, kGateEpiWarps);
         mbar_init(recv_bar, CS * 4);  // the four warps of one lane quarter in every CTA
         *abort_flag = 0;
@@ -251,44 +278,59 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         // ------------------------------------------------------------ producer
         const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + EN * 128);
         int kb = 0;
-        for (; kb < p.KB; ++kb) {
-            const int s = kb % L::ST;
-            const uint32_t ph = (kb / L::ST) & 1u;
-            if (!warp_wait(empty_bar(s), ph ^ 1u, ctl)) break;
-            if (lane == 0) {
+        if (lane == 0) {
+            for (; kb < p.KB; ++kb) {
+                const int s = kb % L::ST;
+                if (!bounded_wait(empty_bar(s), ((kb / L::ST) & 1u) ^ 1u, ctl)) break;
                 mbar_arrive_expect_tx(full_bar(s), tx);
-                tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmX, full_bar(s), kb * kGateK, m0);
+                if constexpr (CS == 1) {
+                    tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmX, full_bar(s), kb * kGateK, m0);
+                } else {
+                    // this CTA's 128 / CS rows of the x tile, to every CTA of the cluster
+                    constexpr int RQ = kGateM / CS;
+                    tma_load_2d_mc(sbase + L::OFF_A + s * L::A_BYTES + crank * (RQ * 128), &tmX, full_bar(s),
+                                   kb * kGateK, m0 + static_cast<int>(crank) * RQ, static_cast<uint16_t>((1u << CS) - 1u));
+                }
                 tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmW, full_bar(s), kb * kGateK, e0);
             }
-            __syncwarp();
         }
+        kb = __shfl_sync(0xffffffffu, kb, 0);
         // every issued load must land before the CTA's shared memory goes away
         const int first = kb > L::ST ? kb - L::ST : 0;
         for (int j = first; j < kb; ++j) drain_wait_g(full_bar(j % L::ST), (j / L::ST) & 1u, ctl);
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp <= 2) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 takes the even K chunks, warp 2 the odd ones, each into its
+        // own accumulator.  A thread's mbarrier wait does not return before
+        // the MMAs it issued earlier have completed, so with one issuer the
+        // tensor core would idle at every chunk; with two, one warp's queued
+        // chunk covers the other's wait.
+        const int j = warp - 1;
+        const uint32_t acc = tmem + static_cast<uint32_t>(j) * L::ACC_COLS;
         const uint32_t idesc = idesc_bf16_f32(kGateM, EN);
         bool issued = false;
-        for (int kb = 0; kb < p.KB; ++kb) {
-            const int s = kb % L::ST;
-            if (!warp_wait(full_bar(s), (kb / L::ST) & 1u, ctl)) break;
-            tc_fence_after();
-            if (lane == 0) {
+        if (lane == 0) {
+            for (int kb = j; kb < p.KB; kb += 2) {
+                const int s = kb % L::ST;
+                if (!bounded_wait(full_bar(s), (kb / L::ST) & 1u, ctl)) break;
+                tc_fence_after();
                 const uint64_t adesc = sdesc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
                 const uint64_t bdesc = sdesc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // K 16 = 32 bytes = +2 in the address field
-                    umma_bf16(tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-                umma_commit(empty_bar(s));
+                    umma_bf16(acc, adesc + 2u * k, bdesc + 2u * k, idesc, (kb > 1 || k > 0) ? 1u : 0u);
+                if constexpr (CS == 1)
+                    umma_commit(empty_bar(s));
+                else  // the stage's x rows came from every CTA: release it in all of them
+                    umma_commit_mc(empty_bar(s), static_cast<uint16_t>((1u << CS) - 1u));
+                issued = true;
             }
-            issued = true;
-            __syncwarp();
+            // Publish the sums (also after a wait that gave up: the status
+            // word then reports the failure and the outputs are not to be used).
+            umma_commit(done_bar);
         }
-        // Publish the sums (also after a wait that gave up: the status word
-        // then reports the failure and the outputs are not to be used).
-        if (lane == 0) umma_commit(done_bar);
         __syncwarp();
-        if (issued) drain_wait_g(done_bar, 0, ctl);
+        if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) drain_wait_g(done_bar, 0, ctl);
     } else {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - kGateEpiWarp0;
@@ -309,8 +351,13 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             const int row = CS == 1 ? quarter * 32 + lane : lane;
             const uint32_t dst = CS == 1 ? sbase + L::OFF_SEL : mapa_rank(sbase + L::OFF_SEL, quarter);
             for (int u = sl; u < EN / 16; u += 4) {
-                uint64_t pr[8];
+                uint64_t pr[8], po[8];
                 tmem_ld_x16_pairs(taddr0 + 16 * u, pr);
+                if (p.KB > 1) {  // logit = even-chunk sum + odd-chunk sum
+                    tmem_ld_x16_pairs(taddr0 + L::ACC_COLS + 16 * u, po);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) pr[i] = f2_add(pr[i], po[i]);
+                }
                 float sv[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) sv[i] = sigmoid_f32((i & 1) ? hi_f32(pr[i >> 1]) : lo_f32(pr[i >> 1]));
@@ -579,7 +626,7 @@ cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, 
     const int cs = (E % 64 == 0) ? 4 : 1;
     CUtensorMap tmX, tmW;
     cudaError_t e;
-    if ((e = make_tmap_2d(&tmX, x, 2, dim, T, ldx * 2, kGateK, kGateM, 128)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&tmX, x, 2, dim, T, ldx * 2, kGateK, kGateM / cs, 128)) != cudaSuccess) return e;
     if ((e = make_tmap_2d(&tmW, wg, 2, dim, E, dim * 2, kGateK, E / cs, 128)) != cudaSuccess) return e;
     {
         static bool ready[64];
