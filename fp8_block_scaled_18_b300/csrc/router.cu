@@ -26,14 +26,15 @@ namespace {
 
 // ------------------------------------------------------------------ gate
 //
-// A 128-token tile is taken by CS CTAs of 608 threads (a thread-block
-// cluster when CS > 1), each computing the logits of E / CS experts: warp 0
-// TMA producer (x tile 128 x 64 bf16 and E / CS gate-weight rows x 64 bf16
-// per 128-byte K chunk, 128-byte swizzle, a ring of GateLayout::ST stages),
-// warps 1 and 2 MMA issuers (four tcgen05.mma.kind::f16, M 128, N E / CS,
-// K 16, per chunk; warp 1 the even chunks, warp 2 the odd ones, each into its
-// own TMEM accumulator; warp 1 owns the TMEM allocation), warps 3-18 the
-// epilogue (four warps per TMEM lane quarter), which adds the two sums.  In a cluster each CTA loads
+// A 128-token tile is taken by CS CTAs of 640 threads (a thread-block
+// cluster when CS > 1), each computing the logits of E / CS experts: warps
+// 0 and 1 TMA producers (x tile 128 x 64 bf16 and E / CS gate-weight rows x
+// 64 bf16 per 128-byte K chunk, 128-byte swizzle, a ring of GateLayout::ST
+// stages; warp 0 the even chunks, warp 1 the odd ones), warps 2 and 3 MMA
+// issuers (four tcgen05.mma.kind::f16, M 128, N E / CS, K 16, per chunk;
+// even and odd chunks again, each into its own TMEM accumulator; warp 2 owns
+// the TMEM allocation), warps 4-19 the epilogue (four warps per TMEM lane
+// quarter), which adds the two sums.  In a cluster each CTA loads
 // 128 / CS rows of the x tile and multicasts them to all CTAs (each stage
 // is then released by the MMAs of every CTA), so the tile leaves L2 once.
 // Epilogue:
@@ -55,7 +56,7 @@ constexpr int kGateK = 64;            // bf16 elements per 128-byte chunk
 constexpr int kGateMaxE = 256;
 constexpr int kGateMaxGroups = 32;
 constexpr int kGateMaxTopK = 16;
-constexpr int kGateEpiWarp0 = 3;
+constexpr int kGateEpiWarp0 = 4;
 constexpr int kGateEpiWarps = 16;
 constexpr int kGateThreads = 32 * (kGateEpiWarp0 + kGateEpiWarps);
 constexpr int kGateSelStride = 260;  // floats per token row of the selection table
@@ -69,7 +70,15 @@ static_assert(kGateMaxE <= 8 * 32, "eight experts per lane");
 // room for a deeper ring.
 template <int CS>
 struct GateLayout {
-    static constexpr int ST = CS == 1 ? 4 : 7;  // pipeline stages
+    // Pipeline stages, a multiple of 2: two producer warps and two MMA warps
+    // each take every other K chunk, so a warp's chunks always fall on the
+    // stages of one parity and the chunk it waits for on a stage is the one
+    // right after its own previous chunk there.  (With an odd count the
+    // previous chunk on a stage would belong to the other warp and might not
+    // have landed yet; a parity wait would then see the phase before it as
+    // complete.)
+    static constexpr int ST = CS == 1 ? 4 : 6;
+    static_assert(ST % 2 == 0, "stages per warp parity");
     static constexpr int A_BYTES = kGateM * 128;
     static constexpr int B_BYTES = (kGateMaxE / CS) * 128;
     static constexpr int OFF_A = 0;
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     if constexpr (CS > 1) cluster_sync_all();  // every CTA's barriers exist before any remote access
     grid_dependency_wait();
     allow_dependents();
-    if (warp == 1) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
+    if (warp == 2) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) bias_s[e] = p.bias ? p.bias[e] : 0.0f;
     tc_fence_before();
     __syncthreads();
@@ -274,12 +283,16 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     const WaitCtl ctl{abort_flag, p.err, p.timeout_ns};
     const int m0 = (blockIdx.x / CS) * kGateM;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp <= 1) {
+        // ------------------------------------------------------------ producers
+        // Warp 0 loads the even K chunks, warp 1 the odd ones: a warp's wait
+        // on a stage also holds until its own earlier copies have landed, so
+        // two producers keep twice the loads in flight.
+        const int j = warp;
         const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + EN * 128);
-        int kb = 0;
+        int kb = j;
         if (lane == 0) {
-            for (; kb < p.KB; ++kb) {
+            for (; kb < p.KB; kb += 2) {
                 const int s = kb % L::ST;
                 if (!bounded_wait(empty_bar(s), ((kb / L::ST) & 1u) ^ 1u, ctl)) break;
                 mbar_arrive_expect_tx(full_bar(s), tx);
@@ -294,18 +307,19 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                 tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmW, full_bar(s), kb * kGateK, e0);
             }
         }
-        kb = __shfl_sync(0xffffffffu, kb, 0);
-        // every issued load must land before the CTA's shared memory goes away
-        const int first = kb > L::ST ? kb - L::ST : 0;
-        for (int j = first; j < kb; ++j) drain_wait_g(full_bar(j % L::ST), (j / L::ST) & 1u, ctl);
-    } else if (warp <= 2) {
+        kb = __shfl_sync(0xffffffffu, kb, 0);  // one past this warp's last issued chunk
+        // every issued load must land before the CTA's shared memory goes
+        // away: the last use of each of this warp's stages
+        for (int c = j; c < kb; c += 2)
+            if (c + L::ST >= kb) drain_wait_g(full_bar(c % L::ST), (c / L::ST) & 1u, ctl);
+    } else if (warp <= 3) {
         // ------------------------------------------------------------ MMA issuers
-        // Warp 1 takes the even K chunks, warp 2 the odd ones, each into its
+        // Warp 2 takes the even K chunks, warp 3 the odd ones, each into its
         // own accumulator.  A thread's mbarrier wait does not return before
         // the MMAs it issued earlier have completed, so with one issuer the
         // tensor core would idle at every chunk; with two, one warp's queued
         // chunk covers the other's wait.
-        const int j = warp - 1;
+        const int j = warp - 2;
         const uint32_t acc = tmem + static_cast<uint32_t>(j) * L::ACC_COLS;
         const uint32_t idesc = idesc_bf16_f32(kGateM, EN);
         bool issued = false;
@@ -470,7 +484,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, L::TMEM_COLS);
     }
