@@ -292,7 +292,7 @@ fp8bs_status fp8bs_moe_route(const int32_t* ids, const float* weights, int64_t T
                              int32_t* offsets, int32_t* token_of_row, int32_t* rows_of_token, float* weight_of_row,
                              fp8bs_stream_t stream) {
     if (T < 0 || top_k <= 0 || E <= 0) return FP8BS_ERR_INVALID_ARG;
-    if (E > 256) return FP8BS_ERR_UNSUPPORTED;
+    if (E > 256 || top_k > 16) return FP8BS_ERR_UNSUPPORTED;
     if (!offsets) return FP8BS_ERR_INVALID_ARG;
     if (T > 0 && (!ids || !weights || !token_of_row || !rows_of_token || !weight_of_row)) return FP8BS_ERR_INVALID_ARG;
     if (T * static_cast<int64_t>(top_k) > kMaxRows) return FP8BS_ERR_UNSUPPORTED;

@@ -493,35 +493,50 @@ __global__ void __launch_bounds__(kGateThreads, 1)
 
 // ------------------------------------------------------------------ routing tables
 //
-// Several CTAs, each owning a contiguous chunk of tokens.  Every CTA counts
-// all the selections per expert (shared-memory atomics: a count is the same
-// whatever the order), splitting them into those of tokens before its chunk
-// and those of its own tokens; the exclusive scan of the totals gives the
-// offsets, and expert e's rows for the chunk start at offsets[e] + the count
-// of earlier tokens that chose e.  Inside the chunk the rank of a selection
-// is formed without any ordering race: tokens are taken kRouteThreads at a
-// time, one per thread; each warp marks, per expert, the lanes that chose it
-// (a 32-bit mask built with atomicOr), a scan over the warps gives each
-// warp's base per expert, and a lane's rank is its warp's base plus the
-// number of lower lanes in the mask.  The rows a chunk owns first get token
-// -1 / gate 0, so a row no selection reaches (a token naming an expert
-// twice) is visible as an out-of-range id downstream.  Re-reading every
-// selection per CTA costs T * top_k * 4 bytes of L2 reads per CTA; the grid
-// is capped at two CTAs per SM.
+// One thread-block cluster of kRouteCtas CTAs, each owning a contiguous
+// chunk of tokens.  Each CTA counts its own chunk's selections per expert
+// (shared-memory atomics: a count is the same whatever the order); after a
+// cluster barrier every CTA reads all the chunks' counts through distributed
+// shared memory, which gives both the totals (their exclusive scan is the
+// offsets) and, per expert, the selections of the chunks before its own:
+// expert e's rows for a chunk start at offsets[e] + that count.  Inside the
+// chunk the rank of a selection is formed without any ordering race: tokens
+// are taken kRouteThreads at a time, one per thread; each warp marks, per
+// expert, the lanes that chose it (a 32-bit mask built with atomicOr), a scan
+// over the warps gives each warp's base per expert, and a lane's rank is its
+// warp's base plus the number of lower lanes in the mask.  A round's rows are
+// gathered in shared memory expert by expert and leave as contiguous runs
+// (coalesced stores).  Rows no selection reaches (a token naming an expert
+// twice) get token -1 / gate 0, visible as an out-of-range id downstream.
 constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteMaxE = 256;
-constexpr int kRouteChunk = 128;  // tokens per CTA, at least
+constexpr int kRouteCtas = 8;  // one cluster (the portable maximum)
+constexpr int kRouteMaxK = 16;
+constexpr int kRouteBatch = 8;  // global loads a thread keeps in flight
 
 struct RouteSmem {
     uint32_t mask[kRouteWarps][kRouteMaxE];
     int32_t base[kRouteWarps][kRouteMaxE];
+    int32_t sel_e[kRouteThreads * kRouteMaxK];  // one round's selections, staged
+    float sel_w[kRouteThreads * kRouteMaxK];
+    int32_t ltok[kRouteThreads * kRouteMaxK];   // one round's rows, expert by expert
+    float lw[kRouteThreads * kRouteMaxK];
+    int32_t rstart[kRouteMaxE];                 // the round's first row of each expert
+    int32_t rcnt[kRouteMaxE];                   // and its number of rows
+    int32_t loc[kRouteMaxE];                    // where they start in ltok / lw
+    int32_t mine[kRouteMaxE];  // this chunk's selections per expert (read by the whole cluster)
     int32_t total[kRouteMaxE];
     int32_t before[kRouteMaxE];
-    int32_t mine[kRouteMaxE];
     int32_t next[kRouteMaxE];
     int32_t scan[kRouteMaxE + 1];
 };
+
+__device__ __forceinline__ int32_t ld_cluster_s32(uint32_t cluster_addr) {
+    int32_t v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
 
 __global__ void __launch_bounds__(kRouteThreads)
     moe_route_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, int T, int top_k, int E,
@@ -530,35 +545,50 @@ __global__ void __launch_bounds__(kRouteThreads)
                      unsigned* __restrict__ err) {
     extern __shared__ uint8_t route_smem_raw[];
     RouteSmem& sm = *reinterpret_cast<RouteSmem*>(route_smem_raw);
-    grid_dependency_wait();
-    allow_dependents();
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int wp = tid >> 5;
-    const int t_begin = blockIdx.x * chunk;
+    const int me = static_cast<int>(cluster_rank());
+    const int t_begin = min(T, me * chunk);
     const int t_end = min(T, t_begin + chunk);
-    const int64_t R = static_cast<int64_t>(T) * top_k;
+    for (int e = tid; e < E; e += kRouteThreads) sm.mine[e] = 0;
+    __syncthreads();
+    grid_dependency_wait();
+    allow_dependents();
+    // this chunk's counts
+    bool bad = false;
     const int64_t i_begin = static_cast<int64_t>(t_begin) * top_k;
     const int64_t i_end = static_cast<int64_t>(t_end) * top_k;
-    for (int e = tid; e < E; e += kRouteThreads) {
-        sm.total[e] = 0;
-        sm.before[e] = 0;
-        sm.mine[e] = 0;
-    }
-    __syncthreads();
-    // counts over every selection: all tokens, those before this chunk, this chunk's
-    bool bad = false;
-    for (int64_t i = tid; i < R; i += kRouteThreads) {
-        const int e = __ldg(ids + i);
-        const bool own = i >= i_begin && i < i_end;
-        if (e >= 0 && e < E) {
-            atomicAdd(&sm.total[e], 1);
-            if (i < i_begin) atomicAdd(&sm.before[e], 1);
-            else if (own) atomicAdd(&sm.mine[e], 1);
-        } else if (own) {
-            bad = true;  // reported by the CTA that owns the token
+    for (int64_t i0 = i_begin; i0 < i_end; i0 += kRouteBatch * kRouteThreads) {
+        int ev[kRouteBatch];
+#pragma unroll
+        for (int u = 0; u < kRouteBatch; ++u) {  // all loads first, then the counts
+            const int64_t i = i0 + u * kRouteThreads + tid;
+            ev[u] = i < i_end ? __ldg(ids + i) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kRouteBatch; ++u) {
+            if (i0 + u * kRouteThreads + tid >= i_end) continue;
+            if (ev[u] >= 0 && ev[u] < E) atomicAdd(&sm.mine[ev[u]], 1);
+            else bad = true;
         }
     }
+    __syncthreads();
+    cluster_sync_all();  // every chunk's counts are complete and visible
+    // totals and the counts of the chunks before this one
+    const uint32_t mine0 = smem_u32(&sm.mine[0]);
+    for (int e = tid; e < E; e += kRouteThreads) {
+        int tot = 0, bef = 0;
+        for (int c = 0; c < kRouteCtas; ++c) {
+            const int v = ld_cluster_s32(mapa_rank(mine0 + 4u * static_cast<uint32_t>(e), static_cast<uint32_t>(c)));
+            tot += v;
+            if (c < me) bef += v;
+        }
+        sm.total[e] = tot;
+        sm.before[e] = bef;
+    }
+    // the peers may leave once everyone has read their counts
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     __syncthreads();
     // exclusive scan of the totals (one warp; E <= 256)
     if (wp == 0) {
@@ -578,24 +608,38 @@ __global__ void __launch_bounds__(kRouteThreads)
         if (lane == 0) sm.scan[E] = run;
     }
     __syncthreads();
-    if (blockIdx.x == 0)
+    if (me == 0)
         for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = sm.scan[e];
-    for (int e = tid; e < E; e += kRouteThreads) {
-        const int first = sm.scan[e] + sm.before[e];  // this chunk's first row of expert e
-        sm.next[e] = first;
-        for (int r = first; r < first + sm.mine[e]; ++r) {
-            token_of_row[r] = -1;
-            weight_of_row[r] = 0.0f;
-        }
-    }
+    for (int e = tid; e < E; e += kRouteThreads) sm.next[e] = sm.scan[e] + sm.before[e];  // this chunk's first row of e
     const uint32_t lt = (1u << lane) - 1u;
     for (int t0 = t_begin; t0 < t_end; t0 += kRouteThreads) {
+        // stage the round's selections and gate values (coalesced, loads in flight together)
+        const int nsel = (min(t_end, t0 + kRouteThreads) - t0) * top_k;
+        const int64_t g0 = static_cast<int64_t>(t0) * top_k;
+        for (int j0 = 0; j0 < nsel; j0 += kRouteBatch * kRouteThreads) {
+            int ev[kRouteBatch];
+            float wv[kRouteBatch];
+#pragma unroll
+            for (int u = 0; u < kRouteBatch; ++u) {
+                const int j = j0 + u * kRouteThreads + tid;
+                ev[u] = j < nsel ? __ldg(ids + g0 + j) : 0;
+                wv[u] = j < nsel ? __ldg(w + g0 + j) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kRouteBatch; ++u) {
+                const int j = j0 + u * kRouteThreads + tid;
+                if (j < nsel) {
+                    sm.sel_e[j] = ev[u];
+                    sm.sel_w[j] = wv[u];
+                }
+            }
+        }
         for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) sm.mask[i / E][i % E] = 0u;
         __syncthreads();
         const int t = t0 + tid;
         if (t < t_end) {
             for (int k = 0; k < top_k; ++k) {
-                const int e = __ldg(ids + static_cast<int64_t>(t) * top_k + k);
+                const int e = sm.sel_e[tid * top_k + k];
                 if (e >= 0 && e < E) {
                     const uint32_t old = atomicOr(&sm.mask[wp][e], 1u << lane);
                     if (old & (1u << lane)) bad = true;  // the same expert twice for one token
@@ -605,29 +649,67 @@ __global__ void __launch_bounds__(kRouteThreads)
         __syncthreads();
         for (int e = tid; e < E; e += kRouteThreads) {
             int run = sm.next[e];
+            sm.rstart[e] = run;
             for (int q = 0; q < kRouteWarps; ++q) {
                 sm.base[q][e] = run;
                 run += __popc(sm.mask[q][e]);
             }
+            sm.rcnt[e] = run - sm.next[e];
             sm.next[e] = run;
+        }
+        __syncthreads();
+        // exclusive scan of the round's row counts: each expert's place in ltok / lw
+        if (wp == 0) {
+            int run = 0;
+            for (int e0 = 0; e0 < E; e0 += 32) {
+                const int e = e0 + lane;
+                const int c = e < E ? sm.rcnt[e] : 0;
+                int incl = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                if (e < E) sm.loc[e] = run + incl - c;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
         }
         __syncthreads();
         if (t < t_end) {
             for (int k = 0; k < top_k; ++k) {
                 const int64_t i = static_cast<int64_t>(t) * top_k + k;
-                const int e = __ldg(ids + i);
+                const int e = sm.sel_e[tid * top_k + k];
                 int32_t r = -1;
                 if (e >= 0 && e < E) {
                     r = sm.base[wp][e] + __popc(sm.mask[wp][e] & lt);
-                    token_of_row[r] = t;
-                    weight_of_row[r] = __ldg(w + i);
+                    const int j = sm.loc[e] + (r - sm.rstart[e]);
+                    sm.ltok[j] = t;
+                    sm.lw[j] = sm.sel_w[tid * top_k + k];
                 }
                 rows_of_token[i] = r;
             }
         }
         __syncthreads();
+        // each expert's rows of the round are contiguous: one warp copies them out
+        for (int e = wp; e < E; e += kRouteWarps) {
+            const int n = sm.rcnt[e], r0 = sm.rstart[e], j0 = sm.loc[e];
+            for (int q = lane; q < n; q += 32) {
+                token_of_row[r0 + q] = sm.ltok[j0 + q];
+                weight_of_row[r0 + q] = sm.lw[j0 + q];
+            }
+        }
+        __syncthreads();
+    }
+    // rows no selection reached (a token naming an expert twice): token -1, gate 0
+    for (int e = wp; e < E; e += kRouteWarps) {
+        const int end = sm.scan[e] + sm.before[e] + sm.mine[e];
+        for (int r = sm.next[e] + lane; r < end; r += 32) {
+            token_of_row[r] = -1;
+            weight_of_row[r] = 0.0f;
+        }
     }
     if (bad) atomicOr(err, kDevErrIndex);
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace
@@ -697,15 +779,23 @@ cudaError_t launch_moe_route(const int32_t* ids, const float* w, int64_t T, int 
         if (e != cudaSuccess) return e;
         ready[dev.device] = true;
     }
-    // chunks of at least kRouteChunk tokens, at most two per SM
-    const int64_t max_chunks = std::max<int64_t>(1, 2 * static_cast<int64_t>(dev.num_sms));
-    const int64_t nchunks = std::max<int64_t>(1, std::min<int64_t>((T + kRouteChunk - 1) / kRouteChunk, max_chunks));
-    const int chunk = static_cast<int>(std::max<int64_t>(1, (T + nchunks - 1) / nchunks));
-    // T == 0: one CTA still writes the (all-zero) offsets
-    const int grid = static_cast<int>(std::max<int64_t>(1, (T + chunk - 1) / chunk));
-    return launch_pdl(moe_route_kernel, dim3(grid), dim3(kRouteThreads), sizeof(RouteSmem), stream, ids, w,
-                      static_cast<int>(T), top_k, E, chunk, offsets, token_of_row, rows_of_token, weight_of_row,
-                      dev.err);
+    // one cluster; chunks of ceil(T / kRouteCtas) tokens (T == 0: the CTAs
+    // still write the all-zero offsets)
+    const int chunk = static_cast<int>(std::max<int64_t>(1, (T + kRouteCtas - 1) / kRouteCtas));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kRouteCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kRouteCtas);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.dynamicSmemBytes = sizeof(RouteSmem);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_route_kernel, ids, w, static_cast<int>(T), top_k, E, chunk, offsets,
+                              token_of_row, rows_of_token, weight_of_row, dev.err);
 }
 
 }  // namespace fp8bs

@@ -350,8 +350,8 @@ fp8bs_status fp8bs_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, 
  *      its token and gate value
  *   rows_of_token int32 [T, top_k]: the routed row of selection (t, k)
  * from ids int32 [T, top_k] and weights fp32 [T, top_k] (fp8bs_moe_gate's
- * outputs).  E <= 256 (else FP8BS_ERR_UNSUPPORTED); all pointers 4-byte
- * aligned.  An id outside [0, E) gets no row (rows_of_token -1); a token
+ * outputs).  E <= 256 and top_k <= 16 (else FP8BS_ERR_UNSUPPORTED); all
+ * pointers 4-byte aligned.  An id outside [0, E) gets no row (rows_of_token -1); a token
  * naming one expert twice leaves a row with token -1 and gate 0; both set
  * FP8BS_ERR_INDEX for the next fp8bs_sync_status(). */
 fp8bs_status fp8bs_moe_route(const int32_t* ids, const float* weights, int64_t T, int32_t top_k, int32_t E,

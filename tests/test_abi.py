@@ -249,6 +249,8 @@ def test_moe_route_validation():
     args = [A, A, 64, 8, 256, A, A, A, A, None]
     bad = list(args); bad[4] = 300
     assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # E > 256
+    bad = list(args); bad[3] = 17
+    assert f(*bad) == fp8bs.FP8BS_ERR_UNSUPPORTED                                 # top_k > 16
     bad = list(args); bad[3] = 0
     assert f(*bad) == fp8bs.FP8BS_ERR_INVALID_ARG
     bad = list(args); bad[6] = None

@@ -167,7 +167,7 @@ def test_gate_without_bias_and_strided_x(F, orc):
 # ------------------------------------------------------------------ routing tables
 
 
-@pytest.mark.parametrize("T,k,E", [(1500, 8, 256), (4096, 8, 256), (3, 2, 16), (1025, 1, 64)])
+@pytest.mark.parametrize("T,k,E", [(1500, 8, 256), (4096, 8, 256), (3, 2, 16), (1025, 1, 64), (20000, 6, 128)])
 def test_route_bit_exact(F, orc, T, k, E):
     rng = np.random.default_rng(T + k)
     ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
