@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfp8bs.so")
-SOURCES = ["status.cu", "tmap.cu", "quant.cu", "gemm.cu", "moe.cu", "router.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["status.cu", "tmap.cu", "quant.cu", "gemm.cu", "skinny.cu", "moe.cu", "router.cu", "api.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "codec.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

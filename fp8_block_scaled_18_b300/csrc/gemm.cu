@@ -1108,6 +1108,7 @@ cudaError_t launch_bn(int bn, const GemmArgs& a, Params& p, int grid, const Devi
 }  // namespace
 
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+    if (gemm_skinny_applies(M, N, K)) return 0;
     return dense_plan(M, N, K, dev.num_sms, ~size_t{0}).ws;
 }
 
@@ -1137,6 +1138,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s
         return launch_mode<256, kStages256, kGrouped>(a, p, dev.num_sms, dev, stream);
     }
     const bool fused = a.bias != nullptr || a.yq != nullptr;
+    if (!fused && gemm_skinny_applies(a.M, a.N, a.K)) return launch_gemm_skinny(a, dev, stream);
     Plan pl = dense_plan(a.M, a.N, a.K, dev.num_sms, a.workspace && !fused ? a.ws_bytes : 0);
     if (a.yq != nullptr && pl.bn != 256) {
         // Output quantisation needs each promotion warpgroup to hold one whole

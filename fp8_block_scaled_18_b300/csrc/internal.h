@@ -115,6 +115,11 @@ struct GemmArgs {
 
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 cudaError_t launch_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+// Few tokens (M <= 128, K within 8 CTAs' chunk budget: 8192 for M <= 64,
+// 4096 for M <= 128): the weight-streaming kernel of skinny.cu (one launch,
+// no workspace); launch_gemm takes it for plain dense GEMMs.
+bool gemm_skinny_applies(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_skinny(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 // Weight gradient dW [N, K] fp32 = dY^T X over T tokens from the column-
 // quantised (128x1 groups along the tokens) operands, stored transposed:

@@ -145,19 +145,7 @@ __device__ __forceinline__ bool drain_wait_g(uint32_t bar, uint32_t parity, cons
     return ok;
 }
 
-// ---- thread-block cluster helpers (distributed shared memory, remote mbarriers)
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// The shared::cluster address of `addr` (a shared::cta address of this CTA)
-// in the CTA of the cluster with the given rank.
-__device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
-    uint32_t d;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
-    return d;
-}
+// ---- thread-block cluster helpers (remote mbarriers, multicast)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -184,12 +172,6 @@ __device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
         "h"(mask)
         : "memory");
-}
-// All threads of every CTA of the cluster: after barrier initialisation
-// (before any CTA touches another's shared memory) and before exit (no CTA
-// leaves while a peer may still write into it).
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -531,12 +513,6 @@ struct RouteSmem {
     int32_t next[kRouteMaxE];
     int32_t scan[kRouteMaxE + 1];
 };
-
-__device__ __forceinline__ int32_t ld_cluster_s32(uint32_t cluster_addr) {
-    int32_t v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-    return v;
-}
 
 __global__ void __launch_bounds__(kRouteThreads)
     moe_route_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, int T, int top_k, int E,

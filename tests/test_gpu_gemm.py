@@ -82,10 +82,37 @@ def test_gemm_tile_widths(F, orc, orc_mt, M, N, K):
     assert_gemm_close(host(y), y_ref, L, f"gemm {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M", [1, 16, 64])
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1536, 7168),    # the decode shape: K over a cluster of 8 CTAs, 7 chunks each
+    (33, 300, 1280),    # 10 chunks: clusters of 5 CTAs of 2 chunks; 48 token columns; ragged N
+    (64, 256, 8192),    # 64 chunks: 8 per CTA (each in its own stage and TMEM columns), 64 tokens
+    (16, 7168, 7168),   # 56 weight tiles x 8 CTAs: several waves of clusters
+    (2, 1, 384),        # one output column, 3 chunks
+    (128, 256, 512),    # the tiny configuration's shape: 128 token columns, one chunk per CTA
+    (100, 300, 2048),   # 112 token columns (30 KB stages, 4 chunks at most): 2 chunks on each of 8 CTAs
+    (128, 1536, 4096),  # 128 token columns, 4 chunks per CTA: all 512 TMEM columns
+])
+def test_gemm_few_tokens(F, orc, M, N, K):
+    """Few tokens (M <= 128 and K within the cluster's chunk budget) take the
+    weight-streaming kernel (weight rows on the MMA's 128-row side, tokens on
+    N, K split over a cluster and summed through distributed shared memory):
+    every element against the oracle, the same bits with and without a
+    workspace, and run to run."""
+    rng = np.random.default_rng(M + N + K)
+    x = synth.activations(rng, M, K, n_outlier=4, outlier_scale=25.0)
+    w = synth.normal_bf16(rng, (N, K), 0.02)
+    assert F.fp8bs_gemm_workspace_size(M, N, K) == 0
+    _, y1 = _gemm_only(F, orc, x, w, workspace=True)
+    _, y2 = _gemm_only(F, orc, x, w, workspace=False)
+    assert np.array_equal(y1, y2)
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 96])
 def test_gemm_decode_split_k_matches_unsplit(F, orc, M):
-    """Small-M uses a split-K plan when a workspace is given; both plans are
-    within the bound, and each is bit-reproducible run to run."""
+    """q_down (K = 7168): M <= 64 runs the weight-streaming kernel with or
+    without a workspace; M = 96 (too many chunks for its 96 token columns)
+    uses the split-K plan when a workspace is given.  Every plan is within the
+    bound and bit-reproducible run to run."""
     c = synth.q_down(M)
     r1, y1 = _gemm_only(F, orc, c.x, c.w, workspace=True)
     r2, y2 = _gemm_only(F, orc, c.x, c.w, workspace=False)
