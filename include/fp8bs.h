@@ -118,10 +118,14 @@ fp8bs_status fp8bs_weight_dequant(const uint8_t* wq, const float* sw, int64_t N,
  *   sw [ceil(N/128), K/128] fp32 dense
  *   y  [M, N] bf16, row stride ldy (ldy >= N, ldy % 8 == 0), 16-byte aligned
  *   workspace: optional device scratch for the split-K path used when M is
- *     small; may be NULL (then no split).  fp8bs_gemm_workspace_size() gives
- *     the size that enables the fastest plan; a smaller buffer selects fewer
- *     splits.  Contents on entry are ignored; the caller must not use it
- *     concurrently from another call. */
+ *     small but above the few-token kernel's range; may be NULL (then no
+ *     split).  fp8bs_gemm_workspace_size() gives the size that enables the
+ *     fastest plan; a smaller buffer selects fewer splits.  Contents on entry
+ *     are ignored; the caller must not use it concurrently from another call.
+ * Few tokens (M <= 64 with K <= 8192, or M <= 128 with K <= 4096) run a
+ * weight-streaming kernel that splits K over a thread-block cluster and adds
+ * the pieces in shared memory: one launch, no workspace, the same bits with
+ * or without one. */
 fp8bs_status fp8bs_gemm(const uint8_t* xq, const float* sx, int64_t lds,
                         const uint8_t* wq, const float* sw,
                         int64_t M, int64_t N, int64_t K,
@@ -183,7 +187,8 @@ size_t fp8bs_grouped_gemm_workspace_size(int32_t G, int64_t N, int64_t K);
  * DeepSeek-V3 pages have no counterpart: this is an interface for such
  * callers, computing exactly what fp8bs_gemm computes.
  * Same arguments and results as fp8bs_gemm without the workspace: the
- * split-K scratch of the small-M plan comes from a fixed array of
+ * split-K scratch of the small-M plan (above the few-token kernel's range,
+ * which needs none) comes from a fixed array of
  * FP8BS_NOALLOC_SCRATCH_BYTES inside the library's device image (every device
  * that loads the library holds it until the process exits).  Returns
  * FP8BS_ERR_UNSUPPORTED, launching nothing, when the shape's plan needs more
