@@ -27,30 +27,33 @@ namespace {
 // ------------------------------------------------------------------ gate
 //
 // A 128-token tile is taken by CS CTAs of 640 threads (a thread-block
-// cluster when CS > 1), each computing the logits of E / CS experts: warps
-// 0 and 1 TMA producers (x tile 128 x 64 bf16 and E / CS gate-weight rows x
-// 64 bf16 per 128-byte K chunk, 128-byte swizzle, a ring of GateLayout::ST
-// stages; warp 0 the even chunks, warp 1 the odd ones), warps 2 and 3 MMA
-// issuers (four tcgen05.mma.kind::f16, M 128, N E / CS, K 16, per chunk;
-// even and odd chunks again, each into its own TMEM accumulator; warp 2 owns
-// the TMEM allocation), warps 4-19 the epilogue (four warps per TMEM lane
-// quarter), which adds the two sums.  In a cluster each CTA loads
-// 128 / CS rows of the x tile and multicasts them to all CTAs (each stage
-// is then released by the MMAs of every CTA), so the tile leaves L2 once.
+// cluster of 4 when E % 64 == 0, else one CTA), each computing all E logits
+// over a quarter of K: warps 0 and 1 TMA producers (x tile 128 x 64 bf16 and
+// the E gate-weight rows x 64 bf16 per 128-byte K chunk, 128-byte swizzle, a
+// ring of 4 stages; warp 0 the even chunks, warp 1 the odd ones), warps 2 and
+// 3 MMA issuers (four tcgen05.mma.kind::f16, M 128, N E, K 16, per chunk; even
+// and odd chunks again, each into its own TMEM accumulator; warp 2 owns the
+// TMEM allocation), warps 4-19 the epilogue (four warps per TMEM lane
+// quarter), which adds the two sums.  With N = E the tensor core reads each
+// x chunk once for all the experts.
 // Epilogue:
-//   1. each warp turns 16-column units of its 32 tokens' logits into
-//      affinities s = sigmoid(l) and writes them, token-major, into the
-//      selection table of the CTA that selects for those tokens (the CTA
-//      itself when CS == 1; cluster rank q takes tokens 32q .. 32q + 31 of
-//      the tile, so a lane quarter's rows go to one CTA of the cluster);
+//   1. (cluster) each CTA writes its partial logits, token-major, into its own
+//      shared memory; after a cluster barrier cluster rank q adds, for tokens
+//      32q .. 32q + 31 of the tile, the CS partials in rank order (16-byte
+//      loads through distributed shared memory) and applies the sigmoid.
+//      (One CTA) the sums become affinities directly.  Either way the
+//      affinities land token-major in the CTA's selection table.
 //   2. one warp per token, lane l holding experts l, l + 32, ...: group
 //      scores (largest s + bias of each group) by warp max-reductions, the
-//      topk_groups best groups (lower index on ties), then top_k rounds of
-//      a warp arg-max over the kept experts' biased affinities (lower expert
-//      on ties), and the gate values from the chosen s.
+//      topk_groups best groups (lower index on ties); each lane then sorts
+//      its kept candidates once, and top_k rounds take the warp's best head
+//      (a max-reduction, then a min-reduction over the expert index for ties,
+//      lower expert first) and advance the winning lane's list; the gate
+//      values come from the chosen s in rank order.
 // Values are compared through an order-preserving map of their fp32 bits
 // to unsigned integers, so the hardware warp reductions give exact fp32
-// comparisons.  The two steps meet at an mbarrier with a bounded wait.
+// comparisons.  The steps meet at a bounded mbarrier wait (one CTA) or
+// cluster barriers.
 constexpr int kGateM = 128;
 constexpr int kGateK = 64;            // bf16 elements per 128-byte chunk
 constexpr int kGateMaxE = 256;
@@ -59,15 +62,14 @@ constexpr int kGateMaxTopK = 16;
 constexpr int kGateEpiWarp0 = 4;
 constexpr int kGateEpiWarps = 16;
 constexpr int kGateThreads = 32 * (kGateEpiWarp0 + kGateEpiWarps);
-constexpr int kGateSelStride = 260;  // floats per token row of the selection table
+constexpr int kGateRowStride = 260;   // floats per token row of the partial-logit and selection tables
 static_assert(kGateMaxGroups <= 32 && kGateMaxTopK <= 32, "one lane per group and per chosen expert");
 static_assert(kGateMaxE <= 8 * 32, "eight experts per lane");
 
-// Shared memory of one CTA.  When CS == 1 the selection table lies over the
-// pipeline stages (written once this CTA's sums are complete); in a cluster
-// the peers write into it while this CTA may still be in its K loop, so it
-// has its own space, and the smaller stages (E / CS weight rows) still leave
-// room for a deeper ring.
+// Shared memory of one CTA.  After the K loop the pipeline stages hold (one
+// CTA) the selection table, or (cluster) this CTA's partial logits for all
+// 128 tokens and, beside them, the selection table of its 32 tokens -- apart,
+// because the peers read the partial logits while the table is written.
 template <int CS>
 struct GateLayout {
     // Pipeline stages, a multiple of 2: two producer warps and two MMA warps
@@ -77,35 +79,37 @@ struct GateLayout {
     // previous chunk on a stage would belong to the other warp and might not
     // have landed yet; a parity wait would then see the phase before it as
     // complete.)
-    static constexpr int ST = CS == 1 ? 4 : 6;
+    static constexpr int ST = 4;
     static_assert(ST % 2 == 0, "stages per warp parity");
     static constexpr int A_BYTES = kGateM * 128;
-    static constexpr int B_BYTES = (kGateMaxE / CS) * 128;
+    static constexpr int B_BYTES = kGateMaxE * 128;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = ST * A_BYTES;
     static constexpr int STAGES_END = OFF_B + ST * B_BYTES;
-    // selection table: affinities [NT tokens][kGateSelStride] fp32 (the
-    // stride keeps both the per-token-row writes and the per-expert reads
-    // free of bank conflicts and rows 16-byte aligned), then per-warp group
-    // keys [16][32] u32
+    // (cluster) partial logits [128 tokens][kGateRowStride] fp32; the stride
+    // keeps both the per-token-row accesses and the per-expert reads free of
+    // bank conflicts and rows 16-byte aligned
+    static constexpr int OFF_PART = 0;
+    static constexpr int PART_END = CS == 1 ? 0 : kGateM * kGateRowStride * 4;
+    // selection table: affinities [NT tokens][kGateRowStride] fp32, then
+    // per-warp group keys [16][32] u32
     static constexpr int NT = kGateM / CS;
-    static constexpr int OFF_SEL = CS == 1 ? 0 : STAGES_END;
-    static constexpr int OFF_GK = OFF_SEL + NT * kGateSelStride * 4;
+    static constexpr int OFF_SEL = PART_END;
+    static constexpr int OFF_GK = OFF_SEL + NT * kGateRowStride * 4;
     static constexpr int SEL_END = OFF_GK + kGateEpiWarps * kGateMaxGroups * 4;
-    static_assert(CS > 1 || SEL_END <= STAGES_END, "the selection table fits in the pipeline stages");
-    // full[ST], empty[ST], done, the epilogue's step barrier, recv (the
-    // selection table is complete)
-    static constexpr int OFF_BAR = CS == 1 ? STAGES_END : SEL_END;
-    static constexpr int NUM_BARS = 2 * ST + 3;
+    static_assert(SEL_END <= STAGES_END, "the tables fit in the pipeline stages");
+    // full[ST], empty[ST], done, the epilogue's step barrier
+    static constexpr int OFF_BAR = STAGES_END;
+    static constexpr int NUM_BARS = 2 * ST + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_BIAS = (OFF_ABORT + 4 + 15) & ~15;
     static constexpr int BYTES = OFF_BIAS + kGateMaxE * 4;
     static constexpr int ALLOC = BYTES + 1024;
-    // two accumulators (even and odd K chunks) of up to E / CS columns
-    static constexpr uint32_t ACC_COLS = kGateMaxE / CS;
+    // two accumulators (even and odd K chunks) of up to E columns
+    static constexpr uint32_t ACC_COLS = kGateMaxE;
     static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
-    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
+    static_assert(TMEM_COLS <= 512, "TMEM allocation");
     static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -114,6 +118,7 @@ struct GateParams {
     int32_t* ids;       // [T, top_k]
     float* w;           // [T, top_k]
     int T, KB, E, n_groups, topk_groups, top_k;
+    int kps;            // K chunks per cluster rank
     float route_scale;
     unsigned* err;
     uint64_t timeout_ns;
@@ -145,63 +150,6 @@ __device__ __forceinline__ bool drain_wait_g(uint32_t bar, uint32_t parity, cons
     return ok;
 }
 
-// ---- thread-block cluster helpers (remote mbarriers, multicast)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
-}
-// TMA 2D load written to the same shared-memory offset in every CTA of the
-// cluster named by `mask`, completing its bytes on the mbarrier at offset
-// `bar` in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0, int32_t c1,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
-        : "memory");
-}
-// Arrive (once the MMAs issued so far complete) on the mbarrier at offset
-// `bar` in every CTA of the cluster named by `mask`.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.b32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// bounded_wait for a barrier that other CTAs of the cluster arrive on
-// (acquire at cluster scope, so their shared-memory writes are visible).
-__device__ __forceinline__ bool bounded_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((i & 31u) == 0) {
-            if (*ctl.abort) return false;
-            if (globaltimer_ns() - t0 > ctl.timeout_ns) {
-                *ctl.abort = 1;
-                atomicOr(ctl.err, DEVERR_WAIT_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
 __device__ __forceinline__ float sigmoid_f32(float v) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-v))); }
 
 // Order-preserving map of fp32 bit patterns to unsigned integers: for
@@ -213,8 +161,22 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return max((u & 0x80000000u) ? ~u : (u | 0x80000000u), 1u);
 }
 
+// Compare-exchange of a lane's candidate slots a < b (static indices, so the
+// lists stay in registers): slot a ends up holding the better candidate,
+// the larger key, or on equal keys the lower slot index (the lower expert).
+__device__ __forceinline__ void cand_cx(uint32_t& ka, int& ja, uint32_t& kb, int& jb) {
+    const bool swap = kb > ka || (kb == ka && jb < ja);
+    const uint32_t tk = swap ? kb : ka;
+    const int tj = swap ? jb : ja;
+    kb = swap ? ka : kb;
+    jb = swap ? ja : jb;
+    ka = tk;
+    ja = tj;
+}
+
 // CS: CTAs per 128-token tile (a thread-block cluster when CS > 1).  Each
-// takes E / CS experts through the K loop and selects for 128 / CS tokens.
+// takes K chunks [rank * kps, (rank + 1) * kps) of the whole tile and
+// selects for 128 / CS tokens.
 template <int CS>
 __global__ void __launch_bounds__(kGateThreads, 1)
     moe_gate_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -231,10 +193,9 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     auto empty_bar = [&](int s) { return bar0 + 8u * (L::ST + s); };
     const uint32_t done_bar = bar0 + 8u * (2 * L::ST);
     const uint32_t step_bar = bar0 + 8u * (2 * L::ST + 1);
-    const uint32_t recv_bar = bar0 + 8u * (2 * L::ST + 2);
     const uint32_t crank = CS > 1 ? cluster_rank() : 0u;
-    const int EN = p.E / CS;                 // this CTA's experts: e0 .. e0 + EN - 1
-    const int e0 = static_cast<int>(crank) * EN;
+    const int kb0 = static_cast<int>(crank) * p.kps;
+    const int nk = max(0, min(p.KB, kb0 + p.kps) - kb0);  // this CTA's K chunks
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
     float* bias_s = reinterpret_cast<float*>(smem + L::OFF_BIAS);
 
@@ -245,15 +206,13 @@ __global__ void __launch_bounds__(kGateThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::ST; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), CS);  // every CTA's MMAs read the stage
+            mbar_init(empty_bar(s), 1);
         }
         mbar_init(done_bar, 2);  // one commit from each MMA warp
         mbar_init(step_bar, kGateEpiWarps);
-        mbar_init(recv_bar, CS * 4);  // the four warps of one lane quarter in every CTA
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if constexpr (CS > 1) cluster_sync_all();  // every CTA's barriers exist before any remote access
     grid_dependency_wait();
     allow_dependents();
     if (warp == 2) tmem_alloc(sbase + L::OFF_TMEM, L::TMEM_COLS);
@@ -271,29 +230,22 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         // on a stage also holds until its own earlier copies have landed, so
         // two producers keep twice the loads in flight.
         const int j = warp;
-        const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + EN * 128);
-        int kb = j;
+        const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + p.E * 128);
+        int c = j;
         if (lane == 0) {
-            for (; kb < p.KB; kb += 2) {
-                const int s = kb % L::ST;
-                if (!bounded_wait(empty_bar(s), ((kb / L::ST) & 1u) ^ 1u, ctl)) break;
+            for (; c < nk; c += 2) {
+                const int s = c % L::ST;
+                if (!bounded_wait(empty_bar(s), ((c / L::ST) & 1u) ^ 1u, ctl)) break;
                 mbar_arrive_expect_tx(full_bar(s), tx);
-                if constexpr (CS == 1) {
-                    tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmX, full_bar(s), kb * kGateK, m0);
-                } else {
-                    // this CTA's 128 / CS rows of the x tile, to every CTA of the cluster
-                    constexpr int RQ = kGateM / CS;
-                    tma_load_2d_mc(sbase + L::OFF_A + s * L::A_BYTES + crank * (RQ * 128), &tmX, full_bar(s),
-                                   kb * kGateK, m0 + static_cast<int>(crank) * RQ, static_cast<uint16_t>((1u << CS) - 1u));
-                }
-                tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmW, full_bar(s), kb * kGateK, e0);
+                tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmX, full_bar(s), (kb0 + c) * kGateK, m0);
+                tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmW, full_bar(s), (kb0 + c) * kGateK, 0);
             }
         }
-        kb = __shfl_sync(0xffffffffu, kb, 0);  // one past this warp's last issued chunk
+        c = __shfl_sync(0xffffffffu, c, 0);  // one past this warp's last issued chunk
         // every issued load must land before the CTA's shared memory goes
         // away: the last use of each of this warp's stages
-        for (int c = j; c < kb; c += 2)
-            if (c + L::ST >= kb) drain_wait_g(full_bar(c % L::ST), (c / L::ST) & 1u, ctl);
+        for (int i = j; i < c; i += 2)
+            if (i + L::ST >= c) drain_wait_g(full_bar(i % L::ST), (i / L::ST) & 1u, ctl);
     } else if (warp <= 3) {
         // ------------------------------------------------------------ MMA issuers
         // Warp 2 takes the even K chunks, warp 3 the odd ones, each into its
@@ -303,22 +255,19 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         // chunk covers the other's wait.
         const int j = warp - 2;
         const uint32_t acc = tmem + static_cast<uint32_t>(j) * L::ACC_COLS;
-        const uint32_t idesc = idesc_bf16_f32(kGateM, EN);
+        const uint32_t idesc = idesc_bf16_f32(kGateM, p.E);
         bool issued = false;
         if (lane == 0) {
-            for (int kb = j; kb < p.KB; kb += 2) {
-                const int s = kb % L::ST;
-                if (!bounded_wait(full_bar(s), (kb / L::ST) & 1u, ctl)) break;
+            for (int c = j; c < nk; c += 2) {
+                const int s = c % L::ST;
+                if (!bounded_wait(full_bar(s), (c / L::ST) & 1u, ctl)) break;
                 tc_fence_after();
                 const uint64_t adesc = sdesc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
                 const uint64_t bdesc = sdesc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)  // K 16 = 32 bytes = +2 in the address field
-                    umma_bf16(acc, adesc + 2u * k, bdesc + 2u * k, idesc, (kb > 1 || k > 0) ? 1u : 0u);
-                if constexpr (CS == 1)
-                    umma_commit(empty_bar(s));
-                else  // the stage's x rows came from every CTA: release it in all of them
-                    umma_commit_mc(empty_bar(s), static_cast<uint16_t>((1u << CS) - 1u));
+                    umma_bf16(acc, adesc + 2u * k, bdesc + 2u * k, idesc, (c > 1 || k > 0) ? 1u : 0u);
+                umma_commit(empty_bar(s));
                 issued = true;
             }
             // Publish the sums (also after a wait that gave up: the status
@@ -332,51 +281,75 @@ __global__ void __launch_bounds__(kGateThreads, 1)
         const int ew = warp - kGateEpiWarp0;
         const int quarter = warp & 3;         // TMEM lane quarter this warp may read
         const int sl = ew >> 2;               // which of the four warps of the quarter
+        const int row = quarter * 32 + lane;  // this thread's token (TMEM lane) in the tile
         const uint32_t taddr0 = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        float* S = reinterpret_cast<float*>(smem + L::OFF_SEL);  // [NT][kGateSelStride]
+        float* S = reinterpret_cast<float*>(smem + L::OFF_SEL);  // [NT][kGateRowStride]
         bool ok = warp_wait(done_bar, 0, ctl);
         tc_fence_after();
-        if constexpr (CS == 1) {
-            // the stages were last written by TMA (async proxy); the table
-            // overwrites them with ordinary stores
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        }
-        // 1. affinities, token-major, into the selecting CTA's table: this
-        //    warp's 16-column units sl, sl + 4, ... of the EN columns
+        // the stages were last written by TMA (async proxy); the tables
+        // overwrite them with ordinary stores
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // 1. the sums of this warp's 16-column units sl, sl + 4, ...: the
+        //    affinities (one CTA) or the partial logits (cluster)
         if (ok) {
-            const int row = CS == 1 ? quarter * 32 + lane : lane;
-            const uint32_t dst = CS == 1 ? sbase + L::OFF_SEL : mapa_rank(sbase + L::OFF_SEL, quarter);
-            for (int u = sl; u < EN / 16; u += 4) {
+            float* dst = reinterpret_cast<float*>(smem + (CS == 1 ? L::OFF_SEL : L::OFF_PART)) + row * kGateRowStride;
+            for (int u = sl; u < p.E / 16; u += 4) {
                 uint64_t pr[8], po[8];
-                tmem_ld_x16_pairs(taddr0 + 16 * u, pr);
-                if (p.KB > 1) {  // logit = even-chunk sum + odd-chunk sum
-                    tmem_ld_x16_pairs(taddr0 + L::ACC_COLS + 16 * u, po);
+                if (nk > 0) {
+                    tmem_ld_x16_pairs(taddr0 + 16 * u, pr);
+                    if (nk > 1) {  // even-chunk sum + odd-chunk sum
+                        tmem_ld_x16_pairs(taddr0 + L::ACC_COLS + 16 * u, po);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) pr[i] = f2_add(pr[i], po[i]);
+                        for (int i = 0; i < 8; ++i) pr[i] = f2_add(pr[i], po[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) pr[i] = 0;  // no chunks in this K slice
                 }
-                float sv[16];
+                float v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) sv[i] = sigmoid_f32((i & 1) ? hi_f32(pr[i >> 1]) : lo_f32(pr[i >> 1]));
-                const uint32_t at = dst + static_cast<uint32_t>((row * kGateSelStride + e0 + 16 * u) * 4);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if constexpr (CS == 1)
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(at + 16u * c),
-                                     "f"(sv[4 * c]), "f"(sv[4 * c + 1]), "f"(sv[4 * c + 2]), "f"(sv[4 * c + 3])
-                                     : "memory");
-                    else
-                        st_cluster_v4(at + 16u * c, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
+                for (int i = 0; i < 16; ++i) {
+                    const float l = (i & 1) ? hi_f32(pr[i >> 1]) : lo_f32(pr[i >> 1]);
+                    v[i] = CS == 1 ? sigmoid_f32(l) : l;
                 }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<float4*>(dst + 16 * u + 4 * q) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+        }
+        if constexpr (CS > 1) {
+            // every CTA's partial logits are complete and visible (the other
+            // warps reach the same barrier after their loops)
+            asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                             "memory");
+            // rank crank's tokens: the CS partials added in rank order, four
+            // experts at a time, every peer's load in flight together
+            const uint32_t part0 = sbase + L::OFF_PART;
+            const int groups = p.E / 4;
+            const int items = L::NT * groups;
+            for (int it = ew * 32 + lane; it < items; it += 32 * kGateEpiWarps) {
+                const int t = it / groups, g = it % groups;
+                const uint32_t off =
+                    static_cast<uint32_t>(((static_cast<int>(crank) * L::NT + t) * kGateRowStride + 4 * g) * 4);
+                float4 pv[CS];
+#pragma unroll
+                for (int q = 0; q < CS; ++q) pv[q] = ld_cluster_v4f32(mapa_rank(part0 + off, static_cast<uint32_t>(q)));
+                float4 sum = pv[0];
+#pragma unroll
+                for (int q = 1; q < CS; ++q) {
+                    sum.x = __fadd_rn(sum.x, pv[q].x);
+                    sum.y = __fadd_rn(sum.y, pv[q].y);
+                    sum.z = __fadd_rn(sum.z, pv[q].z);
+                    sum.w = __fadd_rn(sum.w, pv[q].w);
+                }
+                *reinterpret_cast<float4*>(S + t * kGateRowStride + 4 * g) =
+                    make_float4(sigmoid_f32(sum.x), sigmoid_f32(sum.y), sigmoid_f32(sum.z), sigmoid_f32(sum.w));
             }
         }
         __syncwarp();
-        if constexpr (CS == 1) {
-            if (lane == 0) mbar_arrive(step_bar);
-            ok = warp_wait(step_bar, 0, ctl) && ok;
-        } else {
-            if (lane == 0) mbar_arrive_cluster(mapa_rank(recv_bar, quarter));
-            ok = __all_sync(0xffffffffu, bounded_wait_cluster(recv_bar, 0, ctl)) && ok;
-        }
+        if (lane == 0) mbar_arrive(step_bar);
+        ok = warp_wait(step_bar, 0, ctl) && ok;
         // 2. selection, one warp per token; lane l holds experts l + 32 j
         if (ok) {
             const int J = (p.E + 31) / 32;
@@ -392,7 +365,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             }
             const int tok0 = m0 + static_cast<int>(crank) * L::NT;
             for (int t = ew; t < L::NT && tok0 + t < p.T; t += kGateEpiWarps) {
-                const float* St = S + t * kGateSelStride;
+                const float* St = S + t * kGateRowStride;
                 uint32_t ck[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -427,28 +400,36 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                 }
                 const uint32_t keep = __ballot_sync(0xffffffffu, lane < p.n_groups && better < p.topk_groups);
                 __syncwarp();
+                // this lane's kept candidates sorted best first (Batcher's
+                // odd-even merge network for 8; ties to the lower slot)
+                int cj[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < 8; ++j) {
                     if (grp[j] < 0 || !((keep >> grp[j]) & 1u)) ck[j] = 0u;
-                // top_k rounds of arg-max (largest key, then lowest expert)
+                    cj[j] = j;
+                }
+#define GATE_CX(a, b) cand_cx(ck[a], cj[a], ck[b], cj[b])
+                GATE_CX(0, 1); GATE_CX(2, 3); GATE_CX(4, 5); GATE_CX(6, 7);
+                GATE_CX(0, 2); GATE_CX(1, 3); GATE_CX(4, 6); GATE_CX(5, 7);
+                GATE_CX(1, 2); GATE_CX(5, 6);
+                GATE_CX(0, 4); GATE_CX(1, 5); GATE_CX(2, 6); GATE_CX(3, 7);
+                GATE_CX(2, 4); GATE_CX(3, 5);
+                GATE_CX(1, 2); GATE_CX(3, 4); GATE_CX(5, 6);
+#undef GATE_CX
+                // top_k rounds: the warp's best head (largest key, then the
+                // lowest expert); the winning lane moves to its next candidate
                 int my_id = -1;
                 for (int r = 0; r < p.top_k; ++r) {
-                    uint32_t bk = 0;
-                    int bj = 0;
+                    const uint32_t mk = __reduce_max_sync(0xffffffffu, ck[0]);
+                    const uint32_t me = static_cast<uint32_t>(32 * cj[0] + lane);
+                    const uint32_t win = __reduce_min_sync(0xffffffffu, (ck[0] == mk && mk != 0u) ? me : 0xffffffffu);
+                    if (win == me) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (ck[j] > bk) {
-                            bk = ck[j];
-                            bj = j;
+                        for (int j = 0; j < 7; ++j) {
+                            ck[j] = ck[j + 1];
+                            cj[j] = cj[j + 1];
                         }
-                    }
-                    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-                    const uint32_t cand = (bk == mk && bk != 0u) ? static_cast<uint32_t>(32 * bj + lane) : 0xffffffffu;
-                    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-                    if (win == static_cast<uint32_t>(32 * bj + lane)) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (j == bj) ck[j] = 0u;
+                        ck[7] = 0u;
                     }
                     if (lane == r) my_id = static_cast<int>(win);
                 }
@@ -464,13 +445,19 @@ __global__ void __launch_bounds__(kGateThreads, 1)
             }
         }
     }
+    if constexpr (CS > 1) {
+        // the producer and MMA warps meet the epilogue's cluster barrier
+        if (warp < kGateEpiWarp0)
+            asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                             "memory");
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, L::TMEM_COLS);
     }
-    if constexpr (CS > 1) cluster_sync_all();
+    if constexpr (CS > 1) cluster_sync_all();  // no CTA leaves while a peer may still read its partial logits
 }
 
 // ------------------------------------------------------------------ routing tables
@@ -693,13 +680,15 @@ __global__ void __launch_bounds__(kRouteThreads)
 cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, const float* bias, int64_t T,
                             int64_t dim, int E, int n_groups, int topk_groups, int top_k, float route_scale,
                             int32_t* ids, float* w, const DeviceInfo& dev, cudaStream_t stream) {
-    // Clusters of four CTAs per 128-token tile (a quarter of the experts
-    // each, a multiple of 16 columns) when E allows, else one CTA per tile.
-    const int cs = (E % 64 == 0) ? 4 : 1;
+    // Clusters of four CTAs per 128-token tile (a quarter of K each) while
+    // the tiles fill at most two waves of the SMs that way; beyond that one
+    // CTA per tile already fills the GPU without the partial-logit exchange.
+    const int tiles = static_cast<int>((T + kGateM - 1) / kGateM);
+    const int cs = (static_cast<int64_t>(tiles) * 4 <= 2 * static_cast<int64_t>(dev.num_sms)) ? 4 : 1;
     CUtensorMap tmX, tmW;
     cudaError_t e;
-    if ((e = make_tmap_2d(&tmX, x, 2, dim, T, ldx * 2, kGateK, kGateM / cs, 128)) != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&tmW, wg, 2, dim, E, dim * 2, kGateK, E / cs, 128)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&tmX, x, 2, dim, T, ldx * 2, kGateK, kGateM, 128)) != cudaSuccess) return e;
+    if ((e = make_tmap_2d(&tmW, wg, 2, dim, E, dim * 2, kGateK, E, 128)) != cudaSuccess) return e;
     {
         static bool ready[64];
         if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
@@ -719,6 +708,7 @@ cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, 
     p.w = w;
     p.T = static_cast<int>(T);
     p.KB = static_cast<int>(dim / kGateK);
+    p.kps = (p.KB + cs - 1) / cs;
     p.E = E;
     p.n_groups = n_groups;
     p.topk_groups = topk_groups;
@@ -726,7 +716,6 @@ cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, 
     p.route_scale = route_scale;
     p.err = dev.err;
     p.timeout_ns = wait_timeout_ns();
-    const int tiles = static_cast<int>((T + kGateM - 1) / kGateM);
     if (cs == 1)
         return launch_pdl(moe_gate_kernel<1>, dim3(tiles), dim3(kGateThreads), GateLayout<1>::ALLOC, stream, tmX, tmW, p);
     cudaLaunchAttribute attr[1];

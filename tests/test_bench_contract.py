@@ -34,9 +34,14 @@ def test_traffic_table_lookup():
     import bench
     sha = bench.kernel_sources_sha()
     assert len(sha) == 16
-    t = bench.ncu_traffic("fp8_gemm", "kv_down")
-    # the committed capture holds for the committed sources, else the bench reports null
+    # every committed capture is reported while the sources match it, else null
     with open(os.path.join(ROOT, "profiles", "dram_traffic.txt")) as f:
-        captured = any(f"src_sha={sha}" in line for line in f)
-    assert (t is not None) == captured
+        entries = [dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+                   for line in f if line.strip() and not line.startswith("#")]
+    assert entries
+    for kv in entries:
+        t = bench.ncu_traffic(kv["kernel"], kv["workload"])
+        assert (t is not None) == (kv["src_sha"] == sha)
+        if t is not None:
+            assert t == float(kv["dram_bytes_per_launch"])
     assert bench.ncu_traffic("no_such_kernel", "kv_down") is None

@@ -87,8 +87,9 @@ def _check_gate(ids_g, w_g, x, wg, bias, s_o, ids_o, n_groups, topk_groups, top_
     (300, 512, 256, 8, 4, 8, 0.075),     # DeepSeek-V3's routing shape at a reduced width, ragged tokens
     (130, 128, 64, 16, 3, 5, 0.15),      # groups of 4 experts: a 16-column slice spans several groups
     (5, 64, 16, 1, 1, 1, 0.2),           # one group, top-1, one K chunk
-    (200, 192, 96, 3, 2, 4, 0.15),       # one CTA per tile (E not a multiple of 64), groups of 32
-    (77, 128, 80, 5, 3, 7, 0.15),        # one CTA per tile, groups of 16
+    (200, 192, 96, 3, 2, 4, 0.15),       # six 16-column units (E not a multiple of 64), groups of 32
+    (77, 128, 80, 5, 3, 7, 0.15),        # five units, groups of 16, K of 2 chunks over 4 CTAs
+    (9600, 128, 64, 4, 2, 6, 0.15),      # 75 tiles: more than two waves as clusters, so one CTA per tile
 ])
 def test_gate_vs_oracle(F, orc, T, dim, E, n_groups, topk_groups, top_k, std):
     rng = np.random.default_rng(T + E)
