@@ -64,7 +64,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="large_square",
-                    help="large_square | kv_down | tiny | q_down_m<M>[_fused] | moe | moe_swiglu | moe_layer | moe_router | "
+                    help="large_square | kv_down | tiny | q_down_m<M>[_fused] | moe | moe_e<G> | moe_swiglu | moe_layer | moe_router | "
                          "kv_down_wgrad | large_square_wgrad | q_down_m<M>_wgrad")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -340,12 +340,12 @@ class MoEWork:
     swiglu: the grouped GEMM is the expert first stage with w1 and w3 and the
     SwiGLU activation fused (h = silu(x w1^T) * (x w3^T))."""
 
-    def __init__(self, device, swiglu=False):
+    def __init__(self, device, swiglu=False, experts=None):
         import torch
         from fp8_block_scaled_18_b300 import fp8bs as F
         from fp8_block_scaled_18_b300 import synth
         self.F = F
-        case = synth.moe()
+        case = synth.moe() if experts is None else moe_small_case(experts)
         self.case = case
         G, N, K = case.n_experts, case.n, case.k
         self.G, self.N, self.K = G, N, K
@@ -440,14 +440,16 @@ class MoEWork:
 
     def config(self):
         if self.swiglu:
-            return {"workload": "moe_swiglu", "tokens": 4096, "experts": self.G, "top_k": 8, "rows": self.T,
+            return {"workload": "moe_swiglu", "tokens": self.T // 8, "experts": self.G, "top_k": 8, "rows": self.T,
                     "I": self.N, "K": self.K,
                     "step": "act_quant+grouped w1|w3 fp8_gemm with SwiGLU, h out as FP8 (expert weights "
                             "pre-quantised)",
                     "l2": "working set (7.5 GB of expert weights) larger than the 126 MB L2"}
-        return {"workload": "moe_grouped", "tokens": 4096, "experts": self.G, "top_k": 8, "rows": self.T,
+        wgb = self.G * self.N * self.K / 1e9
+        return {"workload": "moe_grouped" if self.G == 256 else f"moe_e{self.G}", "tokens": self.T // 8,
+                "experts": self.G, "top_k": 8, "rows": self.T,
                 "N": self.N, "K": self.K, "step": "act_quant+grouped_fp8_gemm (expert weights pre-quantised)",
-                "l2": "working set (3.76 GB of expert weights) larger than the 126 MB L2"}
+                "l2": f"working set ({wgb:.2f} GB of expert weights) larger than the 126 MB L2"}
 
 
 class MoELayerWork:
@@ -721,12 +723,21 @@ class RouterWork:
                 "l2": "inputs (59 MB) re-read each step from L2: the router is latency-bound, not HBM-bound"}
 
 
+def moe_small_case(experts: int):
+    """The MoE grouped configuration over fewer experts with the same rows
+    per expert (4096 tokens x top-8 over 256 experts: about 128 each)."""
+    from fp8_block_scaled_18_b300 import synth
+    return synth.moe(tokens=max(64, 4096 * experts // 256), n_experts=experts)
+
+
 def make_work(name: str, device):
     from fp8_block_scaled_18_b300 import synth
     if name == "moe":
         return MoEWork(device)
     if name == "moe_swiglu":
         return MoEWork(device, swiglu=True)
+    if name.startswith("moe_e"):  # the grouped GEMM over fewer experts (a capture-sized case)
+        return MoEWork(device, experts=int(name[len("moe_e"):]))
     if name == "moe_layer":
         return MoELayerWork(device)
     if name == "moe_router":
@@ -1198,9 +1209,9 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
         dt = time.perf_counter() - t0
         sample = (f"{n} experts x <=32 rows: weight_quant of the expert's w1, w3 and w2, router, act_quant, gemm x2, "
                   f"silu(a) * b, act_quant(h), gemm (w2), gated combine; TFLOP/s over the sampled GEMM work")
-    elif workload in ("moe", "moe_swiglu"):
+    elif workload in ("moe", "moe_swiglu") or workload.startswith("moe_e"):
         swiglu = workload == "moe_swiglu"
-        case = synth.moe()
+        case = moe_small_case(int(workload[len("moe_e"):])) if workload.startswith("moe_e") else synth.moe()
         counts = np.diff(case.offsets)
         x_rows = case.x_rows
         experts = np.nonzero(counts)[0]
@@ -1306,9 +1317,9 @@ def run_reference(args, rank, local, world):
                   f"{rows} of its rows through the router, act_quant, w1/w3 gemm, silu * b, act_quant(h), w2 gemm, "
                   f"combine")
         cfg = {"workload": "moe_layer"}
-    elif args.workload in ("moe", "moe_swiglu"):
+    elif args.workload in ("moe", "moe_swiglu") or args.workload.startswith("moe_e"):
         import torch
-        case = synth.moe()
+        case = moe_small_case(int(args.workload[len("moe_e"):])) if args.workload.startswith("moe_e") else synth.moe()
         counts = np.diff(case.offsets)
         x_rows = case.x_rows
         g = int(np.argmax(counts))  # the busiest expert
