@@ -107,6 +107,27 @@ def test_gemm_few_tokens(F, orc, M, N, K):
     assert np.array_equal(y1, y2)
 
 
+@pytest.mark.parametrize("M,N,K", [(5, 300, 1024), (128, 200, 512)])
+def test_gemm_strided_output(F, orc, M, N, K):
+    """y as a column slice of a wider buffer (ldy > N): every element of the
+    slice against the oracle, the columns outside it untouched.  Both shapes
+    take the few-token kernel, whose reduction stores the output itself."""
+    rng = np.random.default_rng(M + N)
+    x = synth.activations(rng, M, K, n_outlier=2, outlier_scale=25.0)
+    w = synth.normal_bf16(rng, (N, K), 0.02)
+    xq, sx = orc.act_quant(x, lds=max(4, (K // 128 + 3) // 4 * 4))
+    wq, sw = orc.weight_quant(w)
+    ld = (N + 72 + 7) // 8 * 8  # the row stride must be a multiple of 8 elements
+    big = torch.full((M, ld), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = big[:, 40:40 + N]  # 80 bytes in: 16-byte aligned
+    F.fp8bs_gemm(dev(xq), dev(sx), dev(wq), dev(sw), y=y)
+    assert F.fp8bs_sync_status() == 0
+    y_ref, L = orc.gemm(xq, sx, wq, sw)
+    assert_gemm_close(host(y.contiguous()), y_ref, L, f"strided y {M}x{N}x{K}")
+    rest = torch.cat([big[:, :40], big[:, 40 + N:]], dim=1)
+    assert bool((rest == 7.0).all())
+
+
 @pytest.mark.parametrize("M", [1, 16, 64, 96])
 def test_gemm_decode_split_k_matches_unsplit(F, orc, M):
     """q_down (K = 7168): M <= 64 runs the weight-streaming kernel with or
