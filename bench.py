@@ -800,7 +800,7 @@ def chunked_graphs(fn, total: int, chunk: int = 200):
 
 def kernel_row(work, k, per_call_s, peaks):
     """Per-kernel roofline row.  A tensor-bound kernel's roofline time is
-    max(FLOP / FP8 peak, bytes / HBM peak) (SURVEY's per-GEMM roofline), so
+    max(FLOP / FP8 peak, bytes / HBM peak) (a GEMM's roofline is whichever is slower), so
     small-M GEMMs are held to the weight read; HBM-bound kernels to their
     algorithmic bytes.  frac = roofline time / measured time, against the
     burst peaks; frac_sustained against the sustained tensor peak."""
