@@ -120,6 +120,11 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    // launched with programmatic stream serialisation: the set-up above ran
+    // while the kernel before may still be finishing; every global read
+    // (operands, scales) and the TMEM allocation come after this wait
+    grid_dependency_wait();
+    allow_dependents();
     __syncthreads();
     if (warp == 0 && lane == 0) {
         // every chunk of the slice at once, one stage each
@@ -315,18 +320,20 @@ cudaError_t launch_gemm_skinny(const GemmArgs& a, const DeviceInfo& dev, cudaStr
     if ((e = make_tmap_2d(&tmW, a.wq, 1, a.K, a.N, a.K, kSkBK, kSkRows, 128)) != cudaSuccess) return e;
     if ((e = make_tmap_2d(&tmX, a.xq, 1, a.K, a.M, a.K, kSkBK, p.NP, 128)) != cudaSuccess) return e;
     const int tiles = static_cast<int>((a.N + kSkRows - 1) / kSkRows);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(p.S);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles * p.S));
     cfg.blockDim = dim3(kSkThreads);
     cfg.dynamicSmemBytes = SkLayout::ALLOC;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, fp8_gemm_skinny_kernel, tmW, tmX, p);
 }
 
