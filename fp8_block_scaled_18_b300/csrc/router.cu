@@ -718,18 +718,20 @@ cudaError_t launch_moe_gate(const uint16_t* x, int64_t ldx, const uint16_t* wg, 
     p.timeout_ns = wait_timeout_ns();
     if (cs == 1)
         return launch_pdl(moe_gate_kernel<1>, dim3(tiles), dim3(kGateThreads), GateLayout<1>::ALLOC, stream, tmX, tmW, p);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 4;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(4 * tiles);
     cfg.blockDim = dim3(kGateThreads);
     cfg.dynamicSmemBytes = GateLayout<4>::ALLOC;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, moe_gate_kernel<4>, tmX, tmW, p);
 }
 
@@ -747,18 +749,20 @@ cudaError_t launch_moe_route(const int32_t* ids, const float* w, int64_t T, int 
     // one cluster; chunks of ceil(T / kRouteCtas) tokens (T == 0: the CTAs
     // still write the all-zero offsets)
     const int chunk = static_cast<int>(std::max<int64_t>(1, (T + kRouteCtas - 1) / kRouteCtas));
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kRouteCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kRouteCtas);
     cfg.blockDim = dim3(kRouteThreads);
     cfg.dynamicSmemBytes = sizeof(RouteSmem);
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, moe_route_kernel, ids, w, static_cast<int>(T), top_k, E, chunk, offsets,
                               token_of_row, rows_of_token, weight_of_row, dev.err);
 }
