@@ -400,38 +400,81 @@ __global__ void __launch_bounds__(kGateThreads, 1)
                 }
                 const uint32_t keep = __ballot_sync(0xffffffffu, lane < p.n_groups && better < p.topk_groups);
                 __syncwarp();
-                // this lane's kept candidates sorted best first (Batcher's
-                // odd-even merge network for 8; ties to the lower slot)
-                int cj[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (grp[j] < 0 || !((keep >> grp[j]) & 1u)) ck[j] = 0u;
-                    cj[j] = j;
-                }
-#define GATE_CX(a, b) cand_cx(ck[a], cj[a], ck[b], cj[b])
-                GATE_CX(0, 1); GATE_CX(2, 3); GATE_CX(4, 5); GATE_CX(6, 7);
-                GATE_CX(0, 2); GATE_CX(1, 3); GATE_CX(4, 6); GATE_CX(5, 7);
-                GATE_CX(1, 2); GATE_CX(5, 6);
-                GATE_CX(0, 4); GATE_CX(1, 5); GATE_CX(2, 6); GATE_CX(3, 7);
-                GATE_CX(2, 4); GATE_CX(3, 5);
-                GATE_CX(1, 2); GATE_CX(3, 4); GATE_CX(5, 6);
-#undef GATE_CX
-                // top_k rounds: the warp's best head (largest key, then the
-                // lowest expert); the winning lane moves to its next candidate
                 int my_id = -1;
-                for (int r = 0; r < p.top_k; ++r) {
-                    const uint32_t mk = __reduce_max_sync(0xffffffffu, ck[0]);
-                    const uint32_t me = static_cast<uint32_t>(32 * cj[0] + lane);
-                    const uint32_t win = __reduce_min_sync(0xffffffffu, (ck[0] == mk && mk != 0u) ? me : 0xffffffffu);
-                    if (win == me) {
+                if (per == 32 && p.topk_groups <= 4) {
+                    // Groups of 32: this lane holds one expert of each group, so at
+                    // most four candidates, reloaded from the table in group order
+                    // and sorted with five compare-exchanges (the selection is
+                    // bound by the integer pipe: fewer candidates, fewer selects).
+                    uint32_t kk = keep;
+                    uint32_t c4[4];
+                    int j4[4];
 #pragma unroll
-                        for (int j = 0; j < 7; ++j) {
-                            ck[j] = ck[j + 1];
-                            cj[j] = cj[j + 1];
+                    for (int i = 0; i < 4; ++i) {
+                        if (kk != 0u) {
+                            const int g = __ffs(kk) - 1;
+                            kk &= kk - 1u;
+                            c4[i] = order_key(__fadd_rn(St[32 * g + lane], bias_s[32 * g + lane]));
+                            j4[i] = g;
+                        } else {
+                            c4[i] = 0u;
+                            j4[i] = 8 + i;
                         }
-                        ck[7] = 0u;
                     }
-                    if (lane == r) my_id = static_cast<int>(win);
+                    cand_cx(c4[0], j4[0], c4[1], j4[1]);
+                    cand_cx(c4[2], j4[2], c4[3], j4[3]);
+                    cand_cx(c4[0], j4[0], c4[2], j4[2]);
+                    cand_cx(c4[1], j4[1], c4[3], j4[3]);
+                    cand_cx(c4[1], j4[1], c4[2], j4[2]);
+                    for (int r = 0; r < p.top_k; ++r) {
+                        const uint32_t mk = __reduce_max_sync(0xffffffffu, c4[0]);
+                        const uint32_t me = static_cast<uint32_t>(32 * j4[0] + lane);
+                        const uint32_t win =
+                            __reduce_min_sync(0xffffffffu, (c4[0] == mk && mk != 0u) ? me : 0xffffffffu);
+                        if (win == me) {
+                            c4[0] = c4[1];
+                            j4[0] = j4[1];
+                            c4[1] = c4[2];
+                            j4[1] = j4[2];
+                            c4[2] = c4[3];
+                            j4[2] = j4[3];
+                            c4[3] = 0u;
+                        }
+                        if (lane == r) my_id = static_cast<int>(win);
+                    }
+                } else {
+                    // this lane's kept candidates sorted best first (Batcher's
+                    // odd-even merge network for 8; ties to the lower slot)
+                    int cj[8];
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (grp[j] < 0 || !((keep >> grp[j]) & 1u)) ck[j] = 0u;
+                        cj[j] = j;
+                    }
+    #define GATE_CX(a, b) cand_cx(ck[a], cj[a], ck[b], cj[b])
+                    GATE_CX(0, 1); GATE_CX(2, 3); GATE_CX(4, 5); GATE_CX(6, 7);
+                    GATE_CX(0, 2); GATE_CX(1, 3); GATE_CX(4, 6); GATE_CX(5, 7);
+                    GATE_CX(1, 2); GATE_CX(5, 6);
+                    GATE_CX(0, 4); GATE_CX(1, 5); GATE_CX(2, 6); GATE_CX(3, 7);
+                    GATE_CX(2, 4); GATE_CX(3, 5);
+                    GATE_CX(1, 2); GATE_CX(3, 4); GATE_CX(5, 6);
+    #undef GATE_CX
+                    // top_k rounds: the warp's best head (largest key, then the
+                    // lowest expert); the winning lane moves to its next candidate
+                    for (int r = 0; r < p.top_k; ++r) {
+                        const uint32_t mk = __reduce_max_sync(0xffffffffu, ck[0]);
+                        const uint32_t me = static_cast<uint32_t>(32 * cj[0] + lane);
+                        const uint32_t win = __reduce_min_sync(0xffffffffu, (ck[0] == mk && mk != 0u) ? me : 0xffffffffu);
+                        if (win == me) {
+    #pragma unroll
+                            for (int j = 0; j < 7; ++j) {
+                                ck[j] = ck[j + 1];
+                                cj[j] = cj[j + 1];
+                            }
+                            ck[7] = 0u;
+                        }
+                        if (lane == r) my_id = static_cast<int>(win);
+                    }
                 }
                 // gate values: the chosen affinities normalised in rank order
                 const float sr = (lane < p.top_k && my_id >= 0 && my_id < p.E) ? St[my_id] : 0.0f;
