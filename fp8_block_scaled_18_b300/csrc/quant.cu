@@ -236,89 +236,176 @@ __global__ void wait_selftest_kernel(unsigned* err, uint64_t timeout_ns) {
 // for each column k and each block of 128 rows, amax over the block's valid
 // rows, s = amax / 448, and the codes written transposed, xqt[k, m], so that
 // each output row holds one channel's tokens contiguously (the layout the
-// weight-gradient GEMM contracts over).  A CTA takes tiles of 128 rows x 64
-// columns: the tile is read with 16-byte loads into shared memory, then
-// thread (c, g) takes column c and rows 32g .. 32g+31, reduces their amax,
-// combines the four partial amaxes of its column through shared memory,
-// encodes its 32 values with the act_quant arithmetic and stores its 32
-// codes -- contiguous in the transposed output -- as two 16-byte stores.
+// weight-gradient GEMM contracts over).
+//
+// A CTA walks tiles of 128 rows x 64 columns (16 KB of bf16) through a
+// three-stage shared-memory ring filled with cp.async (16-byte copies; rows
+// past M are zero-filled, so they never raise the amax): two tiles are in
+// flight while a third is encoded.  Thread (cq, g) takes columns
+// 4cq .. 4cq+3 and rows 8g .. 8g+7: eight 8-byte shared loads bring its 32
+// values, byte permutes regroup them by column, each column's partial amax
+// is combined with the warp's other row group by one shuffle and left in
+// shared memory; one thread per column then finishes the amax over the
+// eight warps and forms the scale once, and every thread encodes its
+// columns' eight values with the act_quant codec.  The codes go to a 64 x 128-byte staging tile, one row per output
+// channel, its 16-byte chunks XOR-swizzled by the writer's column group so
+// that the 8-byte writes meet no bank conflict, and leave as whole 128-byte
+// rows of xqt.
 constexpr int kCqRows = 128;
 constexpr int kCqCols = 64;
+constexpr int kCqStages = 3;
+constexpr int kCqTileBytes = kCqRows * kCqCols * 2;        // 16 KB of bf16
+constexpr int kCqOutOff = kCqStages * kCqTileBytes;         // staging: 64 channels x 128 codes
+constexpr int kCqPamOff = kCqOutOff + kCqCols * kCqRows;    // per-warp column amaxes: 8 x 64 x 4 B
+constexpr int kCqGsOff = kCqPamOff + 8 * kCqCols * 4;     // per column: s, 1/s (f32), flags (u8)
+constexpr int kCqSmem = kCqGsOff + kCqCols * 9;
 
-__global__ void __launch_bounds__(256) act_quant_cols_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
-                                                            int64_t ldx, uint8_t* __restrict__ xqt, int64_t ldt,
-                                                            float* __restrict__ sc, int64_t ldsc) {
-    __shared__ __align__(16) uint16_t tile[kCqRows][kCqCols];
-    __shared__ uint32_t pam[4][kCqCols];
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(256, 3) act_quant_cols_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                               int64_t ldx, uint8_t* __restrict__ xqt, int64_t ldt,
+                                                               float* __restrict__ sc, int64_t ldsc) {
+    extern __shared__ __align__(128) uint8_t cq_smem[];
     grid_dependency_wait();  // the previous kernel may still read xqt / sc
     allow_dependents();
     const int t = threadIdx.x;
-    const int c = t % kCqCols;   // column within the tile
-    const int g = t / kCqCols;   // row group of 32
+    const int lane = t & 31, w = t >> 5;
+    const int cq = t & 15;  // columns 4cq .. 4cq+3 of the tile
+    const int g = t >> 4;   // rows 8g .. 8g+7 of the tile
     const int64_t MB = (M + kCqRows - 1) / kCqRows;
     const int64_t CB = K / kCqCols;
-    // the tile's 128 rows x 128 bytes: four 16-byte chunks per thread, eight
-    // threads per row; rows past M read as zeros (they never raise the amax)
-    auto load_tile = [&](int64_t tt, uint4 (&v)[4]) {
-        const int64_t mb = tt / CB;
-        const int64_t k0 = (tt - mb * CB) * kCqCols;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = t + 256 * i;
-            const int r = q / 8, ch = q % 8;
-            v[i] = make_uint4(0, 0, 0, 0);
-            if (tt < MB * CB && mb * kCqRows + r < M) v[i] = ld_stream(x + (mb * kCqRows + r) * ldx + k0 + ch * 8);
+    const int64_t G = gridDim.x;
+    const uint32_t sbase = smem_u32(cq_smem);
+    uint8_t* const stg = cq_smem + kCqOutOff;
+    uint32_t* const pam = reinterpret_cast<uint32_t*>(cq_smem + kCqPamOff);
+    float* const gs_s = reinterpret_cast<float*>(cq_smem + kCqGsOff);
+    float* const gs_r = gs_s + kCqCols;
+    uint8_t* const gs_f = reinterpret_cast<uint8_t*>(gs_r + kCqCols);  // bit 0: exact division, bit 1: amax 0
+    // tile tt = mb * CB + cb; this CTA's tiles are blockIdx.x + j G, stepped
+    // without a division: G = dq CB + dr
+    struct TilePos {
+        int64_t mb, cb;
+    };
+    const int64_t dq = G / CB, dr = G - (G / CB) * CB;
+    auto advance = [&](TilePos& q) {
+        q.cb += dr;
+        q.mb += dq;
+        if (q.cb >= CB) {
+            q.cb -= CB;
+            ++q.mb;
         }
     };
-    uint4 pre[4];
-    load_tile(blockIdx.x, pre);
-    for (int64_t tt = blockIdx.x; tt < MB * CB; tt += gridDim.x) {
-        const int64_t mb = tt / CB;
-        const int64_t k0 = (tt - mb * CB) * kCqCols;
-        const int64_t m0 = mb * kCqRows;
-        __syncthreads();  // the previous tile's reads of `tile` and `pam` are done
+
+    // one tile's copies into stage st: 128 rows x 8 chunks of 16 bytes, four
+    // per thread; a group is committed even when there is no tile, so that
+    // the group count stays in step with the tiles
+    auto issue = [&](const TilePos& q4, int st) {
+        if (q4.mb < MB) {
+            const int64_t mb = q4.mb;
+            const int64_t k0 = q4.cb * kCqCols;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = t + 256 * i;
-            *reinterpret_cast<uint4*>(&tile[q / 8][(q % 8) * 8]) = pre[i];
+            for (int i = 0; i < 4; ++i) {
+                const int q = t + 256 * i;
+                const int r = q >> 3, ch = q & 7;
+                const int64_t row = mb * kCqRows + r;
+                const bool ok = row < M;
+                cp_async16(sbase + st * kCqTileBytes + r * 128 + ch * 16, ok ? x + row * ldx + k0 + ch * 8 : x,
+                           ok ? 16u : 0u);
+            }
         }
-        load_tile(tt + gridDim.x, pre);  // the next tile's loads run during this tile's work
-        __syncthreads();
-        uint4 v[4];  // rows 32g + 8j .. +7 of column c, as 8 bf16 values each
+        cp_async_commit();
+    };
+    TilePos cur{static_cast<int64_t>(blockIdx.x) / CB, static_cast<int64_t>(blockIdx.x) % CB};
+    TilePos pre = cur;
+    advance(pre);
+    issue(cur, 0);
+    issue(pre, 1);
+    advance(pre);  // two tiles ahead of cur from here on
+    int st = 0;    // stage of the current tile; this CTA's j-th tile sits in stage j % 3
+    for (; cur.mb < MB; advance(cur), advance(pre)) {
+        const int64_t mb = cur.mb;
+        const int64_t k0 = cur.cb * kCqCols;
+        const int64_t m0 = mb * kCqRows;
+        cp_async_wait<1>();  // this thread's copies of the current tile have landed
+        __syncthreads();     // and everyone's; the previous tile's shared reads are over
+        issue(pre, st == 0 ? 2 : st - 1);  // into the stage the previous tile used
+
+        const uint8_t* tile = cq_smem + st * kCqTileBytes;
+        uint2 v[8];  // row 8g + r, columns 4cq .. 4cq+3
+#pragma unroll
+        for (int r = 0; r < 8; ++r) v[r] = *reinterpret_cast<const uint2*>(tile + (8 * g + r) * 128 + cq * 8);
+        uint4 col[4];  // column 4cq + j, rows 8g .. 8g+7 (element e in half e of the words)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            uint32_t w[4];
+            uint32_t wd[4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int r = 32 * g + 8 * j + 2 * h;
-                w[h] = static_cast<uint32_t>(tile[r][c]) | (static_cast<uint32_t>(tile[r + 1][c]) << 16);
+            for (int p = 0; p < 4; ++p) {
+                const uint32_t a = j < 2 ? v[2 * p].x : v[2 * p].y;
+                const uint32_t b = j < 2 ? v[2 * p + 1].x : v[2 * p + 1].y;
+                wd[p] = __byte_perm(a, b, (j & 1) ? 0x7632 : 0x5410);
             }
-            v[j] = make_uint4(w[0], w[1], w[2], w[3]);
+            col[j] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
-        uint32_t amax2 = 0;
+        uint32_t am[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) amax2 = absmax_bits8(v[j], amax2);
-        pam[g][c] = amax2;
+        for (int j = 0; j < 4; ++j) {
+            am[j] = absmax_bits8(col[j], 0u);
+            am[j] = __vmaxu2(am[j], __shfl_xor_sync(0xffffffffu, am[j], 16));  // the warp's other row group
+        }
+        if (lane < 16) *reinterpret_cast<uint4*>(pam + w * kCqCols + 4 * cq) = make_uint4(am[0], am[1], am[2], am[3]);
         __syncthreads();
-        amax2 = __vmaxu2(__vmaxu2(pam[0][c], pam[1][c]), __vmaxu2(pam[2][c], pam[3][c]));
-        const float amax = bits_to_amax(amax2);
-        const GroupScale gs = group_scale(amax);
-        const bool zero = amax == 0.0f;
-        uint2 codes[4];
+        if (t < kCqCols) {  // column t: its amax over the eight warps, and its scale
+            uint32_t m2 = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) codes[j] = encode8(v[j], gs, zero);
-        const int64_t mrow = m0 + 32 * g;  // first token of this thread's 32 codes
-        uint8_t* out = xqt + (k0 + c) * ldt + mrow;
-        if (mrow + 32 <= M) {
-            *reinterpret_cast<uint4*>(out) = make_uint4(codes[0].x, codes[0].y, codes[1].x, codes[1].y);
-            *reinterpret_cast<uint4*>(out + 16) = make_uint4(codes[2].x, codes[2].y, codes[3].x, codes[3].y);
-        } else if (mrow < M) {  // the ragged last block: only the tokens that exist
-            const uint32_t wds[8] = {codes[0].x, codes[0].y, codes[1].x, codes[1].y,
-                                     codes[2].x, codes[2].y, codes[3].x, codes[3].y};
-            for (int b = 0; b < static_cast<int>(M - mrow); ++b) out[b] = static_cast<uint8_t>(wds[b / 4] >> (8 * (b % 4)));
+            for (int ww = 0; ww < 8; ++ww) m2 = __vmaxu2(m2, pam[ww * kCqCols + t]);
+            const float amax = bits_to_amax(m2);
+            const GroupScale gs = group_scale(amax);
+            gs_s[t] = gs.s;
+            gs_r[t] = gs.r;
+            gs_f[t] = static_cast<uint8_t>((gs.exact_div ? 1u : 0u) | (amax == 0.0f ? 2u : 0u));
+            sc[mb * ldsc + k0 + t] = gs.s;
         }
-        if (g == 0) sc[mb * ldsc + k0 + c] = gs.s;
+        __syncthreads();
+        const float4 s4 = *reinterpret_cast<const float4*>(gs_s + 4 * cq);
+        const float4 r4 = *reinterpret_cast<const float4*>(gs_r + 4 * cq);
+        const uint32_t f4 = *reinterpret_cast<const uint32_t*>(gs_f + 4 * cq);
+        const float sj[4] = {s4.x, s4.y, s4.z, s4.w};
+        const float rj[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t fl = f4 >> (8 * j);
+            const GroupScale gs{sj[j], rj[j], (fl & 1u) != 0u};
+            const uint2 codes = encode8(col[j], gs, (fl & 2u) != 0u);
+            const int c = 4 * cq + j;
+            *reinterpret_cast<uint2*>(stg + c * 128 + (((g >> 1) ^ (cq & 7)) * 16) + (g & 1) * 8) = codes;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int q = t + 256 * h;
+            const int c = q >> 3, chl = q & 7;  // channel k0 + c, tokens m0 + 16 chl .. +15
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + c * 128 + ((chl ^ ((c >> 2) & 7)) * 16));
+            const int64_t m = m0 + 16 * chl;
+            uint8_t* out = xqt + (k0 + c) * ldt + m;
+            if (m + 16 <= M) {
+                *reinterpret_cast<uint4*>(out) = val;
+            } else if (m < M) {  // the ragged last block: only the tokens that exist
+                const uint64_t lo = (static_cast<uint64_t>(val.y) << 32) | val.x;
+                const uint64_t hi = (static_cast<uint64_t>(val.w) << 32) | val.z;
+                for (int b = 0; b < static_cast<int>(M - m); ++b)
+                    out[b] = static_cast<uint8_t>(b < 8 ? lo >> (8 * b) : hi >> (8 * (b - 8)));
+            }
+        }
+        st = st == 2 ? 0 : st + 1;
     }
+    cp_async_wait<0>();  // only empty groups can remain; leave with none in flight
 }
 
 }  // namespace
@@ -374,10 +461,21 @@ cudaError_t launch_wait_selftest(uint64_t timeout_ns, const DeviceInfo& dev, cud
 
 cudaError_t launch_act_quant_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt, int64_t ldt,
                                   float* sc, int64_t ldsc, const DeviceInfo& dev, cudaStream_t stream) {
+    {
+        static bool ready[64];
+        if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+        if (!ready[dev.device]) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(act_quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCqSmem);
+            if (e != cudaSuccess) return e;
+            ready[dev.device] = true;
+        }
+    }
     const int64_t tiles = ((M + kCqRows - 1) / kCqRows) * (K / kCqCols);
-    const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 4;
+    const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 3;  // three 60 KB CTAs per SM
     const int blocks = static_cast<int>(tiles < max_blocks ? tiles : max_blocks);
-    return launch_pdl(act_quant_cols_kernel, dim3(blocks), dim3(256), 0, stream, x, M, K, ldx, xqt, ldt, sc, ldsc);
+    return launch_pdl(act_quant_cols_kernel, dim3(blocks), dim3(256), kCqSmem, stream, x, M, K, ldx, xqt, ldt, sc,
+                      ldsc);
 }
 
 }  // namespace fp8bs
