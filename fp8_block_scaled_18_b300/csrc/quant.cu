@@ -239,21 +239,21 @@ __global__ void wait_selftest_kernel(unsigned* err, uint64_t timeout_ns) {
 // weight-gradient GEMM contracts over).
 //
 // A CTA walks tiles of 128 rows x 64 columns (16 KB of bf16) through a
-// three-stage shared-memory ring filled with cp.async (16-byte copies; rows
-// past M are zero-filled, so they never raise the amax): two tiles are in
-// flight while a third is encoded.  Thread (cq, g) takes columns
-// 4cq .. 4cq+3 and rows 8g .. 8g+7: eight 8-byte shared loads bring its 32
-// values, byte permutes regroup them by column, each column's partial amax
-// is combined with the warp's other row group by one shuffle and left in
-// shared memory; one thread per column then finishes the amax over the
-// eight warps and forms the scale once, and every thread encodes its
-// columns' eight values with the act_quant codec.  The codes go to a 64 x 128-byte staging tile, one row per output
-// channel, its 16-byte chunks XOR-swizzled by the writer's column group so
-// that the 8-byte writes meet no bank conflict, and leave as whole 128-byte
-// rows of xqt.
+// two-stage shared-memory ring filled with cp.async (16-byte copies; rows
+// past M are zero-filled, so they never raise the amax): the next tile is in
+// flight while one is encoded, and four CTAs share an SM.  Thread (cq, g)
+// takes columns 4cq .. 4cq+3 and rows 8g .. 8g+7: eight 8-byte shared loads
+// bring its 32 values, byte permutes regroup them by column, each column's
+// partial amax is combined with the warp's other row group by one shuffle
+// and left in shared memory; one thread per column then finishes the amax
+// over the eight warps and forms the scale once, and every thread encodes
+// its columns' eight values with the act_quant codec.  The codes go to a
+// 64 x 128-byte staging tile, one row per output channel, its 16-byte
+// chunks XOR-swizzled by the writer's column group (a warp's writes spread
+// over all 32 banks), and leave as whole 128-byte rows of xqt.
 constexpr int kCqRows = 128;
 constexpr int kCqCols = 64;
-constexpr int kCqStages = 3;
+constexpr int kCqStages = 2;
 constexpr int kCqTileBytes = kCqRows * kCqCols * 2;        // 16 KB of bf16
 constexpr int kCqOutOff = kCqStages * kCqTileBytes;         // staging: 64 channels x 128 codes
 constexpr int kCqPamOff = kCqOutOff + kCqCols * kCqRows;    // per-warp column amaxes: 8 x 64 x 4 B
@@ -269,7 +269,7 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__global__ void __launch_bounds__(256, 3) act_quant_cols_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+__global__ void __launch_bounds__(256, 4) act_quant_cols_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                                int64_t ldx, uint8_t* __restrict__ xqt, int64_t ldt,
                                                                float* __restrict__ sc, int64_t ldsc) {
     extern __shared__ __align__(128) uint8_t cq_smem[];
@@ -324,18 +324,16 @@ __global__ void __launch_bounds__(256, 3) act_quant_cols_kernel(const uint16_t* 
     };
     TilePos cur{static_cast<int64_t>(blockIdx.x) / CB, static_cast<int64_t>(blockIdx.x) % CB};
     TilePos pre = cur;
-    advance(pre);
     issue(cur, 0);
-    issue(pre, 1);
-    advance(pre);  // two tiles ahead of cur from here on
-    int st = 0;    // stage of the current tile; this CTA's j-th tile sits in stage j % 3
+    advance(pre);  // one tile ahead of cur from here on
+    int st = 0;  // stage of the current tile: this CTA's j-th tile sits in stage j % 2
     for (; cur.mb < MB; advance(cur), advance(pre)) {
         const int64_t mb = cur.mb;
         const int64_t k0 = cur.cb * kCqCols;
         const int64_t m0 = mb * kCqRows;
-        cp_async_wait<1>();  // this thread's copies of the current tile have landed
+        cp_async_wait<0>();  // this thread's copies of the current tile have landed
         __syncthreads();     // and everyone's; the previous tile's shared reads are over
-        issue(pre, st == 0 ? 2 : st - 1);  // into the stage the previous tile used
+        issue(pre, st ^ 1);  // into the stage the previous tile used
 
         const uint8_t* tile = cq_smem + st * kCqTileBytes;
         uint2 v[8];  // row 8g + r, columns 4cq .. 4cq+3
@@ -403,9 +401,9 @@ __global__ void __launch_bounds__(256, 3) act_quant_cols_kernel(const uint16_t* 
                     out[b] = static_cast<uint8_t>(b < 8 ? lo >> (8 * b) : hi >> (8 * (b - 8)));
             }
         }
-        st = st == 2 ? 0 : st + 1;
+        st ^= 1;
     }
-    cp_async_wait<0>();  // only empty groups can remain; leave with none in flight
+    cp_async_wait<0>();  // only an empty group can remain; leave with none in flight
 }
 
 }  // namespace
@@ -472,7 +470,7 @@ cudaError_t launch_act_quant_cols(const uint16_t* x, int64_t M, int64_t K, int64
         }
     }
     const int64_t tiles = ((M + kCqRows - 1) / kCqRows) * (K / kCqCols);
-    const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 3;  // three 60 KB CTAs per SM
+    const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * 4;  // four 44 KB CTAs per SM
     const int blocks = static_cast<int>(tiles < max_blocks ? tiles : max_blocks);
     return launch_pdl(act_quant_cols_kernel, dim3(blocks), dim3(256), kCqSmem, stream, x, M, K, ldx, xqt, ldt, sc,
                       ldsc);

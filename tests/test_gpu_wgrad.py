@@ -54,6 +54,30 @@ def test_act_quant_cols_special_blocks(F, orc):
     _cols(F, orc, x)
 
 
+@pytest.mark.parametrize("M,K", [(333, 192), (16, 64)])
+def test_act_quant_cols_strided_padding_untouched(F, orc, M, K):
+    """x, xqt and sc as views with row strides wider than their rows: the
+    codes and scales land at their strides, and nothing past M tokens in a
+    code row (the ragged last block's tail) or past K in a scale row is
+    written."""
+    rng = np.random.default_rng(M * 7 + K)
+    x = synth.activations(rng, M, K, n_outlier=min(3, K // 64), outlier_scale=30.0)
+    xb = torch.zeros((M, K + 128), dtype=torch.bfloat16, device="cuda")
+    xb[:, :K] = dev_bf16(x)
+    ldt = (M + 15) // 16 * 16 + 48
+    xqt_buf = torch.full((K, ldt), 0x5A, dtype=torch.uint8, device="cuda")
+    sc_buf = torch.full(((M + 127) // 128, K + 8), -7.0, dtype=torch.float32, device="cuda")
+    xqt, sc = F.fp8bs_act_quant_cols(xb[:, :K], xqt=xqt_buf, sc=sc_buf[:, :K])
+    assert F.fp8bs_sync_status() == 0
+    xq_o, sc_o = orc.act_quant_cols(x)
+    got = host(xqt_buf)
+    assert_bits_equal(got[:, :M], np.ascontiguousarray(xq_o.T), f"codes {M}x{K}")
+    assert (got[:, M:] == 0x5A).all(), "code bytes past M written"
+    sc_h = host(sc_buf)
+    assert_bits_equal(np.ascontiguousarray(sc_h[:, :K]), sc_o, f"scales {M}x{K}")
+    assert (sc_h[:, K:] == -7.0).all(), "scales past K written"
+
+
 def _wgrad(F, orc, orc_mt, T, N, K, seed, rows=None):
     rng = np.random.default_rng(seed)
     dy = synth.activations(rng, T, N, n_outlier=4, outlier_scale=10.0)
