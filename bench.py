@@ -126,9 +126,17 @@ def sum_over_ranks(x: float, world: int, device: str = "cpu") -> float:
     return float(t.item())
 
 
-def kernel_sources_sha() -> str:
+# the sources each kernel with a committed DRAM-traffic capture is built from
+# (its own file, the shared PTX and codec headers, the launch declarations and
+# the tensor-map encoder): a change to any of them voids the capture
+KERNEL_SOURCES = {
+    "fp8_gemm": ("gemm.cu", "ptx.cuh", "codec.cuh", "internal.h", "tmap.cu"),
+}
+
+
+def kernel_sources_sha(kernel: str = "fp8_gemm") -> str:
     h = hashlib.sha256()
-    for name in ("quant.cu", "gemm.cu", "ptx.cuh", "codec.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "fp8_block_scaled_18_b300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -140,7 +148,9 @@ def ncu_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    sha = kernel_sources_sha()
+    if kernel not in KERNEL_SOURCES:
+        return None
+    sha = kernel_sources_sha(kernel)
     for line in open(path):
         if line.startswith("#") or not line.strip():
             continue

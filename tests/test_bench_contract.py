@@ -32,16 +32,15 @@ def test_reference_arm_line():
 def test_traffic_table_lookup():
     sys.path.insert(0, ROOT)
     import bench
-    sha = bench.kernel_sources_sha()
-    assert len(sha) == 16
-    # every committed capture is reported while the sources match it, else null
+    assert len(bench.kernel_sources_sha("fp8_gemm")) == 16
+    # every committed capture is reported while its kernel's sources match it, else null
     with open(os.path.join(ROOT, "profiles", "dram_traffic.txt")) as f:
         entries = [dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
                    for line in f if line.strip() and not line.startswith("#")]
     assert entries
     for kv in entries:
         t = bench.ncu_traffic(kv["kernel"], kv["workload"])
-        assert (t is not None) == (kv["src_sha"] == sha)
+        assert (t is not None) == (kv["src_sha"] == bench.kernel_sources_sha(kv["kernel"]))
         if t is not None:
             assert t == float(kv["dram_bytes_per_launch"])
     assert bench.ncu_traffic("no_such_kernel", "kv_down") is None
