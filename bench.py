@@ -8,7 +8,8 @@
 One step = one pass of the whole path over one batch of synthetic input:
 dense workloads run act_quant(X) and fp8_gemm with W quantised once before
 timing (the large square adds weight_dequant(Wq); q_down_m<M>_fused runs the
-GEMM with bias and FP8 output);
+GEMM with bias and FP8 output; <dense>_pow2 quantises both operands with
+power-of-two scales and times the fp32-scale quantisers beside them);
 moe runs act_quant over the expert-grouped token rows and the grouped
 fp8_gemm, moe_swiglu the grouped w1|w3 stage with SwiGLU and FP8 h, and
 moe_layer the whole routed layer with its router (expert weights quantised
@@ -64,8 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="large_square",
-                    help="large_square | kv_down | tiny | q_down_m<M>[_fused] | moe | moe_e<G> | moe_swiglu | moe_layer | moe_router | "
-                         "kv_down_wgrad | large_square_wgrad | q_down_m<M>_wgrad")
+                    help="large_square | kv_down | tiny | q_down_m<M>[_fused] | <dense>_pow2 | moe | moe_e<G> | moe_swiglu | "
+                         "moe_layer | moe_router | kv_down_wgrad | large_square_wgrad | q_down_m<M>_wgrad")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
@@ -219,9 +220,12 @@ class DenseWork:
     with W quantised once before timing (weight_quant is timed on its own as
     a table row).  fused: the GEMM is fp8bs_gemm_fused with a bias and the
     output re-quantised to FP8 (1x128 groups, ready for the next FP8 GEMM)
-    instead of bf16."""
+    instead of bf16.  pow2: both operands quantised with power-of-two
+    (UE8M0-style) scales (fp8bs_act_quant_pow2 in the step, W by
+    fp8bs_weight_quant_pow2), the fp32-scale quantisers timed beside them
+    into buffers of their own."""
 
-    def __init__(self, case, device, fused=False, min_sets=1):
+    def __init__(self, case, device, fused=False, min_sets=1, pow2=False):
         import torch
         from fp8_block_scaled_18_b300 import fp8bs as F
         self.F = F
@@ -238,6 +242,7 @@ class DenseWork:
         lds = max(4, (K // 128 + 3) // 4 * 4)
         ws_bytes = F.fp8bs_gemm_workspace_size(M, N, K)
         self.fused = fused
+        self.pow2 = pow2
         if fused:
             self.bias = torch.from_numpy(
                 np.random.default_rng(5).standard_normal(N).astype(np.float32)).to(torch.bfloat16).to(device)
@@ -256,6 +261,9 @@ class DenseWork:
                 s["sy"] = torch.empty((M, max(4, (N // 128 + 3) // 4 * 4)), dtype=torch.float32, device=device)
                 s["yq2"] = torch.empty((M, N), dtype=torch.uint8, device=device)
                 s["sy2"] = torch.empty((M, max(4, (N // 128 + 3) // 4 * 4)), dtype=torch.float32, device=device)
+            if pow2:  # outputs of the fp32-scale quantisers timed for comparison
+                for k in ("xq", "sx", "wq", "sw"):
+                    s[k + "_f32"] = torch.empty_like(s[k])
             self.sets.append(s)
         self.set_bytes = per_set
         self.gemm_launches = 2 if ws_bytes else 1
@@ -275,6 +283,18 @@ class DenseWork:
                                3.0 * N * K + 4.0 * nb * kb, "hbm"),
         }
         self.order = ["weight_quant", "act_quant", "fp8_gemm", "weight_dequant"]
+        if pow2:
+            self.kernels["weight_quant"] = (lambda s: F.fp8bs_weight_quant(s["w"], wq=s["wq_f32"], sw=s["sw_f32"]),
+                                            1, 3.0 * N * K + 4.0 * nb * kb, "hbm")
+            self.kernels["act_quant"] = (lambda s: F.fp8bs_act_quant(s["x"], xq=s["xq_f32"], sx=s["sx_f32"]), 1,
+                                         3.0 * M * K + 4.0 * M * kb, "hbm")
+            self.kernels["weight_quant_pow2"] = (
+                lambda s: F.fp8bs_weight_quant_pow2(s["w"], wq=s["wq"], sw=s["sw"]), 1, 3.0 * N * K + 4.0 * nb * kb,
+                "hbm")
+            self.kernels["act_quant_pow2"] = (lambda s: F.fp8bs_act_quant_pow2(s["x"], xq=s["xq"], sx=s["sx"]), 1,
+                                              3.0 * M * K + 4.0 * M * kb, "hbm")
+            self.order = ["weight_quant", "weight_quant_pow2", "act_quant", "act_quant_pow2", "fp8_gemm",
+                          "weight_dequant"]
         if fused:
             # the fused GEMM, and what it replaces: the plain GEMM plus act_quant over its output
             fused_bytes = gemm_bytes - 2.0 * M * N + 1.0 * M * N + 4.0 * M * (N // 128) + 2.0 * N
@@ -286,19 +306,20 @@ class DenseWork:
                                               3.0 * M * N + 4.0 * M * (N // 128), "hbm")
             self.order = ["weight_quant", "act_quant", "fp8_gemm_fused", "weight_dequant", "fp8_gemm",
                           "act_quant_of_y"]
-        self.step_kernels = ["act_quant", "fp8_gemm_fused" if fused else "fp8_gemm"]
+        self.step_kernels = ["act_quant_pow2" if pow2 else "act_quant", "fp8_gemm_fused" if fused else "fp8_gemm"]
         if self.dequant:
             self.step_kernels.append("weight_dequant")
 
     def prepare(self):
         """The weight as a checkpoint holds it: quantised once, before timing."""
+        quant = self.F.fp8bs_weight_quant_pow2 if self.pow2 else self.F.fp8bs_weight_quant
         for s in self.sets:
-            self.F.fp8bs_weight_quant(s["w"], wq=s["wq"], sw=s["sw"])
+            quant(s["w"], wq=s["wq"], sw=s["sw"])
 
     def step(self, i):
         s = self.sets[i % self.R]
         F = self.F
-        F.fp8bs_act_quant(s["x"], xq=s["xq"], sx=s["sx"])
+        (F.fp8bs_act_quant_pow2 if self.pow2 else F.fp8bs_act_quant)(s["x"], xq=s["xq"], sx=s["sx"])
         if self.fused:
             F.fp8bs_gemm_fused(s["xq"], s["sx"], s["wq"], s["sw"], bias=self.bias, want_y=False, want_fp8=True,
                                yq=s["yq"], sy=s["sy"])
@@ -336,11 +357,15 @@ class DenseWork:
         return slots
 
     def config(self):
-        step = "act_quant+" + ("fp8_gemm_fused(bias, fp8 out)" if self.fused else "fp8_gemm")
+        step = ("act_quant_pow2+" if self.pow2 else "act_quant+") + (
+            "fp8_gemm_fused(bias, fp8 out)" if self.fused else "fp8_gemm")
         if self.dequant:
             step += "+weight_dequant"
-        return {"workload": self.case.name + ("_fused" if self.fused else ""), "M": self.M, "N": self.N, "K": self.K,
-                "step": step + " (W quantised once before timing, as a checkpoint stores it)",
+        wq = "W quantised once before timing, as a checkpoint stores it"
+        if self.pow2:
+            wq = "power-of-two (UE8M0-style) scales on both operands; " + wq
+        return {"workload": self.case.name + ("_fused" if self.fused else "") + ("_pow2" if self.pow2 else ""),
+                "M": self.M, "N": self.N, "K": self.K, "step": f"{step} ({wq})",
                 "l2": f"inputs rotate over {self.R} buffer sets of {self.set_bytes / 1e6:.0f} MB (> 126 MB L2)"
                       if self.R > 1 else f"working set {self.set_bytes / 1e6:.0f} MB, larger than the 126 MB L2"}
 
@@ -764,6 +789,8 @@ def make_work(name: str, device):
         return DenseWork(synth.large_square(), device)
     if name.startswith("q_down_m") and name.endswith("_fused"):
         return DenseWork(synth.q_down(int(name[len("q_down_m"):-len("_fused")])), device, fused=True)
+    if name.endswith("_pow2"):
+        return DenseWork(make_case(name), device, pow2=True)
     if name.startswith("q_down_m"):
         return DenseWork(synth.q_down(int(name[len("q_down_m"):])), device)
     raise SystemExit(f"unknown workload {name}")
@@ -1059,11 +1086,12 @@ def run_ours(args, rank, local, world):
 
 # ---------------------------------------------------------------- oracle legs
 
-def oracle_sample_step(orc, case, rows, wq, sw):
-    """One bounded oracle pass over a dense case's step: act_quant(rows) +
-    gemm(rows) against the quantised W (+ weight_dequant of W for the large
-    square); returns the GEMM flops done."""
-    xq, sx = orc.act_quant(case.x[rows])
+def oracle_sample_step(orc, case, rows, wq, sw, pow2=False):
+    """One bounded oracle pass over a dense case's step: act_quant(rows) (with
+    power-of-two scales for pow2) + gemm(rows) against the quantised W
+    (+ weight_dequant of W for the large square); returns the GEMM flops
+    done."""
+    xq, sx = (orc.act_quant_pow2 if pow2 else orc.act_quant)(case.x[rows])
     orc.gemm(xq, sx, wq, sw)
     if case.name == "large_square":
         orc.weight_dequant(wq, sw)
@@ -1121,7 +1149,10 @@ def oracle_layer_rows(orc, case, wts, rows):
 
 
 def make_case(workload: str):
+    """The dense case of a workload name (a _pow2 suffix names the same case)."""
     from fp8_block_scaled_18_b300 import synth
+    if workload.endswith("_pow2"):
+        workload = workload[:-len("_pow2")]
     if workload == "kv_down":
         return synth.kv_down()
     if workload == "tiny":
@@ -1133,15 +1164,15 @@ def make_case(workload: str):
     raise SystemExit(f"unknown workload {workload}")
 
 
-def oracle_rows_for(orc, case, seconds: float, wq, sw) -> int:
+def oracle_rows_for(orc, case, seconds: float, wq, sw, pow2=False) -> int:
     """Rows of a dense case whose oracle pass takes about `seconds`
     (fixed weight-side cost + per-row GEMM cost, measured on 1 and 5 rows)."""
     M = case.x.shape[0]
     t0 = time.perf_counter()
-    oracle_sample_step(orc, case, np.array([0]), wq, sw)
+    oracle_sample_step(orc, case, np.array([0]), wq, sw, pow2)
     t1 = time.perf_counter() - t0
     t0 = time.perf_counter()
-    oracle_sample_step(orc, case, np.arange(5) % M, wq, sw)
+    oracle_sample_step(orc, case, np.arange(5) % M, wq, sw, pow2)
     t5 = time.perf_counter() - t0
     per_row = max((t5 - t1) / 4, 1e-4)
     fixed = max(t1 - per_row, 0.0)
@@ -1235,14 +1266,16 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
                   f"{'w1 and w3' if swiglu else 'weight'}, act_quant, gemm{' x2, silu(a) * b' if swiglu else ''}")
     else:
         case = make_case(workload)
+        pow2 = workload.endswith("_pow2")
         M = case.x.shape[0]
-        wq, sw = orc.weight_quant(case.w)  # untimed, as the GPU arm quantises W before timing
-        rows = oracle_rows_for(orc, case, seconds, wq, sw)
+        # untimed, as the GPU arm quantises W before timing
+        wq, sw = (orc.weight_quant_pow2 if pow2 else orc.weight_quant)(case.w)
+        rows = oracle_rows_for(orc, case, seconds, wq, sw, pow2)
         sel = np.linspace(0, M - 1, rows).astype(np.int64)
         t0 = time.perf_counter()
-        flops = oracle_sample_step(orc, case, sel, wq, sw)
+        flops = oracle_sample_step(orc, case, sel, wq, sw, pow2)
         dt = time.perf_counter() - t0
-        sample = (f"{rows} of {M} rows: act_quant(rows) + gemm(rows)"
+        sample = (f"{rows} of {M} rows: act_quant{'_pow2' if pow2 else ''}(rows) + gemm(rows)"
                   + (" + weight_dequant(W)" if case.name == "large_square" else "")
                   + ", W quantised before timing; TFLOP/s over the sampled GEMM work")
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "host_cores_available": cpu_cores(),
@@ -1368,10 +1401,11 @@ def run_reference(args, rank, local, world):
         cfg = {"workload": "moe_swiglu" if swiglu else "moe_grouped"}
     else:
         case = make_case(args.workload)
+        pow2 = args.workload.endswith("_pow2")
         M, N, Kd = case.x.shape[0], case.w.shape[0], case.x.shape[1]
         nblk = (N + 127) // 128
         # set-up, untimed: the quantised weight the sampled GEMM rows use
-        wq_all, sw_all = orc.weight_quant(case.w)
+        wq_all, sw_all = (orc.weight_quant_pow2 if pow2 else orc.weight_quant)(case.w)
 
         dequant = case.name == "large_square"
 
@@ -1383,7 +1417,7 @@ def run_reference(args, rank, local, world):
                 b = i % nblk
                 orc.weight_dequant(wq_all[128 * b:128 * (b + 1)], sw_all[b:b + 1])
             rs = (np.arange(rows) + i * rows) % M
-            xq, sx = orc.act_quant(case.x[rs])
+            xq, sx = (orc.act_quant_pow2 if pow2 else orc.act_quant)(case.x[rs])
             orc.gemm(xq, sx, wq_all, sw_all)
             return 2.0 * rows * N * Kd
 
@@ -1399,10 +1433,11 @@ def run_reference(args, rank, local, world):
         rows = int(max(1, min(M, (budget / (K + W) - fixed) / per_row)))
         step_fn = step
         step = lambda i: step_fn(i, rows)  # noqa: E731
-        sample = (f"{rows} of {M} rows per step: act_quant(rows), gemm(rows) against the whole quantised W"
+        sample = (f"{rows} of {M} rows per step: act_quant{'_pow2' if pow2 else ''}(rows), gemm(rows) against "
+                  f"the whole quantised W"
                   + (", weight_dequant of one 128-row block of W (rotating)" if dequant else ""))
         M_, N_, K_ = case.shape
-        cfg = {"workload": case.name, "M": M_, "N": N_, "K": K_}
+        cfg = {"workload": case.name + ("_pow2" if pow2 else ""), "M": M_, "N": N_, "K": K_}
     for i in range(W):
         step(i)
     t0 = time.perf_counter()

@@ -1,5 +1,6 @@
 """The JSON line bench.py prints, checked on the CPU where it can run there:
-the reference arm (the oracle on the host cores) on the tiny workload, and
+the reference arm (the oracle on the host cores) on the tiny workload, with
+fp32 and with power-of-two scales, and
 the committed DRAM-traffic table's lookup."""
 import json
 import os
@@ -12,8 +13,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.mark.skipif(not os.path.exists(os.path.join(ROOT, "oracle", "oracle.c")), reason="no oracle")
-def test_reference_arm_line():
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "2",
+@pytest.mark.parametrize("workload", ["tiny", "tiny_pow2"])
+def test_reference_arm_line(workload):
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", workload, "--steps", "2",
                         "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
@@ -26,7 +28,9 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    assert d["config"]["workload"] == "tiny"
+    assert d["config"]["workload"] == workload
+    if workload.endswith("_pow2"):
+        assert "act_quant_pow2" in d["cpu_baseline"]["sample"]
 
 
 def test_traffic_table_lookup():
